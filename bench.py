@@ -1,0 +1,436 @@
+#!/usr/bin/env python
+"""Benchmark of the Periodic Row-wise Muon optimizer step on synthetic
+DiT-shaped matrix sets, one GB300.
+
+A "step" here is one K=3 PR-Muon cycle over the whole matrix set: the NS5
+refresh at t = 3k and the two RowNorm steps at t = 3k+1, 3k+2 (every row of
+the hot path: momentum, branch choice, RowNorm, NS5 prep / rounds / output,
+parameter update). The headline value is milliseconds per cycle (lower is
+better) with all state resident in HBM; `e2e` repeats the measurement through
+the public API with the gradients copied in from pinned host memory every
+optimizer step and a small result read back. Inputs (22 GB per optimizer
+step on the 1.3B set) are far larger than L2, so no flush is needed.
+
+  python bench.py [--steps K] [--warmup W] [--workload dit_1p3b|dit_15b|dit_1p3b_muonbp]
+  python bench.py --impl reference   # the fp64 CPU oracle on a bounded sample
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "ms per K=3 PR-Muon cycle (1.3B/15B DiT shapes); NS5 TFLOP/s; RowNorm GB/s"
+UNIT = "ms/cycle"
+BASELINE_VALUE = None  # the pages publish no single-GPU number for this metric
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=10, help="timed K=3 cycles")
+    p.add_argument("--warmup", type=int, default=3, help="untimed K=3 cycles")
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", default="dit_1p3b", choices=["dit_1p3b", "dit_15b", "dit_1p3b_muonbp"])
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    return p.parse_args()
+
+
+# ------------------------------------------------------------------ helpers
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self._t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self._t = threading.Thread(target=self._read, daemon=True)
+        self._t.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        if self._t:
+            self._t.join(timeout=2)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ oracle timing
+def oracle_cycle_estimate(ms, size: str):
+    """Times the fp64 oracle on a bounded sample of one K=3 cycle and scales
+    it to the whole matrix set. Returns (ms_per_cycle, sample_text, seconds)."""
+    import numpy as np
+    import torch
+
+    import oracle as O
+    from matrix_aware_optimizer_gb300 import synth
+
+    counts = {}
+    for s in ms.shapes:
+        counts[s] = counts.get(s, 0) + 1
+    shapes = list(counts)
+    t_start = time.perf_counter()
+    total_ms = 0.0
+    if size == "large":
+        # NS5 on one full matrix of every shape (extrapolated by FLOPs only for
+        # shapes whose fp64 cost would exceed the budget), RowNorm on the
+        # full matrix of every shape.
+        ns_ref = None
+        for s in shapes:
+            m, n = s
+            r, c = min(m, n), max(m, n)
+            W = synth.make_param(s, 0, 0).double().numpy()
+            G = synth.make_grad(s, 0, 0, 0, ms.grad_std, ms.grad_dtype).double().numpy()
+            M = np.zeros(s)
+            flops = 5 * (4 * r * r * c + 2 * r ** 3)
+            t0 = time.perf_counter()
+            O.prmuon_step(W, M, G, 1, ms.K, ms.gamma, ms.lr, ms.wd, ms.beta, ms.eps)
+            t_rn = time.perf_counter() - t0
+            if flops <= 1.2e12 or ns_ref is None:
+                t0 = time.perf_counter()
+                O.prmuon_step(W, M, G, 0, ms.K, ms.gamma, ms.lr, ms.wd, ms.beta, ms.eps)
+                t_ns = time.perf_counter() - t0
+                ns_ref = (t_ns, flops)
+            else:
+                t_ns = ns_ref[0] * flops / ns_ref[1]
+            total_ms += counts[s] * (t_ns + 2 * t_rn) * 1e3
+        sample = ("one K=3 cycle (NS5 refresh + 2 RowNorm steps) on one full matrix of each of the "
+                  f"{len(shapes)} shapes, scaled by the shape counts; NS5 of shapes above 1.2 TFLOP "
+                  "extrapolated by FLOP count")
+    else:
+        # NS5 on the smallest shape's r x r square only, RowNorm on 256 rows /
+        # columns of every shape; both scaled (FLOPs, parameters).
+        r0 = min(min(s) for s in shapes)
+        rng = np.random.default_rng(0)
+        X = rng.standard_normal((r0, r0))
+        t0 = time.perf_counter()
+        O.newton_schulz(X)
+        t_ns_ref = time.perf_counter() - t0
+        flops_ref = 5 * (4 * r0 ** 3 + 2 * r0 ** 3)
+        for s in shapes:
+            m, n = s
+            r, c = min(m, n), max(m, n)
+            flops = 5 * (4 * r * r * c + 2 * r ** 3)
+            sub = (256, n) if m <= n else (m, 256)
+            G = rng.standard_normal(sub)
+            t0 = time.perf_counter()
+            O.prmuon_step(np.zeros(sub), np.zeros(sub), G, 1, ms.K, ms.gamma, ms.lr, ms.wd, ms.beta, ms.eps)
+            t_rn = (time.perf_counter() - t0) * (m * n) / (sub[0] * sub[1])
+            t_ns = t_ns_ref * flops / flops_ref
+            total_ms += counts[s] * (t_ns + 2 * t_rn) * 1e3
+        sample = (f"NS5 on one {r0}x{r0} matrix scaled by FLOP count to every shape, RowNorm on 256 "
+                  "short-side vectors of each shape scaled by parameter count; one K=3 cycle")
+    return total_ms, sample, time.perf_counter() - t_start
+
+
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+# ------------------------------------------------------------------ reference arm
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    from matrix_aware_optimizer_gb300 import synth
+    ms = synth.MATRIX_SETS[args.workload]
+    for _ in range(args.warmup):
+        oracle_cycle_estimate(ms, "small")
+    vals, wall = [], 0.0
+    sample = ""
+    for _ in range(args.steps):
+        v, sample, secs = oracle_cycle_estimate(ms, "small")
+        vals.append(v)
+        wall += secs
+    value = sum(vals) / len(vals)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": value, "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": args.workload, "matrices": len(ms.shapes), "params": ms.params, "K": ms.K},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": host_cores(), "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "wall_s": wall,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------ our arm
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    from matrix_aware_optimizer_gb300 import build as _build
+    from matrix_aware_optimizer_gb300 import native as N
+    from matrix_aware_optimizer_gb300 import synth
+    from matrix_aware_optimizer_gb300.optimizer import PeriodicRowMuon
+
+    world, rank, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU: the optimizer has no CPU path")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    _build.build_library()
+    N.load()
+
+    ms = synth.MATRIX_SETS[args.workload]
+    mode = ms.mode
+    blocks = ms.blocks
+    hp = dict(K=ms.K, gamma=ms.gamma, lr=ms.lr, wd=ms.wd, beta=ms.beta, eps=ms.eps)
+    gdt = torch.bfloat16 if ms.grad_dtype == synth.GRAD_BF16 else torch.float32
+
+    # state and one gradient set, generated on the device from the seeded recipe
+    Ws, Ms = synth.make_state(ms, device=dev)
+    grads = []
+    for i, s in enumerate(ms.shapes):
+        g = torch.empty(s, device=dev, dtype=gdt)
+        synth.make_grad(s, ms.seed, 0, i, ms.grad_std, ms.grad_dtype, ms.row_sigma, device=dev, out=g)
+        grads.append(g)
+    torch.cuda.synchronize()
+    opt = PeriodicRowMuon(Ws, Ms, grads, muonbp_blocks=blocks)
+    stream = torch.cuda.current_stream()
+
+    def cycle(k, ev_ref=None):
+        for j in range(ms.K):
+            t = k * ms.K + j
+            if ev_ref is not None:
+                ev_ref[j][0].record(stream)
+            opt.step(t, mode=mode, **hp)
+            if ev_ref is not None:
+                ev_ref[j][1].record(stream)
+
+    for k in range(args.warmup):
+        cycle(k)
+    opt.sync_status()
+
+    # ---- timed region (device-resident inputs)
+    per = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(ms.K)]
+           for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    N.prm_profile(opt.ctx, True)
+    clocks = ClockSampler(local)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    t_start.record(stream)
+    for k in range(args.steps):
+        cycle(args.warmup + k, per[k])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    N.prm_profile(opt.ctx, False)
+    opt.sync_status()
+    total_ms = t_start.elapsed_time(t_end)
+    if world > 1:
+        tt = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        total_ms = tt.item()
+    ms_cycle = total_ms / args.steps
+    step_ms = [[per[k][j][0].elapsed_time(per[k][j][1]) for j in range(ms.K)] for k in range(args.steps)]
+    refresh_ms = statistics.mean(r[0] for r in step_ms)
+    cheap_ms = statistics.mean(x for r in step_ms for x in r[1:]) if ms.K > 1 else 0.0
+
+    fam = {}
+    launches = 0
+    for f, name in enumerate(N.FAMILY_NAMES):
+        tms, recs, kern, work = N.prm_profile_read(opt.ctx, f)
+        fam[name] = dict(ms=tms, records=recs, kernels=kern, work=work)
+        launches += kern
+
+    peaks, peak_src = load_peaks()
+    hbm = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
+    tf_sus = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
+    traffic = load_traffic()
+
+    def roof(name):
+        d = fam[name]
+        if d["records"] == 0 or d["ms"] <= 0:
+            return None
+        tensor = name in ("ns_gram", "ns_poly", "ns_combine")
+        if tensor:
+            ach = d["work"] / (d["ms"] * 1e-3) / 1e12
+            peak, unit = tf_sus, "TFLOP/s"
+        else:
+            ach = d["work"] / (d["ms"] * 1e-3) / 1e9
+            peak, unit = hbm, "GB/s"
+        tr = traffic.get(name)
+        return {"kernel": name, "bound": "tensor" if tensor else "hbm", "achieved": round(ach, 1),
+                "peak": peak, "unit": unit, "frac": round(ach / peak, 4),
+                "traffic": tr, "peak_source": f"{peak_src} ({'sustained bf16' if tensor else 'copy'})",
+                "avg_launch_ms": round(d["ms"] / d["records"], 4), "launches": d["records"],
+                "share_of_timed": round(d["ms"] / total_ms, 4)}
+
+    top = max(fam, key=lambda k: fam[k]["ms"])
+    ns_ms = sum(fam[k]["ms"] for k in ("ns_gram", "ns_poly", "ns_combine"))
+    ns_flop = sum(fam[k]["work"] for k in ("ns_gram", "ns_poly", "ns_combine"))
+    rn_ms = fam["rownorm_wide"]["ms"] + fam["rownorm_tall"]["ms"]
+    rn_bytes = fam["rownorm_wide"]["work"] + fam["rownorm_tall"]["work"]
+
+    # ---- end to end through the public API: pinned host grads in, a row out
+    e2e = None
+    if not args.no_e2e:
+        host = [g.cpu().pin_memory() for g in grads]
+        h2d = sum(h.numel() * h.element_size() for h in host)
+        out_row = torch.empty(ms.shapes[0][1], dtype=torch.float32).pin_memory()
+        d2h = out_row.numel() * 4
+        for k in range(2):
+            for j in range(ms.K):
+                for g, h in zip(grads, host):
+                    g.copy_(h, non_blocking=True)
+                opt.step(k * ms.K + j, mode=mode, **hp)
+                out_row.copy_(Ws[0][0], non_blocking=True)
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for k in range(args.steps):
+            for j in range(ms.K):
+                for g, h in zip(grads, host):
+                    g.copy_(h, non_blocking=True)
+                opt.step((args.warmup + args.steps + k) * ms.K + j, mode=mode, **hp)
+                out_row.copy_(Ws[0][0], non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = e0.elapsed_time(e1) / args.steps
+        if world > 1:
+            tt = torch.tensor([e2e_ms], device=dev)
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+            e2e_ms = tt.item()
+        e2e = {"value": round(e2e_ms, 3), "unit": UNIT, "h2d_bytes_per_step": h2d * ms.K,
+               "d2h_bytes_per_step": d2h * ms.K}
+        opt.sync_status()
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, sample, _ = oracle_cycle_estimate(ms, "large")
+        cpu = {"value": round(v, 1), "unit": UNIT, "cores": host_cores(), "kind": "oracle", "sample": sample}
+
+    n_params = ms.params
+    line = {
+        "metric": METRIC, "value": round(ms_cycle, 3), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_cycle, 3), "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32 state, bf16 x bf16 -> f32 NS5", "data": "synthetic",
+        "config": {"workload": args.workload, "matrices": len(ms.shapes), "params": n_params, "K": ms.K,
+                   "gamma": ms.gamma, "lr": ms.lr, "wd": ms.wd, "beta": ms.beta, "mode": mode,
+                   "muonbp_blocks": blocks, "grad_dtype": ms.grad_dtype,
+                   "l2": "inputs larger than L2 (no flush)", "parallelism": f"replicas x{world}",
+                   "step": "one K=3 cycle: refresh + 2 cheap steps"},
+        "ms_refresh_step": round(refresh_ms, 3), "ms_cheap_step": round(cheap_ms, 3),
+        "ns5_tflops": round(ns_flop / (ns_ms * 1e-3) / 1e12, 1) if ns_ms else None,
+        "rownorm_gbs": round(rn_bytes / (rn_ms * 1e-3) / 1e9, 1) if rn_ms else None,
+        "roofline": roof(top),
+        "roofline_kernels": {k: roof(k) for k in fam if fam[k]["records"]},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": launches,
+        "clocks": clk,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    opt.close()
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def load_traffic():
+    """Per-launch DRAM bytes of each kernel family from the committed ncu
+    summary, if it was taken on the current kernel sources."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+    except Exception:
+        return {}
+    from matrix_aware_optimizer_gb300.build import source_digest
+    if d.get("source_digest") != source_digest():
+        return {}
+    return {k: v.get("dram_bytes_per_launch") for k, v in d.get("kernels", {}).items()}
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

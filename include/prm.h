@@ -1,0 +1,222 @@
+/*
+ * prm.h -- C ABI of libprm: the Periodic Row-wise Muon (PR-Muon) and MuonBP
+ * optimizer step for the 2-D weight matrices of a model, on one GB300 GPU.
+ *
+ * Method sources (cited by title and section):
+ *   [SMDiT]  "Scaling Muon for Diffusion Transformers": abstract, and the
+ *            PaperDaily walkthrough of it -- section "Periodic Row-wise Muon"
+ *            (Fig. 3 update rule with refresh indicator rho_t, Fig. 4 RowNorm
+ *            R_eps), section "Distributed co-design" (Fig. 8 column statistics
+ *            of tall matrices) and the cost note (NS5 Theta(5 r^2 c)).
+ *   [MuonBP] "MuonBP: Faster Muon via Block-Periodic Orthogonalization",
+ *            abstract (blockwise orthogonalisation, periodic full
+ *            orthogonalisation, two step sizes).
+ *
+ * Conventions for every call:
+ *   - Return value: PRM_OK (0) or one of the PRM_ERR_* codes below; no call
+ *     throws, aborts or prints. prm_last_error() gives a one-line reason.
+ *   - "device" pointers are CUDA global-memory addresses on the context's
+ *     device; "host" pointers are ordinary CPU memory.
+ *   - Ownership: the caller owns every tensor and the workspace. The library
+ *     keeps non-owning pointers from prm_register_matrices / prm_set_workspace
+ *     until the next registration or prm_destroy.
+ *   - Streams are passed as `void*` holding a cudaStream_t (NULL = legacy
+ *     default stream). Work is enqueued asynchronously; argument errors are
+ *     returned at once, asynchronous CUDA errors on a later call or from
+ *     prm_sync_status().
+ *   - One context per stream; a context is not thread-safe.
+ */
+#ifndef PRM_H
+#define PRM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define PRM_API __attribute__((visibility("default")))
+#else
+#define PRM_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ---------------------------------------------------- */
+#define PRM_OK                 0
+#define PRM_ERR_INVALID_ARG    1  /* null pointer, K < 1, t < 0, eps <= 0, beta outside [0,1), ... */
+#define PRM_ERR_SHAPE          2  /* rows/cols < 1, MuonBP long side < blocks, pitch < cols */
+#define PRM_ERR_ALIGNMENT      3  /* a pointer is not 16-byte aligned */
+#define PRM_ERR_NOT_REGISTERED 4  /* step before prm_register_matrices / prm_set_workspace */
+#define PRM_ERR_CUDA           5  /* a CUDA runtime or driver call failed */
+#define PRM_ERR_TIMEOUT        6  /* a device-side bounded wait gave up (error word set) */
+#define PRM_ERR_OOM            7  /* host allocation failed */
+#define PRM_ERR_WORKSPACE      8  /* workspace missing or smaller than prm_workspace_bytes() */
+#define PRM_ERR_UNSUPPORTED    9  /* no sm_100-family device, or a size beyond a kernel limit */
+
+/* ---- enums ------------------------------------------------------------ */
+#define PRM_FP32 0   /* gradient element type: float32 */
+#define PRM_BF16 1   /* gradient element type: bfloat16 */
+
+#define PRM_MODE_PRMUON 0   /* [SMDiT] Fig. 3: NS5 when t % K == 0, else gamma * R_eps */
+#define PRM_MODE_MUONBP 1   /* [MuonBP]: full NS5 when t % K == 0, else NS5 per block */
+
+typedef struct prm_ctx prm_ctx;
+
+/* One 2-D weight matrix, stored row-major with rows x cols elements.
+ *   param     float32, device, read and written in place (W).
+ *   momentum  float32, device, read and written in place (M); starts at zero
+ *             for a fresh run; together with t it is the whole optimizer state.
+ *   grad      device, read only (G), element type grad_dtype.
+ *   rows/cols m and n, both >= 1. m <= n is "wide" (rows are the short-side
+ *             vectors), m > n is "tall" (columns are).
+ *   shape_scale  per-matrix multiplier of the step size; <= 0 selects the
+ *             default sqrt(max(1, rows / cols)).
+ * All three pointers must be 16-byte aligned. */
+typedef struct {
+  float*      param;
+  float*      momentum;
+  const void* grad;
+  int32_t     grad_dtype;
+  int32_t     reserved;    /* must be 0 */
+  int64_t     rows;
+  int64_t     cols;
+  float       shape_scale;
+  float       reserved2;   /* must be 0 */
+} prm_matrix_desc;
+
+/* Creates a context bound to CUDA device `cuda_device` (must be compute
+ * capability 10.3, sm_103a). *out receives the handle; free it with
+ * prm_destroy. Errors: INVALID_ARG (out NULL), CUDA, UNSUPPORTED, OOM. */
+PRM_API int prm_create(prm_ctx** out, int cuda_device);
+
+/* Releases the context and its internal device tables. Never frees caller
+ * buffers (tensors or workspace). NULL is accepted and ignored. */
+PRM_API int prm_destroy(prm_ctx* ctx);
+
+/* Registers `count` matrices (count >= 0; 0 clears the registration) and
+ * plans the step: RowNorm launch groups by exact shape, NS5 groups by the
+ * wide orientation r x c (tall matrices are orthogonalised transposed, as the
+ * cost Theta(5 r^2 c) of [SMDiT]'s cost note implies), and -- when
+ * muonbp_blocks = P > 0 -- the [MuonBP] blocks: P contiguous pieces along each
+ * matrix's long side, the last taking the remainder. muonbp_blocks = 0
+ * disables MuonBP mode for this registration.
+ * The descriptor array is copied (host memory, read only).
+ * Errors: INVALID_ARG, SHAPE, ALIGNMENT, CUDA, OOM. */
+PRM_API int prm_register_matrices(prm_ctx* ctx, const prm_matrix_desc* descs, int count,
+                          int muonbp_blocks);
+
+/* Bytes of device scratch the registered plan needs (NS5 operands in bf16,
+ * Gram / polynomial matrices, norm and column partial sums). *bytes (host)
+ * receives the size; 0 when nothing is registered. */
+PRM_API int prm_workspace_bytes(const prm_ctx* ctx, size_t* bytes);
+
+/* Hands the library a caller-allocated device buffer of `bytes` bytes,
+ * 256-byte aligned, at least prm_workspace_bytes(). Its contents need not be
+ * initialised and are overwritten by every step. Errors: INVALID_ARG,
+ * ALIGNMENT, WORKSPACE. */
+PRM_API int prm_set_workspace(prm_ctx* ctx, void* dev_ptr, size_t bytes);
+
+/* One optimizer step at index t over every registered matrix, enqueued on
+ * `stream`:
+ *   M <- beta * M + G                              (momentum)
+ *   PRM_MODE_PRMUON ([SMDiT] Fig. 3 / Fig. 4):
+ *     t % K == 0: D = NS5(M), eta = lr
+ *     otherwise : D = R_eps(M), each short-side vector divided by
+ *                 max(||v||_2, eps), eta = lr * gamma
+ *   PRM_MODE_MUONBP ([MuonBP]): t % K == 0: D = NS5(M), eta = lr;
+ *                 otherwise D = NS5 of each block on its own, eta = lr * gamma
+ *   W <- W * (1 - lr * wd) - eta * s * D           (decoupled weight decay)
+ * NS5: X = M / (||M||_F + 1e-7) (transposed if tall), then five rounds of
+ * A = X X^T, B = b A + c A A, X <- a X + B X, in bf16 operands with fp32
+ * accumulation. ns_coeffs (host, 3 floats: a, b, c) may be NULL for the
+ * default quintic (3.4445, -4.7750, 2.0315) -- the pages print no
+ * coefficients, so this default is a stated choice.
+ * Preconditions: t >= 0, K >= 1 (K = 1 is vanilla Muon), 0 <= beta < 1,
+ * eps > 0, finite lr / wd / gamma. Errors: INVALID_ARG, NOT_REGISTERED,
+ * WORKSPACE, CUDA (launch failures). A device-side wait that gave up is
+ * reported by prm_sync_status(), not here (reading it needs a sync). */
+PRM_API int prm_step(prm_ctx* ctx, int64_t t, int K, float gamma, float lr, float wd, float beta,
+             float eps, const float* ns_coeffs, int mode, void* stream);
+
+/* Pure helper: 1 if step t takes the refresh / full-NS5 branch, 0 if it takes
+ * the RowNorm / block branch ([SMDiT] Fig. 3 refresh indicator; the same rule
+ * in both modes). Returns -PRM_ERR_INVALID_ARG for t < 0, K < 1 or an unknown
+ * mode. */
+PRM_API int prm_branch(int64_t t, int K, int mode);
+
+/* Synchronises `stream` and reads the device error word that bounded waits
+ * inside the NS5 kernels set when they give up. Returns PRM_OK, TIMEOUT or
+ * CUDA; clears the word. */
+PRM_API int prm_sync_status(prm_ctx* ctx, void* stream);
+
+/* ---- kernel timing (benchmarks) --------------------------------------
+ * When enabled, every kernel family launched by prm_step is bracketed by a
+ * pair of CUDA events recorded on the launching stream, and its algorithmic
+ * work is accumulated: dense bf16 FLOPs for the GEMM families (2 r^2 c for
+ * GRAM and COMBINE, 2 r^3 for POLY per matrix), bytes for the memory-bound
+ * ones (RowNorm 18 B per parameter with bf16 gradients, 20 B with fp32;
+ * prep 12 / 14 B; apply 10 B). Families: */
+#define PRM_FAMILY_ROWNORM_WIDE 0
+#define PRM_FAMILY_ROWNORM_TALL 1
+#define PRM_FAMILY_NS_PREP      2
+#define PRM_FAMILY_NS_GRAM      3
+#define PRM_FAMILY_NS_POLY      4
+#define PRM_FAMILY_NS_COMBINE   5
+#define PRM_FAMILY_NS_APPLY     6
+#define PRM_FAMILY_COUNT        7
+
+/* enable = 1 clears the records and starts recording; 0 stops. */
+PRM_API int prm_profile(prm_ctx* ctx, int enable);
+
+/* Totals since the last prm_profile(ctx, 1) for one family (or -1 for all):
+ * *total_ms summed event time, *records bracketed launches of that family,
+ * *kernels individual kernel launches inside them, *work the algorithmic
+ * FLOPs or bytes. Waits for the recorded events (host-blocking). */
+PRM_API int prm_profile_read(prm_ctx* ctx, int family, double* total_ms, int64_t* records,
+                             int64_t* kernels, double* work);
+
+/* Last error message of this context (or of the last failed prm_create when
+ * ctx is NULL). Never NULL; owned by the library. */
+PRM_API const char* prm_last_error(const prm_ctx* ctx);
+
+/* ---- standalone building blocks ---------------------------------------
+ * The stages of NS5 on caller buffers, for users who want the orthogonaliser
+ * without the optimizer state, and for kernel-level tests. A batch holds
+ * `batch` matrices of r x c (r <= c) bf16 values stored row-major with row
+ * pitch `ldc` elements (ldc >= c, ldc % 8 == 0), matrix i at offset
+ * i * r * ldc; r x r matrices use pitch `ldr` (ldr >= r, ldr % 8 == 0).
+ * All pointers are device, 16-byte aligned; bf16 values are passed as
+ * uint16_t bit patterns. `scale` (device, batch floats) may be NULL for 1.
+ * [SMDiT] section "Periodic Row-wise Muon": one NS5 round is
+ * A = X X^T, B = b A + c A A, X' = a X + B X. */
+
+/* A[i] = scale[i]^2 * X[i] X[i]^T  (symmetric; tensor cores, tcgen05). */
+PRM_API int prm_ns_gram(const uint16_t* X, uint16_t* A, const float* scale, int batch, int64_t r,
+                int64_t c, int64_t ldc, int64_t ldr, void* stream);
+
+/* B[i] = b * A[i] + c * A[i] A[i]   (A symmetric). */
+PRM_API int prm_ns_poly(const uint16_t* A, uint16_t* B, float b, float c, int batch, int64_t r,
+                int64_t ldr, void* stream);
+
+/* Xout[i] = scale[i] * (a * X[i] + B[i] X[i])  (Xout must not alias X). */
+PRM_API int prm_ns_combine(const uint16_t* X, const uint16_t* B, uint16_t* Xout, const float* scale,
+                   float a, int batch, int64_t r, int64_t c, int64_t ldc, int64_t ldr,
+                   void* stream);
+
+/* Bytes of workspace prm_newton_schulz needs for `batch` matrices of m x n. */
+PRM_API int prm_newton_schulz_workspace(int batch, int64_t m, int64_t n, size_t* bytes);
+
+/* out[i] = NS_steps(in[i]) for `batch` fp32 matrices of m x n (row-major,
+ * contiguous, device), tall inputs orthogonalised transposed; the result is
+ * fp32. steps >= 1, ns_coeffs NULL for the default quintic. The call
+ * synchronises `stream` before returning (its launch tables are freed). */
+PRM_API int prm_newton_schulz(const float* in, float* out, int batch, int64_t m, int64_t n,
+                      const float* ns_coeffs, int steps, void* workspace, size_t ws_bytes,
+                      void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PRM_H */

@@ -1,0 +1,108 @@
+// Declarations shared by the library's translation units: matrix views, the
+// kernel launchers and the tensor-map encoder.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace prm {
+
+// A row-major m x n view into caller memory with row pitch `ld` elements (a
+// whole matrix has ld == cols; a MuonBP block of a wide matrix has the
+// parent's pitch). W and M are fp32; G is fp32 or bf16.
+struct View {
+  float* W;
+  float* M;
+  const void* G;
+  int64_t rows;
+  int64_t cols;
+  int64_t ld;
+  int32_t grad_bf16;
+  float shape_scale;
+  int32_t slot;     // index of this view inside its NS5 group (batch index)
+  int32_t pad;
+  float* out;       // standalone orthogonaliser only (W == nullptr): D is written here
+};
+
+// Per-step scalars shared by every kernel of one step.
+struct StepScalars {
+  float beta;     // momentum coefficient
+  float decay;    // 1 - lr * wd
+  float eta;      // step size of this branch: lr, or lr * gamma
+  float eps;      // RowNorm threshold
+};
+
+// ---- RowNorm step (non-refresh branch) --------------------------------
+// Fused wide step: one CTA per row, grid (rows, count). All views share
+// rows/cols. Returns a cudaError_t from the launch.
+cudaError_t launch_rownorm_wide(const View* d_views, int count, int64_t rows, int64_t cols, bool vec_ok,
+                                bool grad_bf16, StepScalars s, cudaStream_t stream);
+
+// Tall step in three launches: column partial sums, per-column inverse
+// norms, update. `partials` holds count * row_blocks(rows) * cols floats and
+// `inv` count * cols floats.
+int64_t tall_row_blocks(int64_t rows);
+cudaError_t launch_rownorm_tall(const View* d_views, int count, int64_t rows, int64_t cols, bool vec_ok,
+                                bool grad_bf16, StepScalars s, float* partials, float* inv,
+                                cudaStream_t stream);
+
+// ---- refresh (NS5) branch ---------------------------------------------
+// Momentum update + bf16 pack into X (wide: same orientation; tall:
+// transposed) + per-view Frobenius partial sums (partials: count * slots).
+// With update_momentum false the momentum is read as is (no G).
+int64_t prep_slots(int64_t rows, int64_t cols);
+cudaError_t launch_prep(const View* d_views, int count, int64_t rows, int64_t cols, bool vec_ok,
+                        bool grad_bf16, bool update_momentum, float beta, uint16_t* X, int64_t ldc,
+                        int64_t x_mat_stride, float* partials, int64_t slots, cudaStream_t stream);
+
+// scale[slot] = 1 / (sqrt(sum of that slot's partials) + ns_eps).
+cudaError_t launch_norm_finish(const float* partials, int64_t slots, float* scale, int count, float ns_eps,
+                               cudaStream_t stream);
+
+// W <- W * decay - eta * shape_scale * D, D read from X (bf16, transposed
+// back for tall views). With W == nullptr in the view, writes D (fp32) to
+// the view's M pointer instead (standalone orthogonaliser).
+cudaError_t launch_apply(const View* d_views, int count, int64_t rows, int64_t cols, bool vec_ok,
+                         const uint16_t* X, int64_t ldc, int64_t x_mat_stride, float decay,
+                         float eta, cudaStream_t stream);
+
+// ---- tcgen05 GEMM stages of one NS5 round -------------------------------
+enum GemmKind { GEMM_GRAM = 0, GEMM_POLY = 1, GEMM_COMBINE = 2 };
+
+// Tensor maps of one batch of r x c bf16 matrices (X) and r x r matrices
+// (A, B), built once per buffer address.
+struct NsMaps {
+  CUtensorMap x_rows128;   // X as K-major operand, 128-row box
+  CUtensorMap x_rows256;   // X as K-major operand, 256-row box
+  CUtensorMap x_k64;       // X as MN-major operand, 64 x 64 box
+};
+struct SymMaps {
+  CUtensorMap rows128;
+  CUtensorMap rows256;
+};
+
+int encode_x_maps(NsMaps* maps, const void* X, int batch, int64_t r, int64_t c, int64_t ldc);
+int encode_sym_maps(SymMaps* maps, const void* A, int batch, int64_t r, int64_t ldr);
+
+struct GemmLaunch {
+  int batch;
+  int64_t r, c, ldc, ldr;
+  const float* scale;     // per-matrix scale or nullptr
+  float ca, cb, cc;       // NS coefficients a, b, c
+  int* err;               // device error word
+  int num_sms;
+};
+
+cudaError_t launch_gram(const NsMaps& xin, uint16_t* A, const GemmLaunch& g, cudaStream_t stream);
+cudaError_t launch_poly(const SymMaps& a, const uint16_t* A, uint16_t* B, const GemmLaunch& g,
+                        cudaStream_t stream);
+cudaError_t launch_combine(const SymMaps& b, const NsMaps& xin, const uint16_t* X,
+                           uint16_t* Xout, const GemmLaunch& g, cudaStream_t stream);
+
+// Largest dynamic shared memory the GEMM kernels request (for set-up checks).
+size_t gemm_smem_bytes();
+cudaError_t gemm_setup_attributes();
+
+}  // namespace prm

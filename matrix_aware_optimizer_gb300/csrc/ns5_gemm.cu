@@ -1,0 +1,511 @@
+// The three tensor-core GEMMs of one Newton-Schulz round, as persistent
+// tcgen05/TMEM kernels for sm_103a ("Scaling Muon for Diffusion
+// Transformers", PaperDaily walkthrough, section "Periodic Row-wise Muon":
+// NS5 is five rounds of matrix products and scalings):
+//
+//   GRAM    : A  = s^2 * X X^T          (r x r, symmetric; upper super-blocks
+//                                         computed, lower ones mirrored)
+//   POLY    : B  = b A + c A A           (A symmetric, so A A = A A^T; same
+//                                         triangle scheme, polynomial fused
+//                                         into the epilogue)
+//   COMBINE : X' = s * (a X + B X)       (r x c; axpy fused into the epilogue)
+//
+// Each launch covers every matrix of a same-shape batch: the tile queue runs
+// over (matrix, tile) pairs, so small r x r products still fill the GPU.
+//
+// CTA layout (192 threads, one CTA per SM):
+//   warp 0     : TMA producer (one lane) -- 4-stage ring of 128x64 A and
+//                256x64 B bf16 tiles, 128-byte swizzle
+//   warp 1     : TMEM allocator + MMA issuer (one lane) -- tcgen05.mma
+//                kind::f16, M=128 N=256 K=16, fp32 accumulators in TMEM,
+//                two accumulator buffers (2 x 256 columns)
+//   warps 2..5 : epilogue -- tcgen05.ld of the accumulator (one TMEM lane =
+//                one output row per thread), fused scaling / polynomial /
+//                axpy with the second operand tile read from global memory,
+//                bf16 stores (plus mirrored stores for symmetric outputs)
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace prm {
+namespace {
+
+constexpr int BM = 128;  // output rows per tile (UMMA M)
+constexpr int BN = 256;  // output cols per tile (UMMA N); also the super-block edge of symmetric outputs
+constexpr int BK = 64;   // reduction slice per pipeline stage (64 bf16 = one 128-byte swizzle row)
+constexpr int UK = 16;   // reduction length of one tcgen05.mma kind::f16
+constexpr int STAGES = 4;
+constexpr uint32_t A_TILE_BYTES = BM * BK * 2;
+constexpr uint32_t B_TILE_BYTES = BN * BK * 2;
+constexpr uint32_t STAGE_BYTES = A_TILE_BYTES + B_TILE_BYTES;
+constexpr uint32_t MN_CHUNK_BYTES = 64 * BK * 2;  // one 64-column MN-major box of the B operand
+constexpr int NUM_THREADS = 192;
+constexpr uint32_t TMEM_COLS = 2 * BN;
+constexpr size_t BARRIER_BYTES = 256;
+constexpr size_t SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + BARRIER_BYTES;
+constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;  // 2 s per individual wait
+
+struct GemmParams {
+  int M;              // output rows (r)
+  int N;              // output cols (r for GRAM/POLY, c for COMBINE)
+  int K;              // reduction length (c for GRAM, r otherwise)
+  int tiles_m;        // COMBINE: ceil(M / BM)
+  int nb;             // GRAM/POLY: ceil(M / BN) super-blocks per side
+  int tiles_per_mat;
+  int64_t total_tiles;
+  uint16_t* out;
+  int64_t ld_out, stride_out;
+  const uint16_t* aux;  // POLY: A; COMBINE: X
+  int64_t ld_aux, stride_aux;
+  const float* scale;
+  float ca, cb, cc;
+  int* err;
+  uint64_t timeout_ns;
+};
+
+struct TileCoord {
+  int mat;
+  int m0;
+  int n0;
+  bool mirror;
+  bool valid;
+};
+
+template <int KIND>
+__device__ __forceinline__ TileCoord tile_coord(const GemmParams& p, int64_t tile) {
+  TileCoord t;
+  t.mat = static_cast<int>(tile / p.tiles_per_mat);
+  const int local = static_cast<int>(tile - static_cast<int64_t>(t.mat) * p.tiles_per_mat);
+  if (KIND == GEMM_COMBINE) {
+    // m fastest: consecutive tiles share the same 256-column stripe of X.
+    const int tm = local % p.tiles_m;
+    const int tn = local / p.tiles_m;
+    t.m0 = tm * BM;
+    t.n0 = tn * BN;
+    t.mirror = false;
+    t.valid = true;
+  } else {
+    // Upper-triangle super-block pairs (I <= J), row by row; two 128-row
+    // halves per 256 x 256 super-block.
+    const int half = local & 1;
+    int rem = local >> 1;
+    int I = 0, rowlen = p.nb;
+    while (rem >= rowlen) {
+      rem -= rowlen;
+      ++I;
+      --rowlen;
+    }
+    const int J = I + rem;
+    t.m0 = I * BN + half * BM;
+    t.n0 = J * BN;
+    t.mirror = J > I;
+    t.valid = t.m0 < p.M;
+  }
+  return t;
+}
+
+__device__ __forceinline__ void load_bf16x32(const uint16_t* src, bool full, int n_valid, float (&x)[32]) {
+  if (full) {
+    const uint4* s4 = reinterpret_cast<const uint4*>(src);
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+      const uint4 u = s4[v];
+      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        x[v * 8 + 2 * h] = __uint_as_float(w[h] << 16);
+        x[v * 8 + 2 * h + 1] = __uint_as_float(w[h] & 0xFFFF0000u);
+      }
+    }
+  } else {
+#pragma unroll
+    for (int k = 0; k < 32; ++k) x[k] = (k < n_valid) ? __uint_as_float(static_cast<uint32_t>(src[k]) << 16) : 0.f;
+  }
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+__device__ __forceinline__ uint16_t to_bf16_bits(float v) {
+  const __nv_bfloat16 h = __float2bfloat16_rn(v);
+  return *reinterpret_cast<const uint16_t*>(&h);
+}
+
+template <int KIND>
+__device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileCoord& tc, int row_in_tile,
+                                              uint32_t t_row) {
+  const int i = tc.m0 + row_in_tile;
+  const bool row_ok = i < p.M;
+  float s = 1.f;
+  if (KIND == GEMM_GRAM && p.scale != nullptr) {
+    const float q = p.scale[tc.mat];
+    s = q * q;
+  }
+  if (KIND == GEMM_COMBINE && p.scale != nullptr) s = p.scale[tc.mat];
+  uint16_t* out = p.out + static_cast<int64_t>(tc.mat) * p.stride_out;
+  const uint16_t* aux = (KIND == GEMM_GRAM) ? nullptr : p.aux + static_cast<int64_t>(tc.mat) * p.stride_aux;
+
+#pragma unroll 1
+  for (int q = 0; q < BN / 32; ++q) {
+    const int j0 = tc.n0 + q * 32;
+    if (j0 >= p.N) break;  // uniform over the warp: depends on the tile only
+    float v[32];
+    tmem_load_32cols(t_row + static_cast<uint32_t>(q * 32), v);
+    const bool full = j0 + 32 <= p.N;
+    const int n_valid = p.N - j0;
+    if (row_ok) {
+      if (KIND == GEMM_GRAM) {
+#pragma unroll
+        for (int k = 0; k < 32; ++k) v[k] *= s;
+      } else {
+        float x[32];
+        load_bf16x32(aux + static_cast<int64_t>(i) * p.ld_aux + j0, full, n_valid, x);
+        if (KIND == GEMM_POLY) {
+#pragma unroll
+          for (int k = 0; k < 32; ++k) v[k] = p.cb * x[k] + p.cc * v[k];
+        } else {
+#pragma unroll
+          for (int k = 0; k < 32; ++k) v[k] = s * (p.ca * x[k] + v[k]);
+        }
+      }
+      uint16_t* dst = out + static_cast<int64_t>(i) * p.ld_out + j0;
+      if (full) {
+        uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+          uint4 u;
+          u.x = pack_bf16x2(v[8 * w + 0], v[8 * w + 1]);
+          u.y = pack_bf16x2(v[8 * w + 2], v[8 * w + 3]);
+          u.z = pack_bf16x2(v[8 * w + 4], v[8 * w + 5]);
+          u.w = pack_bf16x2(v[8 * w + 6], v[8 * w + 7]);
+          d4[w] = u;
+        }
+      } else {
+#pragma unroll
+        for (int k = 0; k < 32; ++k)
+          if (k < n_valid) dst[k] = to_bf16_bits(v[k]);
+      }
+      if (KIND != GEMM_COMBINE && tc.mirror) {
+        // Lower super-block (J, I): out[j][i]. For each j the 32 lanes of a
+        // warp write 32 consecutive i, i.e. 64 contiguous bytes.
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+          if (k < n_valid) out[static_cast<int64_t>(j0 + k) * p.ld_out + i] = to_bf16_bits(v[k]);
+        }
+      }
+    }
+  }
+}
+
+template <int KIND>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    ns_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const GemmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + STAGES * A_TILE_BYTES;
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  uint64_t* empty_bar = full_bar + STAGES;
+  uint64_t* tfull_bar = empty_bar + STAGES;
+  uint64_t* tempty_bar = tfull_bar + 2;
+  uint64_t* drain_bar = tempty_bar + 2;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain_bar + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull_bar[a], 1);
+      mbar_init(&tempty_bar[a], 4);  // one arrival per epilogue warp
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_holder, TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem_base = *tmem_holder;
+  const int num_kb = (p.K + BK - 1) / BK;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      tma_prefetch_desc(&tmA);
+      tma_prefetch_desc(&tmB);
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t issued = 0, issued_parity = 0;
+      bool ok = true;
+      for (int64_t tile = blockIdx.x; ok && tile < p.total_tiles; tile += gridDim.x) {
+        const TileCoord tc = tile_coord<KIND>(p, tile);
+        if (!tc.valid) continue;
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!wait_bounded(&empty_bar[stage], phase ^ 1u, abort_flag, p.err, p.timeout_ns)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&full_bar[stage], STAGE_BYTES);
+          uint8_t* a_dst = sA + stage * A_TILE_BYTES;
+          uint8_t* b_dst = sB + stage * B_TILE_BYTES;
+          tma_load_3d(a_dst, &tmA, &full_bar[stage], kb * BK, tc.m0, tc.mat);
+          if (KIND == GEMM_COMBINE) {
+#pragma unroll
+            for (int q = 0; q < BN / 64; ++q)
+              tma_load_3d(b_dst + q * MN_CHUNK_BYTES, &tmB, &full_bar[stage], tc.n0 + q * 64, kb * BK, tc.mat);
+          } else {
+            tma_load_3d(b_dst, &tmB, &full_bar[stage], kb * BK, tc.n0, tc.mat);
+          }
+          issued |= 1u << stage;
+          issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        // Let every load already in flight land before the CTA exits.
+        for (int s = 0; s < STAGES; ++s)
+          if (issued & (1u << s)) wait_drain(&full_bar[s], (issued_parity >> s) & 1u, 50000000ull);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(BM, BN, false, KIND == GEMM_COMBINE);
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true, issued_any = false;
+      for (int64_t tile = blockIdx.x; ok && tile < p.total_tiles; tile += gridDim.x) {
+        const TileCoord tc = tile_coord<KIND>(p, tile);
+        if (!tc.valid) continue;
+        if (!wait_bounded(&tempty_bar[acc], acc_phase ^ 1u, abort_flag, p.err, p.timeout_ns)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!wait_bounded(&full_bar[stage], phase, abort_flag, p.err, p.timeout_ns)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          const uint32_t a_addr = smem_u32(sA + stage * A_TILE_BYTES);
+          const uint32_t b_addr = smem_u32(sB + stage * B_TILE_BYTES);
+#pragma unroll
+          for (int k = 0; k < BK / UK; ++k) {
+            const uint64_t ad = smem_desc_sw128(a_addr + k * UK * 2, 16, 1024);
+            const uint64_t bd = (KIND == GEMM_COMBINE)
+                                    ? smem_desc_sw128(b_addr + k * UK * 128, MN_CHUNK_BYTES, 1024)
+                                    : smem_desc_sw128(b_addr + k * UK * 2, 16, 1024);
+            umma_bf16(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+          }
+          issued_any = true;
+          umma_commit(&empty_bar[stage]);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        umma_commit(&tfull_bar[acc]);
+        if (++acc == 2) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+      }
+      if (!ok && issued_any) {
+        // Let every MMA already issued finish before TMEM is released.
+        umma_commit(drain_bar);
+        wait_drain(drain_bar, 0, 50000000ull);
+      }
+    }
+  } else {
+    const int quarter = warp & 3;  // TMEM lanes [32 * quarter, 32 * quarter + 32) belong to this warp
+    const int row_in_tile = quarter * 32 + lane;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int64_t tile = blockIdx.x; tile < p.total_tiles; tile += gridDim.x) {
+      const TileCoord tc = tile_coord<KIND>(p, tile);
+      if (!tc.valid) continue;
+      const bool got = wait_bounded(&tfull_bar[acc], acc_phase, abort_flag, p.err, p.timeout_ns);
+      if (!__all_sync(0xffffffffu, got)) break;
+      tc_fence_after_sync();
+      const uint32_t t_row = tmem_base + static_cast<uint32_t>(acc * BN) + (static_cast<uint32_t>(quarter * 32) << 16);
+      epilogue_tile<KIND>(p, tc, row_in_tile, t_row);
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty_bar[acc]);
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+  }
+  __syncwarp();
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  if (warp == 1) tmem_dealloc(tmem_base, TMEM_COLS);
+}
+
+// ---------------------------------------------------------------- host side
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+// 3-D bf16 tensor map over `batch` row-major matrices of rows x cols with row
+// pitch ld (elements); box = box_inner x box_rows x 1, 128-byte swizzle,
+// out-of-range elements read as zero.
+int encode_3d(CUtensorMap* map, const void* base, int batch, int64_t rows, int64_t cols, int64_t ld,
+              uint32_t box_inner, uint32_t box_rows) {
+  auto enc = tensor_map_encoder();
+  if (enc == nullptr) return -1;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows),
+                        static_cast<cuuint64_t>(batch)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(ld * 2), static_cast<cuuint64_t>(rows * ld * 2)};
+  cuuint32_t box[3] = {box_inner, box_rows, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? 0 : static_cast<int>(r);
+}
+
+template <int KIND>
+cudaError_t launch_kind(const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p, int num_sms,
+                        cudaStream_t stream) {
+  if (p.total_tiles == 0) return cudaSuccess;
+  const int64_t grid64 = std::min<int64_t>(p.total_tiles, num_sms);
+  ns_gemm_kernel<KIND><<<static_cast<unsigned>(grid64), NUM_THREADS, SMEM_BYTES, stream>>>(a, b, p);
+  return cudaGetLastError();
+}
+
+GemmParams base_params(const GemmLaunch& g) {
+  GemmParams p{};
+  p.scale = g.scale;
+  p.ca = g.ca;
+  p.cb = g.cb;
+  p.cc = g.cc;
+  p.err = g.err;
+  p.timeout_ns = WAIT_LIMIT_NS;
+  return p;
+}
+
+void set_symmetric_tiles(GemmParams& p, int batch, int64_t r) {
+  p.M = static_cast<int>(r);
+  p.N = static_cast<int>(r);
+  p.nb = static_cast<int>((r + BN - 1) / BN);
+  p.tiles_m = 0;
+  p.tiles_per_mat = p.nb * (p.nb + 1);  // nb(nb+1)/2 super-blocks x 2 halves
+  p.total_tiles = static_cast<int64_t>(p.tiles_per_mat) * batch;
+}
+
+}  // namespace
+
+size_t gemm_smem_bytes() { return SMEM_BYTES; }
+
+cudaError_t gemm_setup_attributes() {
+  cudaError_t e;
+  if ((e = cudaFuncSetAttribute(ns_gemm_kernel<GEMM_GRAM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                static_cast<int>(SMEM_BYTES))) != cudaSuccess)
+    return e;
+  if ((e = cudaFuncSetAttribute(ns_gemm_kernel<GEMM_POLY>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                static_cast<int>(SMEM_BYTES))) != cudaSuccess)
+    return e;
+  return cudaFuncSetAttribute(ns_gemm_kernel<GEMM_COMBINE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              static_cast<int>(SMEM_BYTES));
+}
+
+int encode_x_maps(NsMaps* maps, const void* X, int batch, int64_t r, int64_t c, int64_t ldc) {
+  int e;
+  if ((e = encode_3d(&maps->x_rows128, X, batch, r, c, ldc, BK, BM)) != 0) return e;
+  if ((e = encode_3d(&maps->x_rows256, X, batch, r, c, ldc, BK, BN)) != 0) return e;
+  return encode_3d(&maps->x_k64, X, batch, r, c, ldc, 64, BK);
+}
+
+int encode_sym_maps(SymMaps* maps, const void* A, int batch, int64_t r, int64_t ldr) {
+  int e;
+  if ((e = encode_3d(&maps->rows128, A, batch, r, r, ldr, BK, BM)) != 0) return e;
+  return encode_3d(&maps->rows256, A, batch, r, r, ldr, BK, BN);
+}
+
+cudaError_t launch_gram(const NsMaps& xin, uint16_t* A, const GemmLaunch& g, cudaStream_t stream) {
+  GemmParams p = base_params(g);
+  set_symmetric_tiles(p, g.batch, g.r);
+  p.K = static_cast<int>(g.c);
+  p.out = A;
+  p.ld_out = g.ldr;
+  p.stride_out = g.r * g.ldr;
+  p.aux = nullptr;
+  return launch_kind<GEMM_GRAM>(xin.x_rows128, xin.x_rows256, p, g.num_sms, stream);
+}
+
+cudaError_t launch_poly(const SymMaps& a, const uint16_t* A, uint16_t* B, const GemmLaunch& g,
+                        cudaStream_t stream) {
+  GemmParams p = base_params(g);
+  set_symmetric_tiles(p, g.batch, g.r);
+  p.K = static_cast<int>(g.r);
+  p.out = B;
+  p.ld_out = g.ldr;
+  p.stride_out = g.r * g.ldr;
+  p.aux = A;
+  p.ld_aux = g.ldr;
+  p.stride_aux = g.r * g.ldr;
+  p.scale = nullptr;
+  return launch_kind<GEMM_POLY>(a.rows128, a.rows256, p, g.num_sms, stream);
+}
+
+cudaError_t launch_combine(const SymMaps& b, const NsMaps& xin, const uint16_t* X, uint16_t* Xout,
+                           const GemmLaunch& g, cudaStream_t stream) {
+  GemmParams p = base_params(g);
+  p.M = static_cast<int>(g.r);
+  p.N = static_cast<int>(g.c);
+  p.K = static_cast<int>(g.r);
+  p.tiles_m = static_cast<int>((g.r + BM - 1) / BM);
+  p.nb = 0;
+  const int tiles_n = static_cast<int>((g.c + BN - 1) / BN);
+  p.tiles_per_mat = p.tiles_m * tiles_n;
+  p.total_tiles = static_cast<int64_t>(p.tiles_per_mat) * g.batch;
+  p.out = Xout;
+  p.ld_out = g.ldc;
+  p.stride_out = g.r * g.ldc;
+  p.aux = X;
+  p.ld_aux = g.ldc;
+  p.stride_aux = g.r * g.ldc;
+  return launch_kind<GEMM_COMBINE>(b.rows128, xin.x_k64, p, g.num_sms, stream);
+}
+
+}  // namespace prm

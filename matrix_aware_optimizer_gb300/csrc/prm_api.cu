@@ -1,0 +1,818 @@
+// C ABI and host engine of libprm: argument checks, the planner (launch
+// groups by shape, NS5 groups by wide orientation, MuonBP block views,
+// workspace layout) and the launch sequence of one step on the caller's
+// stream. Method: "Scaling Muon for Diffusion Transformers" (PaperDaily
+// walkthrough, section "Periodic Row-wise Muon", Fig. 3 update rule) and
+// "MuonBP: Faster Muon via Block-Periodic Orthogonalization" (abstract).
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <map>
+#include <memory>
+#include <mutex>
+#include <new>
+#include <string>
+#include <tuple>
+#include <vector>
+
+#include "internal.h"
+#include "prm.h"
+
+namespace prm {
+namespace {
+
+constexpr float NS_EPS = 1e-7f;  // added to ||M||_F before NS5 pre-normalisation
+constexpr float DEFAULT_COEFFS[3] = {3.4445f, -4.7750f, 2.0315f};
+constexpr int NS_STEPS = 5;
+
+thread_local std::string g_create_error;
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+int64_t round8(int64_t x) { return (x + 7) / 8 * 8; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Views of one exact shape and orientation, launched together.
+struct LaunchSet {
+  int64_t rows = 0, cols = 0;
+  bool bf16 = false;
+  bool vec_ok = true;
+  std::vector<View> views;
+  View* d_views = nullptr;
+  size_t off_partials = 0, off_inv = 0;  // tall RowNorm scratch (relative to workspace base)
+};
+
+// Same wide-orientation shape r x c: one batch for the tensor-core GEMMs.
+struct NsGroup {
+  int64_t r = 0, c = 0, ldc = 0, ldr = 0;
+  int count = 0;
+  int64_t slots = 0;  // Frobenius partial slots per matrix
+  std::vector<LaunchSet> sets;
+  size_t off_x0 = 0, off_x1 = 0, off_a = 0, off_b = 0, off_scale = 0, off_partials = 0, bytes = 0;
+  // tensor maps for the bound workspace
+  const void* maps_base = nullptr;
+  NsMaps mx0{}, mx1{};
+  SymMaps ma{}, mb{};
+};
+
+struct NsPlan {
+  std::vector<NsGroup> groups;
+  size_t bytes = 0;  // groups run one after another and share the region
+};
+
+struct RowNormPlan {
+  std::vector<LaunchSet> wide, tall;
+  size_t bytes = 0;
+};
+
+void free_sets(std::vector<LaunchSet>& sets) {
+  for (auto& s : sets) {
+    if (s.d_views) cudaFree(s.d_views);
+    s.d_views = nullptr;
+  }
+}
+
+void free_plan(NsPlan& p) {
+  for (auto& g : p.groups) free_sets(g.sets);
+  p.groups.clear();
+  p.bytes = 0;
+}
+
+cudaError_t upload_sets(std::vector<LaunchSet>& sets) {
+  for (auto& s : sets) {
+    if (s.views.empty()) continue;
+    const size_t b = s.views.size() * sizeof(View);
+    cudaError_t e = cudaMalloc(reinterpret_cast<void**>(&s.d_views), b);
+    if (e != cudaSuccess) return e;
+    if ((e = cudaMemcpy(s.d_views, s.views.data(), b, cudaMemcpyHostToDevice)) != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+bool view_vec_ok(const View& v) {
+  const bool base = (v.cols % 4 == 0) && (v.ld % 4 == 0);
+  const bool ptrs = (v.W == nullptr || aligned16(v.W)) && aligned16(v.M) && (v.out == nullptr || aligned16(v.out));
+  const bool g = v.G == nullptr || (v.grad_bf16 ? (reinterpret_cast<uintptr_t>(v.G) & 7u) == 0 : aligned16(v.G));
+  return base && ptrs && g;
+}
+
+// Groups views for the NS5 branch and lays out the shared group workspace.
+void build_ns_plan(const std::vector<View>& views, NsPlan& plan) {
+  std::map<std::pair<int64_t, int64_t>, size_t> index;
+  for (const View& v0 : views) {
+    const bool tall = v0.rows > v0.cols;
+    const int64_t r = tall ? v0.cols : v0.rows, c = tall ? v0.rows : v0.cols;
+    auto key = std::make_pair(r, c);
+    auto it = index.find(key);
+    if (it == index.end()) {
+      NsGroup g;
+      g.r = r;
+      g.c = c;
+      g.ldc = round8(c);
+      g.ldr = round8(r);
+      plan.groups.push_back(std::move(g));
+      it = index.emplace(key, plan.groups.size() - 1).first;
+    }
+    NsGroup& g = plan.groups[it->second];
+    View v = v0;
+    v.slot = g.count++;
+    LaunchSet* set = nullptr;
+    for (auto& s : g.sets)
+      if (s.rows == v.rows && s.cols == v.cols && s.bf16 == (v.grad_bf16 != 0)) set = &s;
+    if (set == nullptr) {
+      g.sets.emplace_back();
+      set = &g.sets.back();
+      set->rows = v.rows;
+      set->cols = v.cols;
+      set->bf16 = v.grad_bf16 != 0;
+    }
+    set->vec_ok = set->vec_ok && view_vec_ok(v);
+    set->views.push_back(v);
+  }
+  plan.bytes = 0;
+  for (auto& g : plan.groups) {
+    g.slots = prep_slots(g.sets.front().rows, g.sets.front().cols);
+    for (auto& s : g.sets) g.slots = std::max(g.slots, prep_slots(s.rows, s.cols));
+    const size_t xb = align_up(static_cast<size_t>(g.count) * g.r * g.ldc * 2, 256);
+    const size_t ab = align_up(static_cast<size_t>(g.count) * g.r * g.ldr * 2, 256);
+    size_t off = 0;
+    g.off_x0 = off;
+    off += xb;
+    g.off_x1 = off;
+    off += xb;
+    g.off_a = off;
+    off += ab;
+    g.off_b = off;
+    off += ab;
+    g.off_scale = off;
+    off += align_up(static_cast<size_t>(g.count) * 4, 256);
+    g.off_partials = off;
+    off += align_up(static_cast<size_t>(g.count) * g.slots * 4, 256);
+    g.bytes = off;
+    plan.bytes = std::max(plan.bytes, off);
+  }
+}
+
+}  // namespace
+}  // namespace prm
+
+using namespace prm;
+
+// Event-pair records of kernel families (prm_profile).
+struct Profiler {
+  struct Rec {
+    int family;
+    size_t ev;       // index of the start event; stop is ev + 1
+    int kernels;
+    double work;
+  };
+  bool on = false;
+  std::vector<cudaEvent_t> pool;
+  std::vector<Rec> recs;
+  size_t used = 0;
+
+  cudaEvent_t next() {
+    if (used == pool.size()) {
+      cudaEvent_t e;
+      if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+      pool.push_back(e);
+    }
+    return pool[used++];
+  }
+  // Returns the start-event index, or SIZE_MAX when not recording.
+  size_t begin(cudaStream_t st) {
+    if (!on) return SIZE_MAX;
+    const size_t i = used;
+    cudaEvent_t a = next(), b = next();
+    if (a == nullptr || b == nullptr) return SIZE_MAX;
+    cudaEventRecord(a, st);
+    return i;
+  }
+  void end(size_t i, int family, int kernels, double work, cudaStream_t st) {
+    if (i == SIZE_MAX) return;
+    cudaEventRecord(pool[i + 1], st);
+    recs.push_back(Rec{family, i, kernels, work});
+  }
+  void reset() {
+    recs.clear();
+    used = 0;
+  }
+  ~Profiler() {
+    for (auto e : pool) cudaEventDestroy(e);
+  }
+};
+
+struct prm_ctx {
+  Profiler prof;
+  int device = 0;
+  int num_sms = 0;
+  std::string err;
+  int* d_err = nullptr;  // device error word of the bounded waits
+  int count = 0;
+  int blocks = 0;
+  RowNormPlan rn;
+  NsPlan ns_full, ns_blocks;
+  bool registered = false;
+  void* ws = nullptr;
+  size_t ws_bytes = 0;
+};
+
+namespace {
+
+int fail(prm_ctx* c, int code, const std::string& msg) {
+  if (c)
+    c->err = msg;
+  else
+    g_create_error = msg;
+  return code;
+}
+
+int cuda_fail(prm_ctx* c, cudaError_t e, const char* what) {
+  return fail(c, PRM_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString(e));
+}
+
+// Makes the context's device current for the duration of a call.
+struct DeviceGuard {
+  int prev = -1;
+  bool changed = false;
+  explicit DeviceGuard(int dev) {
+    if (cudaGetDevice(&prev) == cudaSuccess && prev != dev) {
+      changed = cudaSetDevice(dev) == cudaSuccess;
+    }
+  }
+  ~DeviceGuard() {
+    if (changed) cudaSetDevice(prev);
+  }
+};
+
+void clear_registration(prm_ctx* c) {
+  free_sets(c->rn.wide);
+  free_sets(c->rn.tall);
+  c->rn.wide.clear();
+  c->rn.tall.clear();
+  c->rn.bytes = 0;
+  free_plan(c->ns_full);
+  free_plan(c->ns_blocks);
+  c->count = 0;
+  c->blocks = 0;
+  c->registered = false;
+}
+
+void add_to_sets(std::vector<LaunchSet>& sets, const View& v) {
+  for (auto& s : sets) {
+    if (s.rows == v.rows && s.cols == v.cols && s.bf16 == (v.grad_bf16 != 0)) {
+      s.vec_ok = s.vec_ok && view_vec_ok(v);
+      s.views.push_back(v);
+      return;
+    }
+  }
+  LaunchSet s;
+  s.rows = v.rows;
+  s.cols = v.cols;
+  s.bf16 = v.grad_bf16 != 0;
+  s.vec_ok = view_vec_ok(v);
+  s.views.push_back(v);
+  sets.push_back(std::move(s));
+}
+
+int bind_maps(prm_ctx* c, NsGroup& g, void* base) {
+  if (g.maps_base == base) return PRM_OK;
+  char* b = static_cast<char*>(base);
+  int e = encode_x_maps(&g.mx0, b + g.off_x0, g.count, g.r, g.c, g.ldc);
+  if (e == 0) e = encode_x_maps(&g.mx1, b + g.off_x1, g.count, g.r, g.c, g.ldc);
+  if (e == 0) e = encode_sym_maps(&g.ma, b + g.off_a, g.count, g.r, g.ldr);
+  if (e == 0) e = encode_sym_maps(&g.mb, b + g.off_b, g.count, g.r, g.ldr);
+  if (e != 0) return fail(c, PRM_ERR_CUDA, "cuTensorMapEncodeTiled failed (code " + std::to_string(e) + ")");
+  g.maps_base = base;
+  return PRM_OK;
+}
+
+// One NS5 refresh over every group of `plan`: prep (momentum + pack + norm
+// partials), scale, five GRAM / POLY / COMBINE rounds, apply.
+int run_ns(prm_ctx* c, NsPlan& plan, void* base, bool update_momentum, float beta, float decay, float eta,
+           const float coeffs[3], int steps, cudaStream_t stream) {
+  char* b = static_cast<char*>(base);
+  for (auto& g : plan.groups) {
+    int rc = bind_maps(c, g, base);
+    if (rc != PRM_OK) return rc;
+    uint16_t* x0 = reinterpret_cast<uint16_t*>(b + g.off_x0);
+    uint16_t* x1 = reinterpret_cast<uint16_t*>(b + g.off_x1);
+    uint16_t* A = reinterpret_cast<uint16_t*>(b + g.off_a);
+    uint16_t* B = reinterpret_cast<uint16_t*>(b + g.off_b);
+    float* scale = reinterpret_cast<float*>(b + g.off_scale);
+    float* partials = reinterpret_cast<float*>(b + g.off_partials);
+    cudaError_t e;
+    const double params = static_cast<double>(g.count) * g.r * g.c;
+    double prep_bytes = 0;
+    for (auto& s : g.sets)
+      prep_bytes += static_cast<double>(s.views.size()) * s.rows * s.cols *
+                    (update_momentum ? (s.bf16 ? 12.0 : 14.0) : 6.0);
+    size_t ev = c->prof.begin(stream);
+    for (auto& s : g.sets) {
+      e = launch_prep(s.d_views, static_cast<int>(s.views.size()), s.rows, s.cols, s.vec_ok, s.bf16,
+                      update_momentum, beta, x0, g.ldc, g.r * g.ldc, partials, g.slots, stream);
+      if (e != cudaSuccess) return cuda_fail(c, e, "prep launch");
+    }
+    if ((e = launch_norm_finish(partials, g.slots, scale, g.count, NS_EPS, stream)) != cudaSuccess)
+      return cuda_fail(c, e, "norm launch");
+    c->prof.end(ev, PRM_FAMILY_NS_PREP, static_cast<int>(g.sets.size()) + 1, prep_bytes, stream);
+    GemmLaunch gl{};
+    gl.batch = g.count;
+    gl.r = g.r;
+    gl.c = g.c;
+    gl.ldc = g.ldc;
+    gl.ldr = g.ldr;
+    gl.ca = coeffs[0];
+    gl.cb = coeffs[1];
+    gl.cc = coeffs[2];
+    gl.err = c->d_err;
+    gl.num_sms = c->num_sms;
+    uint16_t* cur = x0;
+    uint16_t* nxt = x1;
+    const NsMaps* mcur = &g.mx0;
+    const NsMaps* mnxt = &g.mx1;
+    for (int it = 0; it < steps; ++it) {
+      gl.scale = it == 0 ? scale : nullptr;
+      ev = c->prof.begin(stream);
+      if ((e = launch_gram(*mcur, A, gl, stream)) != cudaSuccess) return cuda_fail(c, e, "gram launch");
+      c->prof.end(ev, PRM_FAMILY_NS_GRAM, 1, 2.0 * params * g.r, stream);
+      ev = c->prof.begin(stream);
+      if ((e = launch_poly(g.ma, A, B, gl, stream)) != cudaSuccess) return cuda_fail(c, e, "poly launch");
+      c->prof.end(ev, PRM_FAMILY_NS_POLY, 1, 2.0 * g.count * double(g.r) * g.r * g.r, stream);
+      ev = c->prof.begin(stream);
+      if ((e = launch_combine(g.mb, *mcur, cur, nxt, gl, stream)) != cudaSuccess)
+        return cuda_fail(c, e, "combine launch");
+      c->prof.end(ev, PRM_FAMILY_NS_COMBINE, 1, 2.0 * params * g.r, stream);
+      std::swap(cur, nxt);
+      std::swap(mcur, mnxt);
+    }
+    ev = c->prof.begin(stream);
+    for (auto& s : g.sets) {
+      e = launch_apply(s.d_views, static_cast<int>(s.views.size()), s.rows, s.cols, s.vec_ok, cur, g.ldc,
+                       g.r * g.ldc, decay, eta, stream);
+      if (e != cudaSuccess) return cuda_fail(c, e, "apply launch");
+    }
+    c->prof.end(ev, PRM_FAMILY_NS_APPLY, static_cast<int>(g.sets.size()), params * 10.0, stream);
+  }
+  return PRM_OK;
+}
+
+int run_rownorm(prm_ctx* c, void* base, StepScalars sc, cudaStream_t stream) {
+  char* b = static_cast<char*>(base);
+  cudaError_t e;
+  for (auto& s : c->rn.wide) {
+    const double bytes = static_cast<double>(s.views.size()) * s.rows * s.cols * (s.bf16 ? 18.0 : 20.0);
+    const size_t ev = c->prof.begin(stream);
+    e = launch_rownorm_wide(s.d_views, static_cast<int>(s.views.size()), s.rows, s.cols, s.vec_ok, s.bf16, sc,
+                            stream);
+    if (e != cudaSuccess) return cuda_fail(c, e, "rownorm wide launch");
+    c->prof.end(ev, PRM_FAMILY_ROWNORM_WIDE, 1, bytes, stream);
+  }
+  for (auto& s : c->rn.tall) {
+    const double bytes = static_cast<double>(s.views.size()) * s.rows * s.cols * (s.bf16 ? 18.0 : 20.0);
+    const size_t ev = c->prof.begin(stream);
+    e = launch_rownorm_tall(s.d_views, static_cast<int>(s.views.size()), s.rows, s.cols, s.vec_ok, s.bf16, sc,
+                            reinterpret_cast<float*>(b + s.off_partials), reinterpret_cast<float*>(b + s.off_inv),
+                            stream);
+    if (e != cudaSuccess) return cuda_fail(c, e, "rownorm tall launch");
+    c->prof.end(ev, PRM_FAMILY_ROWNORM_TALL, 3, bytes, stream);
+  }
+  return PRM_OK;
+}
+
+bool finite(float x) { return std::isfinite(x); }
+
+// Per-device state of the standalone entry points (no context).
+struct DeviceState {
+  int num_sms = 0;
+  int* d_err = nullptr;
+  bool ready = false;
+};
+std::mutex g_dev_mutex;
+DeviceState g_dev[64];
+
+int device_state(DeviceState** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return PRM_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_dev_mutex);
+  DeviceState& d = g_dev[dev];
+  if (!d.ready) {
+    cudaDeviceProp prop;
+    if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return PRM_ERR_CUDA;
+    if (prop.major != 10) return PRM_ERR_UNSUPPORTED;
+    d.num_sms = prop.multiProcessorCount;
+    if (gemm_setup_attributes() != cudaSuccess) return PRM_ERR_CUDA;
+    if (cudaMalloc(reinterpret_cast<void**>(&d.d_err), sizeof(int)) != cudaSuccess) return PRM_ERR_CUDA;
+    if (cudaMemset(d.d_err, 0, sizeof(int)) != cudaSuccess) return PRM_ERR_CUDA;
+    d.ready = true;
+  }
+  *out = &d;
+  return PRM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int prm_create(prm_ctx** out, int cuda_device) {
+  if (out == nullptr) return fail(nullptr, PRM_ERR_INVALID_ARG, "out is NULL");
+  *out = nullptr;
+  int ndev = 0;
+  cudaError_t e = cudaGetDeviceCount(&ndev);
+  if (e != cudaSuccess) return fail(nullptr, PRM_ERR_CUDA, std::string("cudaGetDeviceCount: ") + cudaGetErrorString(e));
+  if (cuda_device < 0 || cuda_device >= ndev) return fail(nullptr, PRM_ERR_INVALID_ARG, "no such CUDA device");
+  cudaDeviceProp prop;
+  if ((e = cudaGetDeviceProperties(&prop, cuda_device)) != cudaSuccess)
+    return fail(nullptr, PRM_ERR_CUDA, std::string("cudaGetDeviceProperties: ") + cudaGetErrorString(e));
+  if (prop.major != 10)
+    return fail(nullptr, PRM_ERR_UNSUPPORTED,
+                "device compute capability " + std::to_string(prop.major) + "." + std::to_string(prop.minor) +
+                    " is not in the sm_100 family this library is built for");
+  prm_ctx* c = new (std::nothrow) prm_ctx();
+  if (c == nullptr) return fail(nullptr, PRM_ERR_OOM, "out of host memory");
+  c->device = cuda_device;
+  c->num_sms = prop.multiProcessorCount;
+  DeviceGuard guard(cuda_device);
+  if ((e = gemm_setup_attributes()) != cudaSuccess) {
+    delete c;
+    return fail(nullptr, PRM_ERR_CUDA, std::string("cudaFuncSetAttribute: ") + cudaGetErrorString(e));
+  }
+  if ((e = cudaMalloc(reinterpret_cast<void**>(&c->d_err), sizeof(int))) != cudaSuccess ||
+      (e = cudaMemset(c->d_err, 0, sizeof(int))) != cudaSuccess) {
+    if (c->d_err) cudaFree(c->d_err);
+    delete c;
+    return fail(nullptr, PRM_ERR_CUDA, std::string("error word: ") + cudaGetErrorString(e));
+  }
+  *out = c;
+  return PRM_OK;
+}
+
+int prm_destroy(prm_ctx* c) {
+  if (c == nullptr) return PRM_OK;
+  DeviceGuard guard(c->device);
+  clear_registration(c);
+  if (c->d_err) cudaFree(c->d_err);
+  delete c;
+  return PRM_OK;
+}
+
+int prm_register_matrices(prm_ctx* c, const prm_matrix_desc* d, int count, int muonbp_blocks) {
+  if (c == nullptr) return fail(nullptr, PRM_ERR_INVALID_ARG, "ctx is NULL");
+  if (count < 0 || (count > 0 && d == nullptr)) return fail(c, PRM_ERR_INVALID_ARG, "bad descriptor array");
+  if (count > 65535 / std::max(1, muonbp_blocks))
+    return fail(c, PRM_ERR_UNSUPPORTED, "too many matrices for one registration (limit 65535 views)");
+  if (muonbp_blocks < 0) return fail(c, PRM_ERR_INVALID_ARG, "muonbp_blocks must be >= 0");
+  DeviceGuard guard(c->device);
+  clear_registration(c);
+  c->ws = nullptr;
+  c->ws_bytes = 0;
+  std::vector<View> full;
+  full.reserve(count);
+  for (int i = 0; i < count; ++i) {
+    const prm_matrix_desc& m = d[i];
+    if (m.param == nullptr || m.momentum == nullptr || m.grad == nullptr)
+      return fail(c, PRM_ERR_INVALID_ARG, "matrix " + std::to_string(i) + ": NULL pointer");
+    if (m.grad_dtype != PRM_FP32 && m.grad_dtype != PRM_BF16)
+      return fail(c, PRM_ERR_INVALID_ARG, "matrix " + std::to_string(i) + ": unknown grad_dtype");
+    if (m.reserved != 0 || m.reserved2 != 0.f)
+      return fail(c, PRM_ERR_INVALID_ARG, "matrix " + std::to_string(i) + ": reserved fields must be 0");
+    if (m.rows < 1 || m.cols < 1 || m.rows > (int64_t(1) << 31) - 1 || m.cols > (int64_t(1) << 31) - 1)
+      return fail(c, PRM_ERR_SHAPE, "matrix " + std::to_string(i) + ": rows and cols must be in [1, 2^31)");
+    // Launch-grid limits: views of one shape share grid.y / grid.z (<= 65535),
+    // tall row blocks of 256 rows and 64 x 64 transpose tiles use grid.y.
+    if (std::min(m.rows, m.cols) > int64_t(65535) * 64 || (m.rows > m.cols && m.rows > int64_t(65535) * 64))
+      return fail(c, PRM_ERR_UNSUPPORTED, "matrix " + std::to_string(i) + ": shape beyond the kernels' grid limits");
+    if (!aligned16(m.param) || !aligned16(m.momentum) || !aligned16(m.grad))
+      return fail(c, PRM_ERR_ALIGNMENT, "matrix " + std::to_string(i) + ": pointers must be 16-byte aligned");
+    if (!std::isfinite(m.shape_scale))
+      return fail(c, PRM_ERR_INVALID_ARG, "matrix " + std::to_string(i) + ": shape_scale not finite");
+    View v{};
+    v.W = m.param;
+    v.M = m.momentum;
+    v.G = m.grad;
+    v.rows = m.rows;
+    v.cols = m.cols;
+    v.ld = m.cols;
+    v.grad_bf16 = m.grad_dtype == PRM_BF16;
+    v.shape_scale = m.shape_scale > 0.f
+                        ? m.shape_scale
+                        : static_cast<float>(std::sqrt(std::max(1.0, double(m.rows) / double(m.cols))));
+    full.push_back(v);
+  }
+  // MuonBP blocks: P contiguous pieces along the long side, last takes the remainder.
+  std::vector<View> blocks;
+  if (muonbp_blocks > 0) {
+    for (int i = 0; i < count; ++i) {
+      const View& v = full[i];
+      const bool wide = v.rows <= v.cols;
+      const int64_t L = wide ? v.cols : v.rows;
+      if (L < muonbp_blocks)
+        return fail(c, PRM_ERR_SHAPE, "matrix " + std::to_string(i) + ": long side shorter than muonbp_blocks");
+      const int64_t base = L / muonbp_blocks;
+      for (int k = 0; k < muonbp_blocks; ++k) {
+        const int64_t lo = k * base, hi = (k == muonbp_blocks - 1) ? L : lo + base;
+        View b = v;
+        if (wide) {
+          b.W = v.W + lo;
+          b.M = v.M + lo;
+          b.G = v.grad_bf16 ? static_cast<const void*>(static_cast<const uint16_t*>(v.G) + lo)
+                            : static_cast<const void*>(static_cast<const float*>(v.G) + lo);
+          b.cols = hi - lo;
+        } else {
+          b.W = v.W + lo * v.ld;
+          b.M = v.M + lo * v.ld;
+          b.G = v.grad_bf16 ? static_cast<const void*>(static_cast<const uint16_t*>(v.G) + lo * v.ld)
+                            : static_cast<const void*>(static_cast<const float*>(v.G) + lo * v.ld);
+          b.rows = hi - lo;
+        }
+        blocks.push_back(b);
+      }
+    }
+  }
+  // RowNorm launch sets (whole matrices), tall scratch laid out back to back.
+  for (const View& v : full) add_to_sets(v.rows <= v.cols ? c->rn.wide : c->rn.tall, v);
+  size_t off = 0;
+  for (auto& s : c->rn.tall) {
+    s.off_partials = off;
+    off += align_up(s.views.size() * tall_row_blocks(s.rows) * s.cols * 4, 256);
+    s.off_inv = off;
+    off += align_up(s.views.size() * s.cols * 4, 256);
+  }
+  c->rn.bytes = off;
+  build_ns_plan(full, c->ns_full);
+  if (muonbp_blocks > 0) build_ns_plan(blocks, c->ns_blocks);
+  cudaError_t e = upload_sets(c->rn.wide);
+  if (e == cudaSuccess) e = upload_sets(c->rn.tall);
+  for (auto& g : c->ns_full.groups)
+    if (e == cudaSuccess) e = upload_sets(g.sets);
+  for (auto& g : c->ns_blocks.groups)
+    if (e == cudaSuccess) e = upload_sets(g.sets);
+  if (e != cudaSuccess) {
+    clear_registration(c);
+    return cuda_fail(c, e, "uploading launch tables");
+  }
+  c->count = count;
+  c->blocks = muonbp_blocks;
+  c->registered = true;
+  return PRM_OK;
+}
+
+int prm_workspace_bytes(const prm_ctx* c, size_t* bytes) {
+  if (c == nullptr || bytes == nullptr) return PRM_ERR_INVALID_ARG;
+  *bytes = c->registered ? std::max({c->rn.bytes, c->ns_full.bytes, c->ns_blocks.bytes}) : 0;
+  return PRM_OK;
+}
+
+int prm_set_workspace(prm_ctx* c, void* dev_ptr, size_t bytes) {
+  if (c == nullptr) return fail(nullptr, PRM_ERR_INVALID_ARG, "ctx is NULL");
+  size_t need = 0;
+  prm_workspace_bytes(c, &need);
+  if (need > 0 && dev_ptr == nullptr) return fail(c, PRM_ERR_INVALID_ARG, "workspace pointer is NULL");
+  if ((reinterpret_cast<uintptr_t>(dev_ptr) & 255u) != 0)
+    return fail(c, PRM_ERR_ALIGNMENT, "workspace must be 256-byte aligned");
+  if (bytes < need)
+    return fail(c, PRM_ERR_WORKSPACE, "workspace of " + std::to_string(bytes) + " bytes is smaller than the " +
+                                          std::to_string(need) + " required");
+  c->ws = dev_ptr;
+  c->ws_bytes = bytes;
+  return PRM_OK;
+}
+
+int prm_branch(int64_t t, int K, int mode) {
+  if (t < 0 || K < 1 || (mode != PRM_MODE_PRMUON && mode != PRM_MODE_MUONBP)) return -PRM_ERR_INVALID_ARG;
+  return (t % K == 0) ? 1 : 0;
+}
+
+int prm_step(prm_ctx* c, int64_t t, int K, float gamma, float lr, float wd, float beta, float eps,
+             const float* ns_coeffs, int mode, void* stream) {
+  if (c == nullptr) return fail(nullptr, PRM_ERR_INVALID_ARG, "ctx is NULL");
+  if (t < 0) return fail(c, PRM_ERR_INVALID_ARG, "t must be >= 0");
+  if (K < 1) return fail(c, PRM_ERR_INVALID_ARG, "K must be >= 1");
+  if (mode != PRM_MODE_PRMUON && mode != PRM_MODE_MUONBP) return fail(c, PRM_ERR_INVALID_ARG, "unknown mode");
+  if (!(beta >= 0.f && beta < 1.f)) return fail(c, PRM_ERR_INVALID_ARG, "beta must be in [0, 1)");
+  if (!(eps > 0.f) || !finite(eps)) return fail(c, PRM_ERR_INVALID_ARG, "eps must be > 0");
+  if (!finite(lr) || !finite(wd) || !finite(gamma)) return fail(c, PRM_ERR_INVALID_ARG, "lr, wd, gamma must be finite");
+  float coeffs[3] = {DEFAULT_COEFFS[0], DEFAULT_COEFFS[1], DEFAULT_COEFFS[2]};
+  if (ns_coeffs != nullptr) {
+    for (int i = 0; i < 3; ++i) {
+      if (!finite(ns_coeffs[i])) return fail(c, PRM_ERR_INVALID_ARG, "ns_coeffs must be finite");
+      coeffs[i] = ns_coeffs[i];
+    }
+  }
+  if (!c->registered) return fail(c, PRM_ERR_NOT_REGISTERED, "no matrices registered");
+  if (mode == PRM_MODE_MUONBP && c->blocks == 0)
+    return fail(c, PRM_ERR_NOT_REGISTERED, "MuonBP step needs a registration with muonbp_blocks > 0");
+  size_t need = 0;
+  prm_workspace_bytes(c, &need);
+  if (need > 0 && (c->ws == nullptr || c->ws_bytes < need))
+    return fail(c, PRM_ERR_WORKSPACE, "workspace not set or too small");
+  if (c->count == 0) return PRM_OK;
+  DeviceGuard guard(c->device);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const bool refresh = (t % K) == 0;
+  StepScalars sc;
+  sc.beta = beta;
+  sc.decay = 1.f - lr * wd;
+  sc.eta = refresh ? lr : lr * gamma;
+  sc.eps = eps;
+  if (mode == PRM_MODE_PRMUON && !refresh) return run_rownorm(c, c->ws, sc, st);
+  NsPlan& plan = (mode == PRM_MODE_MUONBP && !refresh) ? c->ns_blocks : c->ns_full;
+  return run_ns(c, plan, c->ws, true, beta, sc.decay, sc.eta, coeffs, NS_STEPS, st);
+}
+
+int prm_sync_status(prm_ctx* c, void* stream) {
+  if (c == nullptr) return fail(nullptr, PRM_ERR_INVALID_ARG, "ctx is NULL");
+  DeviceGuard guard(c->device);
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(c, e, "stream synchronize");
+  int word = 0;
+  if ((e = cudaMemcpy(&word, c->d_err, sizeof(int), cudaMemcpyDeviceToHost)) != cudaSuccess)
+    return cuda_fail(c, e, "reading error word");
+  if (word != 0) {
+    cudaMemset(c->d_err, 0, sizeof(int));
+    return fail(c, PRM_ERR_TIMEOUT, "a device-side wait gave up (error word " + std::to_string(word) + ")");
+  }
+  return PRM_OK;
+}
+
+int prm_profile(prm_ctx* c, int enable) {
+  if (c == nullptr) return fail(nullptr, PRM_ERR_INVALID_ARG, "ctx is NULL");
+  DeviceGuard guard(c->device);
+  if (enable) c->prof.reset();
+  c->prof.on = enable != 0;
+  return PRM_OK;
+}
+
+int prm_profile_read(prm_ctx* c, int family, double* total_ms, int64_t* records, int64_t* kernels,
+                     double* work) {
+  if (c == nullptr) return fail(nullptr, PRM_ERR_INVALID_ARG, "ctx is NULL");
+  if (family < -1 || family >= PRM_FAMILY_COUNT) return fail(c, PRM_ERR_INVALID_ARG, "unknown family");
+  DeviceGuard guard(c->device);
+  double ms = 0, w = 0;
+  int64_t n = 0, k = 0;
+  for (const auto& r : c->prof.recs) {
+    if (family != -1 && r.family != family) continue;
+    cudaError_t e = cudaEventSynchronize(c->prof.pool[r.ev + 1]);
+    if (e != cudaSuccess) return cuda_fail(c, e, "event synchronize");
+    float dt = 0.f;
+    if ((e = cudaEventElapsedTime(&dt, c->prof.pool[r.ev], c->prof.pool[r.ev + 1])) != cudaSuccess)
+      return cuda_fail(c, e, "event elapsed time");
+    ms += dt;
+    w += r.work;
+    ++n;
+    k += r.kernels;
+  }
+  if (total_ms) *total_ms = ms;
+  if (records) *records = n;
+  if (kernels) *kernels = k;
+  if (work) *work = w;
+  return PRM_OK;
+}
+
+const char* prm_last_error(const prm_ctx* c) {
+  if (c == nullptr) return g_create_error.c_str();
+  return c->err.c_str();
+}
+
+// ---------------------------------------------------------------- standalone
+int prm_ns_gram(const uint16_t* X, uint16_t* A, const float* scale, int batch, int64_t r, int64_t c, int64_t ldc,
+                int64_t ldr, void* stream) {
+  if (X == nullptr || A == nullptr || batch < 0 || r < 1 || c < r || ldc < c || ldr < r) return PRM_ERR_INVALID_ARG;
+  if (ldc % 8 || ldr % 8 || !aligned16(X) || !aligned16(A)) return PRM_ERR_ALIGNMENT;
+  if (batch == 0) return PRM_OK;
+  DeviceState* ds;
+  int rc = device_state(&ds);
+  if (rc != PRM_OK) return rc;
+  NsMaps mx;
+  if (encode_x_maps(&mx, X, batch, r, c, ldc) != 0) return PRM_ERR_CUDA;
+  GemmLaunch g{};
+  g.batch = batch;
+  g.r = r;
+  g.c = c;
+  g.ldc = ldc;
+  g.ldr = ldr;
+  g.scale = scale;
+  g.err = ds->d_err;
+  g.num_sms = ds->num_sms;
+  return launch_gram(mx, A, g, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PRM_OK : PRM_ERR_CUDA;
+}
+
+int prm_ns_poly(const uint16_t* A, uint16_t* B, float b, float cc, int batch, int64_t r, int64_t ldr,
+                void* stream) {
+  if (A == nullptr || B == nullptr || batch < 0 || r < 1 || ldr < r) return PRM_ERR_INVALID_ARG;
+  if (ldr % 8 || !aligned16(A) || !aligned16(B)) return PRM_ERR_ALIGNMENT;
+  if (batch == 0) return PRM_OK;
+  DeviceState* ds;
+  int rc = device_state(&ds);
+  if (rc != PRM_OK) return rc;
+  SymMaps ma;
+  if (encode_sym_maps(&ma, A, batch, r, ldr) != 0) return PRM_ERR_CUDA;
+  GemmLaunch g{};
+  g.batch = batch;
+  g.r = r;
+  g.c = r;
+  g.ldc = ldr;
+  g.ldr = ldr;
+  g.cb = b;
+  g.cc = cc;
+  g.err = ds->d_err;
+  g.num_sms = ds->num_sms;
+  return launch_poly(ma, A, B, g, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PRM_OK : PRM_ERR_CUDA;
+}
+
+int prm_ns_combine(const uint16_t* X, const uint16_t* B, uint16_t* Xout, const float* scale, float a, int batch,
+                   int64_t r, int64_t c, int64_t ldc, int64_t ldr, void* stream) {
+  if (X == nullptr || B == nullptr || Xout == nullptr || batch < 0 || r < 1 || c < r || ldc < c || ldr < r)
+    return PRM_ERR_INVALID_ARG;
+  if (X == Xout) return PRM_ERR_INVALID_ARG;
+  if (ldc % 8 || ldr % 8 || !aligned16(X) || !aligned16(B) || !aligned16(Xout)) return PRM_ERR_ALIGNMENT;
+  if (batch == 0) return PRM_OK;
+  DeviceState* ds;
+  int rc = device_state(&ds);
+  if (rc != PRM_OK) return rc;
+  NsMaps mx;
+  SymMaps mb;
+  if (encode_x_maps(&mx, X, batch, r, c, ldc) != 0 || encode_sym_maps(&mb, B, batch, r, ldr) != 0)
+    return PRM_ERR_CUDA;
+  GemmLaunch g{};
+  g.batch = batch;
+  g.r = r;
+  g.c = c;
+  g.ldc = ldc;
+  g.ldr = ldr;
+  g.scale = scale;
+  g.ca = a;
+  g.err = ds->d_err;
+  g.num_sms = ds->num_sms;
+  return launch_combine(mb, mx, X, Xout, g, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PRM_OK
+                                                                                                : PRM_ERR_CUDA;
+}
+
+static void standalone_group(int batch, int64_t m, int64_t n, NsPlan& plan) {
+  std::vector<View> views(batch);
+  for (int i = 0; i < batch; ++i) {
+    views[i] = View{};
+    views[i].rows = m;
+    views[i].cols = n;
+    views[i].ld = n;
+  }
+  build_ns_plan(views, plan);
+}
+
+int prm_newton_schulz_workspace(int batch, int64_t m, int64_t n, size_t* bytes) {
+  if (bytes == nullptr || batch < 0 || m < 1 || n < 1) return PRM_ERR_INVALID_ARG;
+  if (batch == 0) {
+    *bytes = 0;
+    return PRM_OK;
+  }
+  NsPlan plan;
+  standalone_group(batch, m, n, plan);
+  *bytes = plan.bytes;
+  return PRM_OK;
+}
+
+int prm_newton_schulz(const float* in, float* out, int batch, int64_t m, int64_t n, const float* ns_coeffs,
+                      int steps, void* workspace, size_t ws_bytes, void* stream) {
+  if (in == nullptr || out == nullptr || batch < 0 || m < 1 || n < 1 || steps < 1) return PRM_ERR_INVALID_ARG;
+  if (!aligned16(in) || !aligned16(out) || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return PRM_ERR_ALIGNMENT;
+  if (batch == 0) return PRM_OK;
+  float coeffs[3] = {DEFAULT_COEFFS[0], DEFAULT_COEFFS[1], DEFAULT_COEFFS[2]};
+  if (ns_coeffs)
+    for (int i = 0; i < 3; ++i) coeffs[i] = ns_coeffs[i];
+  DeviceState* ds;
+  int rc = device_state(&ds);
+  if (rc != PRM_OK) return rc;
+  NsPlan plan;
+  std::vector<View> views(batch);
+  for (int i = 0; i < batch; ++i) {
+    View v{};
+    v.M = const_cast<float*>(in) + static_cast<int64_t>(i) * m * n;
+    v.out = out + static_cast<int64_t>(i) * m * n;
+    v.rows = m;
+    v.cols = n;
+    v.ld = n;
+    v.shape_scale = 1.f;
+    views[i] = v;
+  }
+  build_ns_plan(views, plan);
+  if (workspace == nullptr || ws_bytes < plan.bytes) return PRM_ERR_WORKSPACE;
+  if (upload_sets(plan.groups[0].sets) != cudaSuccess) {
+    free_plan(plan);
+    return PRM_ERR_CUDA;
+  }
+  prm_ctx tmp;
+  tmp.num_sms = ds->num_sms;
+  tmp.d_err = ds->d_err;
+  rc = run_ns(&tmp, plan, workspace, false, 0.f, 1.f, 1.f, coeffs, steps, static_cast<cudaStream_t>(stream));
+  // The launch tables must outlive the kernels that read them.
+  cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  free_plan(plan);
+  tmp.d_err = nullptr;
+  return rc;
+}
+
+}  // extern "C"

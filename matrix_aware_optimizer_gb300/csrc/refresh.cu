@@ -1,0 +1,295 @@
+// Memory-bound kernels around the NS5 refresh ("Scaling Muon for Diffusion
+// Transformers", PaperDaily walkthrough, section "Periodic Row-wise Muon":
+// on steps with t % K == 0 the direction is NS5 of the momentum).
+//
+//   prep   : M <- beta M + G (in place), X0 = bf16(M) in the wide orientation
+//            (tall views are transposed through shared memory), and per-CTA
+//            partial sums of M^2 for the Frobenius pre-normalisation. The
+//            scale 1 / (||M||_F + eps) is not applied here: the first GRAM
+//            epilogue multiplies by its square and the first COMBINE epilogue
+//            by the scale itself, which is the same NS5 round on M / ||M||.
+//   finish : per-view scale = 1 / (sqrt(sum of partials) + eps_ns).
+//   apply  : W <- W * (1 - lr wd) - eta * s * D with D = X5 (bf16), read
+//            transposed back for tall views.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "internal.h"
+
+namespace prm {
+namespace {
+
+constexpr int PREP_THREADS = 256;
+constexpr int TILE = 64;  // transpose tile edge for tall views
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+__device__ __forceinline__ float block_sum256(float v, float* red) {
+  const int t = threadIdx.x + threadIdx.y * blockDim.x;
+  const int lane = t & 31, warp = t >> 5;
+  v = warp_sum(v);
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  if (warp == 0) {
+    v = lane < PREP_THREADS / 32 ? red[lane] : 0.f;
+    v = warp_sum(v);
+    if (lane == 0) red[32] = v;
+  }
+  __syncthreads();
+  return red[32];
+}
+
+__device__ __forceinline__ uint16_t bf16_bits(float v) {
+  const __nv_bfloat16 h = __float2bfloat16_rn(v);
+  return *reinterpret_cast<const uint16_t*>(&h);
+}
+
+__device__ __forceinline__ float bf16_to_float(uint32_t bits16) { return __uint_as_float(bits16 << 16); }
+
+template <bool BF16>
+__device__ __forceinline__ float grad_at(const void* G, int64_t off) {
+  if (BF16) return bf16_to_float(static_cast<const uint16_t*>(G)[off]);
+  return static_cast<const float*>(G)[off];
+}
+
+// ---------------------------------------------------------------- prep
+// Wide views: one CTA per row, X row = same row.
+template <bool BF16, bool VEC, bool UPDATE>
+__global__ void __launch_bounds__(PREP_THREADS) prep_wide_kernel(const View* __restrict__ views, int64_t cols,
+                                                                 float beta, uint16_t* __restrict__ X,
+                                                                 int64_t ldc, int64_t x_stride,
+                                                                 float* __restrict__ partials, int64_t slots) {
+  __shared__ float red[33];
+  const View v = views[blockIdx.y];
+  const int64_t row = blockIdx.x;
+  float* Mr = v.M + row * v.ld;
+  uint16_t* Xr = X + v.slot * x_stride + row * ldc;
+  float ss = 0.f;
+  if constexpr (VEC) {
+    for (int64_t c = threadIdx.x * 4; c < cols; c += PREP_THREADS * 4) {
+      float4 m = *reinterpret_cast<const float4*>(Mr + c);
+      if constexpr (UPDATE) {
+        const int64_t go = row * v.ld + c;
+        float4 g;
+        if constexpr (BF16) {
+          const uint2 u = __ldcs(reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(v.G) + go));
+          g = make_float4(bf16_to_float(u.x & 0xFFFFu), bf16_to_float(u.x >> 16), bf16_to_float(u.y & 0xFFFFu),
+                          bf16_to_float(u.y >> 16));
+        } else {
+          g = __ldcs(reinterpret_cast<const float4*>(static_cast<const float*>(v.G) + go));
+        }
+        m.x = fmaf(beta, m.x, g.x);
+        m.y = fmaf(beta, m.y, g.y);
+        m.z = fmaf(beta, m.z, g.z);
+        m.w = fmaf(beta, m.w, g.w);
+        *reinterpret_cast<float4*>(Mr + c) = m;
+      }
+      ss = fmaf(m.x, m.x, ss);
+      ss = fmaf(m.y, m.y, ss);
+      ss = fmaf(m.z, m.z, ss);
+      ss = fmaf(m.w, m.w, ss);
+      uint2 packed;
+      packed.x = static_cast<uint32_t>(bf16_bits(m.x)) | (static_cast<uint32_t>(bf16_bits(m.y)) << 16);
+      packed.y = static_cast<uint32_t>(bf16_bits(m.z)) | (static_cast<uint32_t>(bf16_bits(m.w)) << 16);
+      *reinterpret_cast<uint2*>(Xr + c) = packed;
+    }
+  } else {
+    for (int64_t c = threadIdx.x; c < cols; c += PREP_THREADS) {
+      float m = Mr[c];
+      if constexpr (UPDATE) {
+        m = fmaf(beta, m, grad_at<BF16>(v.G, row * v.ld + c));
+        Mr[c] = m;
+      }
+      ss = fmaf(m, m, ss);
+      Xr[c] = bf16_bits(m);
+    }
+  }
+  const float total = block_sum256(ss, red);
+  if (threadIdx.x == 0) partials[static_cast<int64_t>(v.slot) * slots + row] = total;
+}
+
+// Tall views (rows > cols): 64 x 64 tiles, X[j][i] = bf16(M[i][j]).
+template <bool BF16, bool UPDATE>
+__global__ void __launch_bounds__(PREP_THREADS) prep_tall_kernel(const View* __restrict__ views, int64_t rows,
+                                                                 int64_t cols, float beta,
+                                                                 uint16_t* __restrict__ X, int64_t ldc,
+                                                                 int64_t x_stride, float* __restrict__ partials,
+                                                                 int64_t slots) {
+  __shared__ float tile[TILE][TILE + 1];
+  __shared__ float red[33];
+  const View v = views[blockIdx.z];
+  const int tx = threadIdx.x;  // 0..63 along columns
+  const int ty = threadIdx.y;  // 0..3
+  const int64_t i0 = static_cast<int64_t>(blockIdx.y) * TILE;
+  const int64_t j0 = static_cast<int64_t>(blockIdx.x) * TILE;
+  float ss = 0.f;
+  for (int ii = ty; ii < TILE; ii += 4) {
+    const int64_t i = i0 + ii, j = j0 + tx;
+    float m = 0.f;
+    if (i < rows && j < cols) {
+      float* Mp = v.M + i * v.ld + j;
+      m = *Mp;
+      if constexpr (UPDATE) {
+        m = fmaf(beta, m, grad_at<BF16>(v.G, i * v.ld + j));
+        *Mp = m;
+      }
+      ss = fmaf(m, m, ss);
+    }
+    tile[ii][tx] = m;
+  }
+  __syncthreads();
+  uint16_t* Xv = X + v.slot * x_stride;
+  for (int jj = ty; jj < TILE; jj += 4) {
+    const int64_t j = j0 + jj, i = i0 + tx;
+    if (j < cols && i < rows) Xv[j * ldc + i] = bf16_bits(tile[tx][jj]);
+  }
+  const float total = block_sum256(ss, red);
+  if (tx == 0 && ty == 0)
+    partials[static_cast<int64_t>(v.slot) * slots + blockIdx.y * gridDim.x + blockIdx.x] = total;
+}
+
+__global__ void __launch_bounds__(256) norm_finish_kernel(const float* __restrict__ partials, int64_t slots,
+                                                          float* __restrict__ scale, float ns_eps) {
+  __shared__ float red[33];
+  const float* p = partials + static_cast<int64_t>(blockIdx.x) * slots;
+  float s = 0.f;
+  for (int64_t k = threadIdx.x; k < slots; k += 256) s += p[k];
+  const float total = block_sum256(s, red);
+  if (threadIdx.x == 0) scale[blockIdx.x] = 1.f / (sqrtf(total) + ns_eps);
+}
+
+// ---------------------------------------------------------------- apply
+template <bool VEC>
+__global__ void __launch_bounds__(PREP_THREADS) apply_wide_kernel(const View* __restrict__ views, int64_t cols,
+                                                                  const uint16_t* __restrict__ X, int64_t ldc,
+                                                                  int64_t x_stride, float decay, float eta) {
+  const View v = views[blockIdx.y];
+  const int64_t row = blockIdx.x;
+  const uint16_t* Xr = X + v.slot * x_stride + row * ldc;
+  const float step = eta * v.shape_scale;
+  if (v.W == nullptr) {
+    float* Or = v.out + row * v.ld;
+    for (int64_t c = threadIdx.x; c < cols; c += PREP_THREADS) Or[c] = bf16_to_float(Xr[c]);
+    return;
+  }
+  float* Wr = v.W + row * v.ld;
+  if constexpr (VEC) {
+    for (int64_t c = threadIdx.x * 4; c < cols; c += PREP_THREADS * 4) {
+      const uint2 u = *reinterpret_cast<const uint2*>(Xr + c);
+      float4 w = *reinterpret_cast<const float4*>(Wr + c);
+      w.x = fmaf(w.x, decay, -step * bf16_to_float(u.x & 0xFFFFu));
+      w.y = fmaf(w.y, decay, -step * bf16_to_float(u.x >> 16));
+      w.z = fmaf(w.z, decay, -step * bf16_to_float(u.y & 0xFFFFu));
+      w.w = fmaf(w.w, decay, -step * bf16_to_float(u.y >> 16));
+      *reinterpret_cast<float4*>(Wr + c) = w;
+    }
+  } else {
+    for (int64_t c = threadIdx.x; c < cols; c += PREP_THREADS) Wr[c] = fmaf(Wr[c], decay, -step * bf16_to_float(Xr[c]));
+  }
+}
+
+__global__ void __launch_bounds__(PREP_THREADS) apply_tall_kernel(const View* __restrict__ views, int64_t rows,
+                                                                  int64_t cols, const uint16_t* __restrict__ X,
+                                                                  int64_t ldc, int64_t x_stride, float decay,
+                                                                  float eta) {
+  __shared__ float tile[TILE][TILE + 1];
+  const View v = views[blockIdx.z];
+  const int tx = threadIdx.x, ty = threadIdx.y;
+  const int64_t i0 = static_cast<int64_t>(blockIdx.y) * TILE;
+  const int64_t j0 = static_cast<int64_t>(blockIdx.x) * TILE;
+  const uint16_t* Xv = X + v.slot * x_stride;
+  // X is cols x rows (wide orientation): coalesced along i.
+  for (int jj = ty; jj < TILE; jj += 4) {
+    const int64_t j = j0 + jj, i = i0 + tx;
+    tile[jj][tx] = (j < cols && i < rows) ? bf16_to_float(Xv[j * ldc + i]) : 0.f;
+  }
+  __syncthreads();
+  const float step = eta * v.shape_scale;
+  for (int ii = ty; ii < TILE; ii += 4) {
+    const int64_t i = i0 + ii, j = j0 + tx;
+    if (i < rows && j < cols) {
+      const float d = tile[tx][ii];
+      if (v.W == nullptr) {
+        v.out[i * v.ld + j] = d;
+      } else {
+        float* Wp = v.W + i * v.ld + j;
+        *Wp = fmaf(*Wp, decay, -step * d);
+      }
+    }
+  }
+}
+
+}  // namespace
+
+int64_t prep_slots(int64_t rows, int64_t cols) {
+  if (rows <= cols) return rows;
+  return ((rows + TILE - 1) / TILE) * ((cols + TILE - 1) / TILE);
+}
+
+cudaError_t launch_prep(const View* d_views, int count, int64_t rows, int64_t cols, bool vec_ok, bool grad_bf16,
+                        bool update_momentum, float beta, uint16_t* X, int64_t ldc, int64_t x_mat_stride,
+                        float* partials, int64_t slots, cudaStream_t stream) {
+  if (count == 0) return cudaSuccess;
+  if (rows <= cols) {
+    const dim3 grid(static_cast<unsigned>(rows), static_cast<unsigned>(count));
+#define PRM_PREP_WIDE(B, V, U) \
+  prep_wide_kernel<B, V, U><<<grid, PREP_THREADS, 0, stream>>>(d_views, cols, beta, X, ldc, x_mat_stride, partials, slots)
+    if (!update_momentum) {
+      if (vec_ok) PRM_PREP_WIDE(false, true, false);
+      else PRM_PREP_WIDE(false, false, false);
+    } else if (grad_bf16) {
+      if (vec_ok) PRM_PREP_WIDE(true, true, true);
+      else PRM_PREP_WIDE(true, false, true);
+    } else {
+      if (vec_ok) PRM_PREP_WIDE(false, true, true);
+      else PRM_PREP_WIDE(false, false, true);
+    }
+#undef PRM_PREP_WIDE
+  } else {
+    const dim3 block(TILE, 4);
+    const dim3 grid(static_cast<unsigned>((cols + TILE - 1) / TILE), static_cast<unsigned>((rows + TILE - 1) / TILE),
+                    static_cast<unsigned>(count));
+    if (!update_momentum)
+      prep_tall_kernel<false, false><<<grid, block, 0, stream>>>(d_views, rows, cols, beta, X, ldc, x_mat_stride,
+                                                                 partials, slots);
+    else if (grad_bf16)
+      prep_tall_kernel<true, true><<<grid, block, 0, stream>>>(d_views, rows, cols, beta, X, ldc, x_mat_stride,
+                                                               partials, slots);
+    else
+      prep_tall_kernel<false, true><<<grid, block, 0, stream>>>(d_views, rows, cols, beta, X, ldc, x_mat_stride,
+                                                                partials, slots);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_norm_finish(const float* partials, int64_t slots, float* scale, int count, float ns_eps,
+                               cudaStream_t stream) {
+  if (count == 0) return cudaSuccess;
+  norm_finish_kernel<<<count, 256, 0, stream>>>(partials, slots, scale, ns_eps);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_apply(const View* d_views, int count, int64_t rows, int64_t cols, bool vec_ok, const uint16_t* X,
+                         int64_t ldc, int64_t x_mat_stride, float decay, float eta, cudaStream_t stream) {
+  if (count == 0) return cudaSuccess;
+  if (rows <= cols) {
+    const dim3 grid(static_cast<unsigned>(rows), static_cast<unsigned>(count));
+    if (vec_ok)
+      apply_wide_kernel<true><<<grid, PREP_THREADS, 0, stream>>>(d_views, cols, X, ldc, x_mat_stride, decay, eta);
+    else
+      apply_wide_kernel<false><<<grid, PREP_THREADS, 0, stream>>>(d_views, cols, X, ldc, x_mat_stride, decay, eta);
+  } else {
+    const dim3 block(TILE, 4);
+    const dim3 grid(static_cast<unsigned>((cols + TILE - 1) / TILE), static_cast<unsigned>((rows + TILE - 1) / TILE),
+                    static_cast<unsigned>(count));
+    apply_tall_kernel<<<grid, block, 0, stream>>>(d_views, rows, cols, X, ldc, x_mat_stride, decay, eta);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace prm

@@ -1,0 +1,110 @@
+"""torch glue over the C ABI: PyTorch supplies device memory (the tensors and
+the workspace) and the stream; every arithmetic step runs in libprm."""
+from __future__ import annotations
+
+from typing import Optional, Sequence
+
+import torch
+
+from . import native as N
+
+_MODES = {"prmuon": N.PRM_MODE_PRMUON, "muonbp": N.PRM_MODE_MUONBP}
+
+
+def _stream_handle(stream: Optional[torch.cuda.Stream]) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return int(s.cuda_stream)
+
+
+class PeriodicRowMuon:
+    """Periodic Row-wise Muon (and MuonBP) over a list of 2-D fp32 parameters.
+
+    params / momenta : fp32 CUDA tensors, updated in place.
+    grads            : bf16 or fp32 CUDA tensors with the same shapes (read).
+    muonbp_blocks    : 0, or P > 0 to also plan MuonBP blocks.
+    shape_scales     : optional per-matrix step multipliers (default
+                       sqrt(max(1, rows / cols))).
+    """
+
+    def __init__(self, params: Sequence[torch.Tensor], momenta: Sequence[torch.Tensor],
+                 grads: Sequence[torch.Tensor], muonbp_blocks: int = 0,
+                 shape_scales: Optional[Sequence[float]] = None):
+        if not (len(params) == len(momenta) == len(grads)):
+            raise ValueError("params, momenta and grads must have the same length")
+        dev = params[0].device if params else torch.device("cuda", torch.cuda.current_device())
+        if dev.type != "cuda":
+            raise ValueError("tensors must live on a CUDA device")
+        descs = []
+        for i, (w, m, g) in enumerate(zip(params, momenta, grads)):
+            if w.dim() != 2 or w.shape != m.shape or w.shape != g.shape:
+                raise ValueError(f"matrix {i}: param, momentum and grad must be 2-D with one shape")
+            if w.dtype != torch.float32 or m.dtype != torch.float32:
+                raise ValueError(f"matrix {i}: param and momentum must be float32")
+            if g.dtype not in (torch.bfloat16, torch.float32):
+                raise ValueError(f"matrix {i}: grad must be bfloat16 or float32")
+            for t in (w, m, g):
+                if not t.is_contiguous() or t.device != dev:
+                    raise ValueError(f"matrix {i}: tensors must be contiguous and on {dev}")
+            d = N.prm_matrix_desc()
+            d.param, d.momentum, d.grad = w.data_ptr(), m.data_ptr(), g.data_ptr()
+            d.grad_dtype = N.PRM_BF16 if g.dtype == torch.bfloat16 else N.PRM_FP32
+            d.rows, d.cols = w.shape
+            d.shape_scale = 0.0 if shape_scales is None else float(shape_scales[i])
+            descs.append(d)
+        self.device = dev
+        self._tensors = (list(params), list(momenta), list(grads))
+        with torch.cuda.device(dev):
+            self.ctx = N.prm_create(dev.index if dev.index is not None else torch.cuda.current_device())
+            try:
+                N.prm_register_matrices(self.ctx, descs, muonbp_blocks)
+                nbytes = N.prm_workspace_bytes(self.ctx)
+                self.workspace = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=dev)
+                N.prm_set_workspace(self.ctx, self.workspace.data_ptr(), self.workspace.numel())
+            except Exception:
+                N.prm_destroy(self.ctx)
+                self.ctx = None
+                raise
+        self.muonbp_blocks = muonbp_blocks
+
+    @property
+    def workspace_bytes(self) -> int:
+        return self.workspace.numel()
+
+    def step(self, t: int, K: int = 3, gamma: float = 0.15, lr: float = 0.02, wd: float = 0.01,
+             beta: float = 0.95, eps: float = 1e-8, ns_coeffs=None, mode: str = "prmuon",
+             stream: Optional[torch.cuda.Stream] = None) -> int:
+        """Enqueues step t; returns the branch taken (1 = NS5 refresh / full)."""
+        N.prm_step(self.ctx, t, K, gamma, lr, wd, beta, eps, ns_coeffs, _MODES[mode], _stream_handle(stream))
+        return N.prm_branch(t, K, _MODES[mode])
+
+    def sync_status(self, stream: Optional[torch.cuda.Stream] = None) -> None:
+        N.check(N.prm_sync_status(self.ctx, _stream_handle(stream)), "prm_sync_status", self.ctx)
+
+    def close(self) -> None:
+        if getattr(self, "ctx", None) is not None:
+            N.prm_destroy(self.ctx)
+            self.ctx = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def newton_schulz(x: torch.Tensor, steps: int = 5, ns_coeffs=None,
+                  stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """NS iterations of a batch of fp32 matrices [batch, m, n] (or one [m, n])
+    on the tensor cores; tall matrices are orthogonalised transposed."""
+    squeeze = x.dim() == 2
+    xb = x.unsqueeze(0) if squeeze else x
+    if xb.dtype != torch.float32 or not xb.is_cuda:
+        raise ValueError("x must be a float32 CUDA tensor")
+    xb = xb.contiguous()
+    b, m, n = xb.shape
+    out = torch.empty_like(xb)
+    nbytes = N.prm_newton_schulz_workspace(b, m, n)
+    ws = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=xb.device)
+    N.prm_newton_schulz(xb.data_ptr(), out.data_ptr(), b, m, n, ns_coeffs, steps, ws.data_ptr(), ws.numel(),
+                        _stream_handle(stream))
+    return out[0] if squeeze else out

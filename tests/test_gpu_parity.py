@@ -1,0 +1,254 @@
+"""Parity of the CUDA optimizer step (through the C ABI) with the fp64 oracle
+on the same seeded inputs.
+
+Tolerances (relative Frobenius error unless stated):
+  momentum M after a step                      <= 1e-6   (fp32 fma vs fp64)
+  parameter W after a RowNorm step             <= 1e-5
+  RowNorm direction recovered from the update  <= 1e-4   (limited by fp32 W)
+  NS5 direction (bf16 operands, fp32 accum.)   <= 2e-2
+  branch schedule                               exact
+Checks are teacher-forced: before every step the oracle receives the GPU's
+own state, so each step is judged on its own."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from matrix_aware_optimizer_gb300 import native as N
+from matrix_aware_optimizer_gb300 import synth
+from matrix_aware_optimizer_gb300.optimizer import PeriodicRowMuon, newton_schulz
+
+from .gpu_helpers import direction_from_update, ensure_built, host64, rel_frob
+
+pytestmark = pytest.mark.gpu
+
+TOL_M = 1e-6
+TOL_W_ROWNORM = 1e-5
+TOL_D_ROWNORM = 1e-4
+TOL_D_NS5 = 2e-2
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    ensure_built()
+    N.load()
+
+
+def _hp(ms):
+    return dict(K=ms.K, gamma=ms.gamma, lr=ms.lr, wd=ms.wd, beta=ms.beta, eps=ms.eps)
+
+
+def _run_teacher_forced(ms, steps, check_idx=None, mode="prmuon", blocks=0):
+    shapes = ms.shapes
+    Ws, Ms = synth.make_state(ms, device="cuda")
+    gdt = torch.bfloat16 if ms.grad_dtype == synth.GRAD_BF16 else torch.float32
+    grads = [torch.empty(s, device="cuda", dtype=gdt) for s in shapes]
+    opt = PeriodicRowMuon(Ws, Ms, grads, muonbp_blocks=blocks)
+    hp = _hp(ms)
+    idx = range(len(shapes)) if check_idx is None else check_idx
+    report = []
+    for t in steps:
+        for i, g in enumerate(grads):
+            synth.make_grad(shapes[i], ms.seed, t, i, ms.grad_std, ms.grad_dtype, ms.row_sigma, device="cuda", out=g)
+        torch.cuda.synchronize()
+        prev = {i: (host64(Ws[i]), host64(Ms[i]), host64(grads[i])) for i in idx}
+        branch = opt.step(t, K=ms.K, gamma=ms.gamma, lr=ms.lr, wd=ms.wd, beta=ms.beta, eps=ms.eps, mode=mode)
+        opt.sync_status()
+        assert branch == O.refresh_indicator(t, ms.K)
+        for i in idx:
+            W0, M0, G0 = prev[i]
+            m, n = shapes[i]
+            s = O.lr_shape_scale(m, n)
+            if mode == "prmuon":
+                W1, M1, D1, rho = O.prmuon_step(W0, M0, G0, t, **hp)
+            else:
+                W1, M1, D1, rho = O.muonbp_step(W0, M0, G0, t, P=blocks, **hp)
+            assert rho == branch
+            Wg, Mg = host64(Ws[i]), host64(Ms[i])
+            eta = ms.lr if rho else ms.lr * ms.gamma
+            Dg = direction_from_update(W0, Wg, ms.lr, ms.wd, eta, s)
+            eM, eW, eD = rel_frob(Mg, M1), rel_frob(Wg, W1), rel_frob(Dg, D1)
+            report.append((t, i, rho, eM, eW, eD))
+            assert eM <= TOL_M, (t, i, eM)
+            if rho == 0 and mode == "prmuon":
+                assert eW <= TOL_W_ROWNORM, (t, i, eW)
+                assert eD <= TOL_D_ROWNORM, (t, i, eD)
+            else:
+                assert eD <= TOL_D_NS5, (t, i, eD)
+    opt.close()
+    return report
+
+
+def test_tiny_set_six_steps():
+    """4 fp32 matrices (one tall, one ragged 128x96), K=3, 6 steps: two
+    refresh cycles."""
+    rep = _run_teacher_forced(synth.MATRIX_SETS["tiny"], range(6))
+    assert [r[2] for r in rep[::4]] == [1, 0, 0, 1, 0, 0]
+
+
+def test_dit_block_d2048_full_size():
+    """The one-DiT-block set at full size (bf16 grads): a refresh step and two
+    RowNorm steps on every matrix, including the tall 8192x2048."""
+    _run_teacher_forced(synth.MATRIX_SETS["dit_block_d2048"], range(3))
+
+
+def test_free_running_tiny_matches_oracle():
+    """Six steps without teacher forcing: the trajectories stay close (the
+    bf16 NS5 error enters W through lr * D only)."""
+    ms = synth.MATRIX_SETS["tiny"]
+    Ws, Ms = synth.make_state(ms, device="cuda")
+    W0 = [host64(w) for w in Ws]
+    grads = [torch.empty(s, device="cuda") for s in ms.shapes]
+    opt = PeriodicRowMuon(Ws, Ms, grads)
+    host_grads = {}
+    for t in range(ms.steps):
+        for i, g in enumerate(grads):
+            synth.make_grad(ms.shapes[i], ms.seed, t, i, ms.grad_std, ms.grad_dtype, ms.row_sigma, device="cuda", out=g)
+            host_grads[(t, i)] = host64(g)
+        opt.step(t, K=ms.K, gamma=ms.gamma, lr=ms.lr, wd=ms.wd, beta=ms.beta, eps=ms.eps)
+    opt.sync_status()
+    Wo, Mo, br = O.run_steps(W0, [np.zeros(s) for s in ms.shapes], lambda t, i: host_grads[(t, i)], 0, ms.steps,
+                             ms.K, ms.gamma, ms.lr, ms.wd, ms.beta, ms.eps)
+    assert br == [1, 0, 0, 1, 0, 0]
+    for i in range(len(ms.shapes)):
+        assert rel_frob(host64(Ms[i]), Mo[i]) <= 1e-6
+        assert rel_frob(host64(Ws[i]), Wo[i]) <= 5e-3
+    opt.close()
+
+
+EDGE_SHAPES = [(1, 300), (300, 1), (37, 104), (100, 40), (129, 257), (257, 129), (8, 8), (64, 4100), (2, 3)]
+
+
+@pytest.mark.parametrize("gdtype", [torch.float32, torch.bfloat16])
+def test_edge_shapes_directions(gdtype):
+    """Ragged, degenerate and odd shapes, zero vectors and vectors below eps:
+    with W = 0 and wd = 0 the update is exactly -eta s D, so D is read back
+    directly."""
+    gen = torch.Generator().manual_seed(3)
+    eps = 1e-8
+    for t, K in ((1, 3), (0, 3)):
+        Ws, Ms, Gs, Gh = [], [], [], []
+        for (m, n) in EDGE_SHAPES:
+            G = torch.randn(m, n, generator=gen)
+            if m <= n and m >= 3:
+                G[1] = 0.0            # a zero row
+                G[2] *= 1e-11         # a row below eps
+            elif m > n and n >= 3:
+                G[:, 1] = 0.0
+                G[:, 2] *= 1e-11
+            Gd = G.to(gdtype)
+            Gh.append(Gd.double().numpy())
+            Gs.append(Gd.cuda())
+            Ws.append(torch.zeros(m, n, device="cuda"))
+            Ms.append(torch.zeros(m, n, device="cuda"))
+        opt = PeriodicRowMuon(Ws, Ms, Gs)
+        opt.step(t, K=K, gamma=0.5, lr=0.1, wd=0.0, beta=0.9, eps=eps)
+        opt.sync_status()
+        for i, (m, n) in enumerate(EDGE_SHAPES):
+            s = O.lr_shape_scale(m, n)
+            eta = 0.1 if t % K == 0 else 0.05
+            Dg = -host64(Ws[i]) / (eta * s)
+            if t % K == 0:
+                Do = O.newton_schulz(Gh[i])
+                assert rel_frob(Dg, Do) <= TOL_D_NS5, ((m, n), rel_frob(Dg, Do))
+            else:
+                Do = O.row_normalize(Gh[i], eps)
+                assert rel_frob(Dg, Do) <= 1e-6, ((m, n), rel_frob(Dg, Do))
+                assert np.all(Dg[Do == 0] == 0)
+        opt.close()
+
+
+def test_muonbp_block_and_full_steps():
+    """MuonBP with P = 4: block steps orthogonalise each block on its own
+    (wide and tall blocks, a square parent), full steps the whole matrix."""
+    shapes = [(256, 1024), (1024, 256), (384, 384), (96, 640), (200, 72)]
+    gen = torch.Generator().manual_seed(9)
+    for t in (1, 3):
+        Gh = [torch.randn(s, generator=gen) for s in shapes]
+        Ws = [torch.zeros(s, device="cuda") for s in shapes]
+        Ms = [torch.zeros(s, device="cuda") for s in shapes]
+        Gs = [g.cuda() for g in Gh]
+        opt = PeriodicRowMuon(Ws, Ms, Gs, muonbp_blocks=4)
+        assert opt.step(t, K=3, gamma=1.25, lr=0.016, wd=0.0, beta=0.9, eps=1e-8, mode="muonbp") == (t % 3 == 0)
+        opt.sync_status()
+        for i, (m, n) in enumerate(shapes):
+            _, _, Do, full = O.muonbp_step(np.zeros((m, n)), np.zeros((m, n)), Gh[i].double().numpy(), t, 3, 1.25,
+                                           0.016, 0.0, 0.9, 1e-8, 4)
+            eta = 0.016 if full else 0.016 * 1.25
+            Dg = -host64(Ws[i]) / (eta * O.lr_shape_scale(m, n))
+            assert rel_frob(Dg, Do) <= TOL_D_NS5, ((m, n), t, rel_frob(Dg, Do))
+        opt.close()
+
+
+def test_resume_is_bitwise():
+    """The optimizer state is (M, t): six steps equal three steps, a fresh
+    context, and three more steps, bit for bit."""
+    ms = synth.MatrixSet(name="resume", shapes=((128, 384), (384, 128), (256, 256)), grad_dtype=synth.GRAD_BF16,
+                         grad_std=1e-3, steps=6)
+
+    def run(split):
+        Ws, Ms = synth.make_state(ms, device="cuda")
+        grads = [torch.empty(s, device="cuda", dtype=torch.bfloat16) for s in ms.shapes]
+        opt = PeriodicRowMuon(Ws, Ms, grads)
+        for t in range(6):
+            if t == split:
+                opt.close()
+                opt = PeriodicRowMuon(Ws, Ms, grads)
+            for i, g in enumerate(grads):
+                synth.make_grad(ms.shapes[i], 0, t, i, 1e-3, synth.GRAD_BF16, device="cuda", out=g)
+            opt.step(t)
+        opt.sync_status()
+        opt.close()
+        return [w.cpu() for w in Ws], [m.cpu() for m in Ms]
+
+    a, b = run(-1), run(3)
+    for x, y in zip(a[0] + a[1], b[0] + b[1]):
+        assert torch.equal(x, y)
+
+
+def test_standalone_newton_schulz():
+    gen = torch.Generator().manual_seed(21)
+    for shape in [(3, 128, 512), (2, 700, 300), (1, 33, 50)]:
+        X = torch.randn(*shape, generator=gen)
+        D = newton_schulz(X.cuda()).cpu().double().numpy()
+        for i in range(shape[0]):
+            assert rel_frob(D[i], O.newton_schulz(X[i].double().numpy())) <= TOL_D_NS5
+
+
+def test_argument_errors_on_device():
+    w = torch.zeros(64, 128, device="cuda")
+    m = torch.zeros(64, 128, device="cuda")
+    g = torch.zeros(64, 128, device="cuda")
+    ctx = N.prm_create(0)
+    try:
+        d = N.prm_matrix_desc()
+        d.param, d.momentum, d.grad, d.grad_dtype, d.rows, d.cols = w.data_ptr(), m.data_ptr(), g.data_ptr(), 0, 64, 128
+        with pytest.raises(N.PrmError) as e:
+            N.prm_step(ctx, 0, 3, 0.15, 0.02, 0.01, 0.95, 1e-8)
+        assert e.value.code == N.PRM_ERR_NOT_REGISTERED
+        bad = N.prm_matrix_desc()
+        bad.param, bad.momentum, bad.grad, bad.rows, bad.cols = w.data_ptr() + 4, m.data_ptr(), g.data_ptr(), 64, 128
+        with pytest.raises(N.PrmError) as e:
+            N.prm_register_matrices(ctx, [bad])
+        assert e.value.code == N.PRM_ERR_ALIGNMENT
+        N.prm_register_matrices(ctx, [d])
+        with pytest.raises(N.PrmError) as e:
+            N.prm_step(ctx, 0, 3, 0.15, 0.02, 0.01, 0.95, 1e-8)
+        assert e.value.code == N.PRM_ERR_WORKSPACE
+        ws = torch.empty(N.prm_workspace_bytes(ctx) + 256, dtype=torch.uint8, device="cuda")
+        with pytest.raises(N.PrmError) as e:
+            N.prm_set_workspace(ctx, ws.data_ptr() + 16, N.prm_workspace_bytes(ctx))
+        assert e.value.code == N.PRM_ERR_ALIGNMENT
+        N.prm_set_workspace(ctx, ws.data_ptr(), ws.numel())
+        with pytest.raises(N.PrmError) as e:
+            N.prm_step(ctx, 1, 3, 0.15, 0.02, 0.01, 0.95, 1e-8, mode=N.PRM_MODE_MUONBP)
+        assert e.value.code == N.PRM_ERR_NOT_REGISTERED
+        for bad_args in ((0, 0, 0.95, 1e-8), (-1, 3, 0.95, 1e-8), (0, 3, 1.0, 1e-8), (0, 3, 0.95, 0.0)):
+            t, K, beta, eps = bad_args
+            with pytest.raises(N.PrmError) as e:
+                N.prm_step(ctx, t, K, 0.15, 0.02, 0.01, beta, eps)
+            assert e.value.code == N.PRM_ERR_INVALID_ARG
+        N.prm_step(ctx, 1, 3, 0.15, 0.02, 0.01, 0.95, 1e-8)
+        assert N.prm_sync_status(ctx, 0) == N.PRM_OK
+    finally:
+        N.prm_destroy(ctx)
