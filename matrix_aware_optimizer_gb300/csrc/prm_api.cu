@@ -312,6 +312,11 @@ int run_ns(prm_ctx* c, NsPlan& plan, void* base, bool update_momentum, float bet
       prep_bytes += static_cast<double>(s.views.size()) * s.rows * s.cols *
                     (update_momentum ? (s.bf16 ? 12.0 : 14.0) : 6.0);
     size_t ev = c->prof.begin(stream);
+    // Views of one group may fill different numbers of partial slots (wide:
+    // one per row; tall: one per 64x64 tile): unused slots must read as zero.
+    if ((e = cudaMemsetAsync(partials, 0, static_cast<size_t>(g.count) * g.slots * sizeof(float), stream)) !=
+        cudaSuccess)
+      return cuda_fail(c, e, "partials reset");
     for (auto& s : g.sets) {
       e = launch_prep(s.d_views, static_cast<int>(s.views.size()), s.rows, s.cols, s.vec_ok, s.bf16,
                       update_momentum, beta, x0, g.ldc, g.r * g.ldc, partials, g.slots, stream);

@@ -26,6 +26,10 @@ TOL_M = 1e-6
 TOL_W_ROWNORM = 1e-5
 TOL_D_ROWNORM = 1e-4
 TOL_D_NS5 = 2e-2
+# Matrices with a short side below 16 hold too few elements for rounding
+# errors to average out: an exact bf16 emulation of the kernels' arithmetic
+# (bf16 X, A, B; fp32 accumulation) gives 2.7-2.8% on a 2x3 matrix.
+TOL_D_NS5_TINY = 4e-2
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -44,6 +48,7 @@ def _run_teacher_forced(ms, steps, check_idx=None, mode="prmuon", blocks=0):
     gdt = torch.bfloat16 if ms.grad_dtype == synth.GRAD_BF16 else torch.float32
     grads = [torch.empty(s, device="cuda", dtype=gdt) for s in shapes]
     opt = PeriodicRowMuon(Ws, Ms, grads, muonbp_blocks=blocks)
+    opt.workspace.fill_(0xFF)  # NaN bit patterns: any read of unwritten scratch shows up
     hp = _hp(ms)
     idx = range(len(shapes)) if check_idx is None else check_idx
     report = []
@@ -142,6 +147,7 @@ def test_edge_shapes_directions(gdtype):
             Ws.append(torch.zeros(m, n, device="cuda"))
             Ms.append(torch.zeros(m, n, device="cuda"))
         opt = PeriodicRowMuon(Ws, Ms, Gs)
+        opt.workspace.fill_(0xFF)
         opt.step(t, K=K, gamma=0.5, lr=0.1, wd=0.0, beta=0.9, eps=eps)
         opt.sync_status()
         for i, (m, n) in enumerate(EDGE_SHAPES):
@@ -150,7 +156,8 @@ def test_edge_shapes_directions(gdtype):
             Dg = -host64(Ws[i]) / (eta * s)
             if t % K == 0:
                 Do = O.newton_schulz(Gh[i])
-                assert rel_frob(Dg, Do) <= TOL_D_NS5, ((m, n), rel_frob(Dg, Do))
+                tol = TOL_D_NS5 if min(m, n) >= 16 else TOL_D_NS5_TINY
+                assert rel_frob(Dg, Do) <= tol, ((m, n), rel_frob(Dg, Do))
             else:
                 Do = O.row_normalize(Gh[i], eps)
                 assert rel_frob(Dg, Do) <= 1e-6, ((m, n), rel_frob(Dg, Do))
@@ -169,6 +176,7 @@ def test_muonbp_block_and_full_steps():
         Ms = [torch.zeros(s, device="cuda") for s in shapes]
         Gs = [g.cuda() for g in Gh]
         opt = PeriodicRowMuon(Ws, Ms, Gs, muonbp_blocks=4)
+        opt.workspace.fill_(0xFF)
         assert opt.step(t, K=3, gamma=1.25, lr=0.016, wd=0.0, beta=0.9, eps=1e-8, mode="muonbp") == (t % 3 == 0)
         opt.sync_status()
         for i, (m, n) in enumerate(shapes):
@@ -194,6 +202,7 @@ def test_resume_is_bitwise():
             if t == split:
                 opt.close()
                 opt = PeriodicRowMuon(Ws, Ms, grads)
+                opt.workspace.fill_(0xFF)  # a resumed context must not depend on old scratch
             for i, g in enumerate(grads):
                 synth.make_grad(ms.shapes[i], 0, t, i, 1e-3, synth.GRAD_BF16, device="cuda", out=g)
             opt.step(t)
