@@ -150,6 +150,31 @@ PRM_API int prm_branch(int64_t t, int K, int mode);
  * CUDA; clears the word. */
 PRM_API int prm_sync_status(prm_ctx* ctx, void* stream);
 
+/* ---- allocation-free RowNorm step for one tall matrix -------------------
+ * The pages have no counterpart to this call; it exists for callers that
+ * cannot allocate device memory when the update runs (a host process whose
+ * allocator owns all device memory and refuses new allocations mid-step, an
+ * integration that cannot afford cudaMalloc's implicit synchronisation, a
+ * plugin that only receives the tensors it updates). It performs the same
+ * RowNorm step as prm_step does for a tall matrix on a non-refresh step
+ * (momentum, column norms, update; fp32 parameter and momentum updated in
+ * place, gradient fp32 or bf16, all row-major and contiguous on the current
+ * device), but takes its scratch from a fixed 4 MiB array compiled into the
+ * library instead of a workspace: it calls no cudaMalloc, cudaFree or other
+ * allocating routine.
+ *   Limits: rows > cols (tall), ceil(rows / 256) * cols + cols <= 1,048,576
+ *   floats (e.g. up to 32768 x 4096 or 20480 x 5120); larger shapes return
+ *   PRM_ERR_UNSUPPORTED. shape_scale <= 0 selects sqrt(rows / cols).
+ *   The first call on a device looks up the array's device address (a
+ *   one-time set-up per device); make that first call before any stream
+ *   capture. Every call shares the array: calls whose work may overlap on
+ *   the GPU (other streams, unordered host threads) race and must not be
+ *   issued. Errors: INVALID_ARG, SHAPE, UNSUPPORTED, CUDA. */
+PRM_API int prm_rownorm_tall_step_noalloc(float* param, float* momentum, const void* grad,
+                                          int grad_dtype, int64_t rows, int64_t cols, float gamma,
+                                          float lr, float wd, float beta, float eps,
+                                          float shape_scale, void* stream);
+
 /* ---- kernel timing (benchmarks) --------------------------------------
  * When enabled, every kernel family launched by prm_step is bracketed by a
  * pair of CUDA events recorded on the launching stream, and its algorithmic

@@ -76,6 +76,8 @@ SIGNATURES = {
     "prm_ns_poly": (c_int, [c_void_p, c_void_p, c_float, c_float, c_int, c_int64, c_int64, c_void_p]),
     "prm_ns_combine": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_float, c_int, c_int64, c_int64,
                                c_int64, c_int64, c_void_p]),
+    "prm_rownorm_tall_step_noalloc": (c_int, [c_void_p, c_void_p, c_void_p, c_int, c_int64, c_int64, c_float,
+                                              c_float, c_float, c_float, c_float, c_float, c_void_p]),
     "prm_newton_schulz_workspace": (c_int, [c_int, c_int64, c_int64, POINTER(c_size_t)]),
     "prm_newton_schulz": (c_int, [c_void_p, c_void_p, c_int, c_int64, c_int64, POINTER(c_float), c_int,
                                   c_void_p, c_size_t, c_void_p]),
@@ -191,6 +193,14 @@ def prm_ns_combine(X: int, B: int, Xout: int, scale: int, a: float, batch: int, 
                    ldr: int, stream: int = 0):
     check(load().prm_ns_combine(c_void_p(X), c_void_p(B), c_void_p(Xout), c_void_p(scale), a, batch, r, c,
                                 ldc, ldr, c_void_p(stream)), "prm_ns_combine")
+
+
+def prm_rownorm_tall_step_noalloc(param: int, momentum: int, grad: int, grad_dtype: int, rows: int, cols: int,
+                                  gamma: float, lr: float, wd: float, beta: float, eps: float,
+                                  shape_scale: float = 0.0, stream: int = 0) -> None:
+    check(load().prm_rownorm_tall_step_noalloc(c_void_p(param), c_void_p(momentum), c_void_p(grad), grad_dtype,
+                                               rows, cols, gamma, lr, wd, beta, eps, shape_scale,
+                                               c_void_p(stream)), "prm_rownorm_tall_step_noalloc")
 
 
 def prm_newton_schulz_workspace(batch: int, m: int, n: int) -> int:
