@@ -41,7 +41,7 @@ def parse_args():
     p.add_argument("--steps", type=int, default=10, help="timed K=3 cycles")
     p.add_argument("--warmup", type=int, default=3, help="untimed K=3 cycles")
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--workload", default="dit_1p3b", choices=["dit_1p3b", "dit_15b", "dit_1p3b_muonbp", "dit_block_d2048"])
+    p.add_argument("--workload", default="dit_1p3b", choices=["dit_1p3b", "dit_15b", "dit_1p3b_muonbp", "dit_block_d2048", "dit_1p3b_4blk"])
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     return p.parse_args()

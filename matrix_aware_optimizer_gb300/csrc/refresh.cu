@@ -30,7 +30,7 @@ __device__ __forceinline__ float warp_sum(float v) {
 }
 
 __device__ __forceinline__ float block_sum256(float v, float* red) {
-  const int t = threadIdx.x + threadIdx.y * blockDim.x;
+  const int t = threadIdx.x;
   const int lane = t & 31, warp = t >> 5;
   v = warp_sum(v);
   if (lane == 0) red[warp] = v;
@@ -114,7 +114,11 @@ __global__ void __launch_bounds__(PREP_THREADS) prep_wide_kernel(const View* __r
 }
 
 // Tall views (rows > cols): 64 x 64 tiles, X[j][i] = bf16(M[i][j]).
-template <bool BF16, bool UPDATE>
+// Vector path (cols % 4 == 0, 16-byte aligned rows): 16 x 16 threads, each
+// owning 4 rows x 4 columns; all loads of a thread are issued before its first
+// store so that they overlap, and the transposed bf16 tile leaves as 32-byte
+// row pieces.
+template <bool BF16, bool UPDATE, bool VEC>
 __global__ void __launch_bounds__(PREP_THREADS) prep_tall_kernel(const View* __restrict__ views, int64_t rows,
                                                                  int64_t cols, float beta,
                                                                  uint16_t* __restrict__ X, int64_t ldc,
@@ -123,34 +127,101 @@ __global__ void __launch_bounds__(PREP_THREADS) prep_tall_kernel(const View* __r
   __shared__ float tile[TILE][TILE + 1];
   __shared__ float red[33];
   const View v = views[blockIdx.z];
-  const int tx = threadIdx.x;  // 0..63 along columns
-  const int ty = threadIdx.y;  // 0..3
+  const int tid = threadIdx.x;
   const int64_t i0 = static_cast<int64_t>(blockIdx.y) * TILE;
   const int64_t j0 = static_cast<int64_t>(blockIdx.x) * TILE;
   float ss = 0.f;
-  for (int ii = ty; ii < TILE; ii += 4) {
-    const int64_t i = i0 + ii, j = j0 + tx;
-    float m = 0.f;
-    if (i < rows && j < cols) {
-      float* Mp = v.M + i * v.ld + j;
-      m = *Mp;
-      if constexpr (UPDATE) {
-        m = fmaf(beta, m, grad_at<BF16>(v.G, i * v.ld + j));
-        *Mp = m;
+  if constexpr (VEC) {
+    const int tx = tid & 15, ty = tid >> 4;  // 16 float4 columns x 16 row lanes
+    const int64_t j = j0 + tx * 4;
+    float4 m[4];
+    float4 g[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int64_t i = i0 + ty + 16 * k;
+      m[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+      g[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (i < rows && j < cols) {
+        m[k] = *reinterpret_cast<const float4*>(v.M + i * v.ld + j);
+        if constexpr (UPDATE) {
+          if constexpr (BF16) {
+            const uint2 u = __ldcs(reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(v.G) + i * v.ld + j));
+            g[k] = make_float4(bf16_to_float(u.x & 0xFFFFu), bf16_to_float(u.x >> 16),
+                               bf16_to_float(u.y & 0xFFFFu), bf16_to_float(u.y >> 16));
+          } else {
+            g[k] = __ldcs(reinterpret_cast<const float4*>(static_cast<const float*>(v.G) + i * v.ld + j));
+          }
+        }
       }
-      ss = fmaf(m, m, ss);
     }
-    tile[ii][tx] = m;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int64_t i = i0 + ty + 16 * k;
+      if constexpr (UPDATE) {
+        m[k].x = fmaf(beta, m[k].x, g[k].x);
+        m[k].y = fmaf(beta, m[k].y, g[k].y);
+        m[k].z = fmaf(beta, m[k].z, g[k].z);
+        m[k].w = fmaf(beta, m[k].w, g[k].w);
+        if (i < rows && j < cols) *reinterpret_cast<float4*>(v.M + i * v.ld + j) = m[k];
+      }
+      ss = fmaf(m[k].x, m[k].x, ss);
+      ss = fmaf(m[k].y, m[k].y, ss);
+      ss = fmaf(m[k].z, m[k].z, ss);
+      ss = fmaf(m[k].w, m[k].w, ss);
+      float* t = &tile[ty + 16 * k][tx * 4];
+      t[0] = m[k].x;
+      t[1] = m[k].y;
+      t[2] = m[k].z;
+      t[3] = m[k].w;
+    }
+  } else {
+    const int tx = tid & 63, ty = tid >> 6;  // 64 columns x 4 row lanes
+    float m[16], g[16];
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+      const int64_t i = i0 + ty + 4 * k, j = j0 + tx;
+      m[k] = 0.f;
+      g[k] = 0.f;
+      if (i < rows && j < cols) {
+        m[k] = v.M[i * v.ld + j];
+        if constexpr (UPDATE) g[k] = grad_at<BF16>(v.G, i * v.ld + j);
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+      const int64_t i = i0 + ty + 4 * k, j = j0 + tx;
+      if constexpr (UPDATE) {
+        m[k] = fmaf(beta, m[k], g[k]);
+        if (i < rows && j < cols) v.M[i * v.ld + j] = m[k];
+      }
+      ss = fmaf(m[k], m[k], ss);
+      tile[ty + 4 * k][tx] = m[k];
+    }
   }
   __syncthreads();
+  // X row j (= column j of M) gets 64 consecutive i: four threads per row,
+  // 16 bf16 (32 bytes) each.
   uint16_t* Xv = X + v.slot * x_stride;
-  for (int jj = ty; jj < TILE; jj += 4) {
-    const int64_t j = j0 + jj, i = i0 + tx;
-    if (j < cols && i < rows) Xv[j * ldc + i] = bf16_bits(tile[tx][jj]);
+  {
+    const int jj = tid >> 2, ic = (tid & 3) * 16;
+    const int64_t j = j0 + jj, ib = i0 + ic;
+    if (j < cols && ib < rows) {
+      uint16_t* dst = Xv + j * ldc + ib;
+      if (ib + 16 <= rows) {
+        uint32_t w[8];
+#pragma unroll
+        for (int h = 0; h < 8; ++h)
+          w[h] = static_cast<uint32_t>(bf16_bits(tile[ic + 2 * h][jj])) |
+                 (static_cast<uint32_t>(bf16_bits(tile[ic + 2 * h + 1][jj])) << 16);
+        reinterpret_cast<uint4*>(dst)[0] = make_uint4(w[0], w[1], w[2], w[3]);
+        reinterpret_cast<uint4*>(dst)[1] = make_uint4(w[4], w[5], w[6], w[7]);
+      } else {
+        for (int k = 0; ib + k < rows; ++k) dst[k] = bf16_bits(tile[ic + k][jj]);
+      }
+    }
   }
   const float total = block_sum256(ss, red);
-  if (tx == 0 && ty == 0)
-    partials[static_cast<int64_t>(v.slot) * slots + blockIdx.y * gridDim.x + blockIdx.x] = total;
+  if (tid == 0) partials[static_cast<int64_t>(v.slot) * slots + blockIdx.y * gridDim.x + blockIdx.x] = total;
 }
 
 __global__ void __launch_bounds__(256) norm_finish_kernel(const float* __restrict__ partials, int64_t slots,
@@ -193,32 +264,84 @@ __global__ void __launch_bounds__(PREP_THREADS) apply_wide_kernel(const View* __
   }
 }
 
+// Tall views: W[i][j] -= step * X[j][i]. X rows arrive as 32-byte pieces
+// (four threads per row of the 64 x 64 tile), are transposed in shared
+// memory, and W is updated with all its loads issued before the stores.
+template <bool VEC>
 __global__ void __launch_bounds__(PREP_THREADS) apply_tall_kernel(const View* __restrict__ views, int64_t rows,
                                                                   int64_t cols, const uint16_t* __restrict__ X,
                                                                   int64_t ldc, int64_t x_stride, float decay,
                                                                   float eta) {
   __shared__ float tile[TILE][TILE + 1];
   const View v = views[blockIdx.z];
-  const int tx = threadIdx.x, ty = threadIdx.y;
+  const int tid = threadIdx.x;
   const int64_t i0 = static_cast<int64_t>(blockIdx.y) * TILE;
   const int64_t j0 = static_cast<int64_t>(blockIdx.x) * TILE;
   const uint16_t* Xv = X + v.slot * x_stride;
-  // X is cols x rows (wide orientation): coalesced along i.
-  for (int jj = ty; jj < TILE; jj += 4) {
-    const int64_t j = j0 + jj, i = i0 + tx;
-    tile[jj][tx] = (j < cols && i < rows) ? bf16_to_float(Xv[j * ldc + i]) : 0.f;
+  {
+    const int jj = tid >> 2, ic = (tid & 3) * 16;
+    const int64_t j = j0 + jj, ib = i0 + ic;
+    if (j < cols && ib + 16 <= rows) {
+      const uint4* src = reinterpret_cast<const uint4*>(Xv + j * ldc + ib);
+      const uint4 a = src[0], b = src[1];
+      const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+      for (int h = 0; h < 8; ++h) {
+        tile[ic + 2 * h][jj] = bf16_to_float(w[h] & 0xFFFFu);
+        tile[ic + 2 * h + 1][jj] = bf16_to_float(w[h] >> 16);
+      }
+    } else {
+#pragma unroll
+      for (int k = 0; k < 16; ++k)
+        tile[ic + k][jj] = (j < cols && ib + k < rows) ? bf16_to_float(Xv[j * ldc + ib + k]) : 0.f;
+    }
   }
   __syncthreads();
   const float step = eta * v.shape_scale;
-  for (int ii = ty; ii < TILE; ii += 4) {
-    const int64_t i = i0 + ii, j = j0 + tx;
-    if (i < rows && j < cols) {
-      const float d = tile[tx][ii];
-      if (v.W == nullptr) {
-        v.out[i * v.ld + j] = d;
-      } else {
-        float* Wp = v.W + i * v.ld + j;
-        *Wp = fmaf(*Wp, decay, -step * d);
+  if constexpr (VEC) {
+    const int tx = tid & 15, ty = tid >> 4;
+    const int64_t j = j0 + tx * 4;
+    float4 w[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int64_t i = i0 + ty + 16 * k;
+      w[k] = (v.W != nullptr && i < rows && j < cols) ? *reinterpret_cast<const float4*>(v.W + i * v.ld + j)
+                                                       : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int64_t i = i0 + ty + 16 * k;
+      if (i < rows && j < cols) {
+        const float* d = &tile[ty + 16 * k][tx * 4];
+        if (v.W == nullptr) {
+          *reinterpret_cast<float4*>(v.out + i * v.ld + j) = make_float4(d[0], d[1], d[2], d[3]);
+        } else {
+          float4 o;
+          o.x = fmaf(w[k].x, decay, -step * d[0]);
+          o.y = fmaf(w[k].y, decay, -step * d[1]);
+          o.z = fmaf(w[k].z, decay, -step * d[2]);
+          o.w = fmaf(w[k].w, decay, -step * d[3]);
+          *reinterpret_cast<float4*>(v.W + i * v.ld + j) = o;
+        }
+      }
+    }
+  } else {
+    const int tx = tid & 63, ty = tid >> 6;
+    float w[16];
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+      const int64_t i = i0 + ty + 4 * k, j = j0 + tx;
+      w[k] = (v.W != nullptr && i < rows && j < cols) ? v.W[i * v.ld + j] : 0.f;
+    }
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+      const int64_t i = i0 + ty + 4 * k, j = j0 + tx;
+      if (i < rows && j < cols) {
+        const float d = tile[ty + 4 * k][tx];
+        if (v.W == nullptr)
+          v.out[i * v.ld + j] = d;
+        else
+          v.W[i * v.ld + j] = fmaf(w[k], decay, -step * d);
       }
     }
   }
@@ -251,18 +374,21 @@ cudaError_t launch_prep(const View* d_views, int count, int64_t rows, int64_t co
     }
 #undef PRM_PREP_WIDE
   } else {
-    const dim3 block(TILE, 4);
     const dim3 grid(static_cast<unsigned>((cols + TILE - 1) / TILE), static_cast<unsigned>((rows + TILE - 1) / TILE),
                     static_cast<unsigned>(count));
-    if (!update_momentum)
-      prep_tall_kernel<false, false><<<grid, block, 0, stream>>>(d_views, rows, cols, beta, X, ldc, x_mat_stride,
-                                                                 partials, slots);
-    else if (grad_bf16)
-      prep_tall_kernel<true, true><<<grid, block, 0, stream>>>(d_views, rows, cols, beta, X, ldc, x_mat_stride,
-                                                               partials, slots);
-    else
-      prep_tall_kernel<false, true><<<grid, block, 0, stream>>>(d_views, rows, cols, beta, X, ldc, x_mat_stride,
-                                                                partials, slots);
+#define PRM_PREP_TALL(B, U, V) \
+  prep_tall_kernel<B, U, V><<<grid, PREP_THREADS, 0, stream>>>(d_views, rows, cols, beta, X, ldc, x_mat_stride, partials, slots)
+    if (!update_momentum) {
+      if (vec_ok) PRM_PREP_TALL(false, false, true);
+      else PRM_PREP_TALL(false, false, false);
+    } else if (grad_bf16) {
+      if (vec_ok) PRM_PREP_TALL(true, true, true);
+      else PRM_PREP_TALL(true, true, false);
+    } else {
+      if (vec_ok) PRM_PREP_TALL(false, true, true);
+      else PRM_PREP_TALL(false, true, false);
+    }
+#undef PRM_PREP_TALL
   }
   return cudaGetLastError();
 }
@@ -284,10 +410,12 @@ cudaError_t launch_apply(const View* d_views, int count, int64_t rows, int64_t c
     else
       apply_wide_kernel<false><<<grid, PREP_THREADS, 0, stream>>>(d_views, cols, X, ldc, x_mat_stride, decay, eta);
   } else {
-    const dim3 block(TILE, 4);
     const dim3 grid(static_cast<unsigned>((cols + TILE - 1) / TILE), static_cast<unsigned>((rows + TILE - 1) / TILE),
                     static_cast<unsigned>(count));
-    apply_tall_kernel<<<grid, block, 0, stream>>>(d_views, rows, cols, X, ldc, x_mat_stride, decay, eta);
+    if (vec_ok)
+      apply_tall_kernel<true><<<grid, PREP_THREADS, 0, stream>>>(d_views, rows, cols, X, ldc, x_mat_stride, decay, eta);
+    else
+      apply_tall_kernel<false><<<grid, PREP_THREADS, 0, stream>>>(d_views, rows, cols, X, ldc, x_mat_stride, decay, eta);
   }
   return cudaGetLastError();
 }

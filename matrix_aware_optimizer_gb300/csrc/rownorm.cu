@@ -86,18 +86,18 @@ __global__ void __launch_bounds__(THREADS) rownorm_wide_kernel(const View* __res
       const int64_t c = (static_cast<int64_t>(k) * THREADS + threadIdx.x) * 4;
       if (c < cols) {
         const float4 g = load_grad4<BF16>(v.G, goff + c);
-        float4 mm = *reinterpret_cast<const float4*>(Mr + c);
+        float4 mm = __ldcs(reinterpret_cast<const float4*>(Mr + c));
         mm.x = fmaf(s.beta, mm.x, g.x);
         mm.y = fmaf(s.beta, mm.y, g.y);
         mm.z = fmaf(s.beta, mm.z, g.z);
         mm.w = fmaf(s.beta, mm.w, g.w);
-        *reinterpret_cast<float4*>(Mr + c) = mm;
+        __stcs(reinterpret_cast<float4*>(Mr + c), mm);
         ss = fmaf(mm.x, mm.x, ss);
         ss = fmaf(mm.y, mm.y, ss);
         ss = fmaf(mm.z, mm.z, ss);
         ss = fmaf(mm.w, mm.w, ss);
         m[k] = mm;
-        w[k] = *reinterpret_cast<const float4*>(Wr + c);
+        w[k] = __ldcs(reinterpret_cast<const float4*>(Wr + c));
       }
     }
     const float total = block_sum<THREADS>(ss, red);
@@ -111,7 +111,7 @@ __global__ void __launch_bounds__(THREADS) rownorm_wide_kernel(const View* __res
         ww.y = fmaf(ww.y, s.decay, -coef * m[k].y);
         ww.z = fmaf(ww.z, s.decay, -coef * m[k].z);
         ww.w = fmaf(ww.w, s.decay, -coef * m[k].w);
-        *reinterpret_cast<float4*>(Wr + c) = ww;
+        __stcs(reinterpret_cast<float4*>(Wr + c), ww);
       }
     }
   } else {

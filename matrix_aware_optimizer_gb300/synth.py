@@ -78,6 +78,12 @@ MATRIX_SETS: Dict[str, MatrixSet] = {
         shapes=_dit_set(2048, 24, 12288),
         grad_dtype=GRAD_BF16, grad_std=1e-3, steps=30,
         description="1.3B-shaped DiT matrix set: 24 blocks at d=2048 + shared adaLN 2048x12288"),
+    "dit_1p3b_4blk": MatrixSet(
+        name="dit_1p3b_4blk",
+        shapes=_dit_set(2048, 4, None),
+        grad_dtype=GRAD_BF16, grad_std=1e-3, steps=30,
+        description="4 blocks of the 1.3B-shaped set (16 matrices, 2.4 GB of state): a profiling case "
+                    "whose launches have the full set's per-group shape but a few GB on the device"),
     "dit_1p3b_muonbp": MatrixSet(
         name="dit_1p3b_muonbp",
         shapes=_dit_set(2048, 24, 12288),
