@@ -75,12 +75,10 @@ enum GemmKind { GEMM_GRAM = 0, GEMM_POLY = 1, GEMM_COMBINE = 2 };
 // (A, B), built once per buffer address.
 struct NsMaps {
   CUtensorMap x_rows128;   // X as K-major operand, 128-row box
-  CUtensorMap x_rows256;   // X as K-major operand, 256-row box
   CUtensorMap x_k64;       // X as MN-major operand, 64 x 64 box
 };
 struct SymMaps {
-  CUtensorMap rows128;
-  CUtensorMap rows256;
+  CUtensorMap rows128;     // A or B as K-major operand, 128-row box
 };
 
 int encode_x_maps(NsMaps* maps, const void* X, int batch, int64_t r, int64_t c, int64_t ldc);

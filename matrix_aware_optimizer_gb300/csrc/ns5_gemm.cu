@@ -13,16 +13,25 @@
 // Each launch covers every matrix of a same-shape batch: the tile queue runs
 // over (matrix, tile) pairs, so small r x r products still fill the GPU.
 //
+// CTA pairs. The kernel runs in 2-CTA clusters, one CTA per SM; a pair owns a
+// 256 x 256 output tile and computes it with tcgen05.mma.cta_group::2
+// (M = 256, N = 256, K = 16): the even CTA issues the MMAs, each CTA holds
+// 128 rows of A and 128 rows (N) of B in its own shared memory, and each
+// CTA's TMEM receives its 128 output rows. Per SM this halves the operand
+// bytes read from shared memory and L2 for a given number of FLOPs, and it
+// leaves room for a 6-stage TMA ring.
+//
 // CTA layout (192 threads, one CTA per SM):
-//   warp 0     : TMA producer (one lane) -- 4-stage ring of 128x64 A and
-//                256x64 B bf16 tiles, 128-byte swizzle
-//   warp 1     : TMEM allocator + MMA issuer (one lane) -- tcgen05.mma
-//                kind::f16, M=128 N=256 K=16, fp32 accumulators in TMEM,
-//                two accumulator buffers (2 x 256 columns)
-//   warps 2..5 : epilogue -- tcgen05.ld of the accumulator (one TMEM lane =
-//                one output row per thread), fused scaling / polynomial /
-//                axpy with the second operand tile read from global memory,
-//                bf16 stores (plus mirrored stores for symmetric outputs)
+//   warp 0     : TMA producer (one lane): per stage a 128x64 A tile and a
+//                128-row (N) slice of B, 128-byte swizzle; completion counted
+//                on the even CTA's barrier
+//   warp 1     : TMEM allocation for the pair (512 columns: two 128x256 fp32
+//                accumulators); in the even CTA one lane issues the MMAs
+//   warps 2..5 : epilogue -- tcgen05.ld of this CTA's 128 accumulator rows
+//                (one TMEM lane = one output row per thread), fused scaling /
+//                polynomial / axpy with the second operand tile read from
+//                global memory, bf16 stores (plus mirrored stores for
+//                symmetric outputs)
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cudaTypedefs.h>
@@ -37,16 +46,20 @@
 namespace prm {
 namespace {
 
-constexpr int BM = 128;  // output rows per tile (UMMA M)
-constexpr int BN = 256;  // output cols per tile (UMMA N); also the super-block edge of symmetric outputs
-constexpr int BK = 64;   // reduction slice per pipeline stage (64 bf16 = one 128-byte swizzle row)
-constexpr int UK = 16;   // reduction length of one tcgen05.mma kind::f16
-constexpr int STAGES = 4;
-constexpr uint32_t A_TILE_BYTES = BM * BK * 2;
-constexpr uint32_t B_TILE_BYTES = BN * BK * 2;
+constexpr int PAIR_M = 256;  // output rows per CTA pair (UMMA M)
+constexpr int BM = 128;      // output rows per CTA
+constexpr int BN = 256;      // output cols per tile (UMMA N); also the super-block edge of symmetric outputs
+constexpr int BN_HALF = 128; // B rows (N) held by each CTA
+constexpr int BK = 64;       // reduction slice per pipeline stage (64 bf16 = one 128-byte swizzle row)
+constexpr int UK = 16;       // reduction length of one tcgen05.mma kind::f16
+constexpr int STAGES = 6;
+constexpr uint32_t A_TILE_BYTES = BM * BK * 2;       // 16 KB
+constexpr uint32_t B_TILE_BYTES = BN_HALF * BK * 2;  // 16 KB
 constexpr uint32_t STAGE_BYTES = A_TILE_BYTES + B_TILE_BYTES;
-constexpr uint32_t MN_CHUNK_BYTES = 64 * BK * 2;  // one 64-column MN-major box of the B operand
+constexpr uint32_t PAIR_STAGE_BYTES = 2 * STAGE_BYTES;  // what the even CTA's full barrier expects
+constexpr uint32_t MN_CHUNK_BYTES = 64 * BK * 2;        // one 64-column MN-major box of the B operand
 constexpr int NUM_THREADS = 192;
+constexpr int EPI_WARPS = 4;
 constexpr uint32_t TMEM_COLS = 2 * BN;
 constexpr size_t BARRIER_BYTES = 256;
 constexpr size_t SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + BARRIER_BYTES;
@@ -56,8 +69,8 @@ struct GemmParams {
   int M;              // output rows (r)
   int N;              // output cols (r for GRAM/POLY, c for COMBINE)
   int K;              // reduction length (c for GRAM, r otherwise)
-  int tiles_m;        // COMBINE: ceil(M / BM)
-  int nb;             // GRAM/POLY: ceil(M / BN) super-blocks per side
+  int tiles_m;        // COMBINE: ceil(M / 256)
+  int nb;             // GRAM/POLY: ceil(M / 256) super-blocks per side
   int tiles_per_mat;
   int64_t total_tiles;
   uint16_t* out;
@@ -72,12 +85,12 @@ struct GemmParams {
 
 struct TileCoord {
   int mat;
-  int m0;
+  int m0;  // first output row of the pair's 256-row tile
   int n0;
   bool mirror;
-  bool valid;
 };
 
+// Pair tile `tile` of the queue: (matrix, 256-row block, 256-column block).
 template <int KIND>
 __device__ __forceinline__ TileCoord tile_coord(const GemmParams& p, int64_t tile) {
   TileCoord t;
@@ -87,15 +100,12 @@ __device__ __forceinline__ TileCoord tile_coord(const GemmParams& p, int64_t til
     // m fastest: consecutive tiles share the same 256-column stripe of X.
     const int tm = local % p.tiles_m;
     const int tn = local / p.tiles_m;
-    t.m0 = tm * BM;
+    t.m0 = tm * PAIR_M;
     t.n0 = tn * BN;
     t.mirror = false;
-    t.valid = true;
   } else {
-    // Upper-triangle super-block pairs (I <= J), row by row; two 128-row
-    // halves per 256 x 256 super-block.
-    const int half = local & 1;
-    int rem = local >> 1;
+    // Upper-triangle super-block pairs (I <= J), row by row.
+    int rem = local;
     int I = 0, rowlen = p.nb;
     while (rem >= rowlen) {
       rem -= rowlen;
@@ -103,10 +113,9 @@ __device__ __forceinline__ TileCoord tile_coord(const GemmParams& p, int64_t til
       --rowlen;
     }
     const int J = I + rem;
-    t.m0 = I * BN + half * BM;
+    t.m0 = I * PAIR_M;
     t.n0 = J * BN;
     t.mirror = J > I;
-    t.valid = t.m0 < p.M;
   }
   return t;
 }
@@ -141,9 +150,7 @@ __device__ __forceinline__ uint16_t to_bf16_bits(float v) {
 }
 
 template <int KIND>
-__device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileCoord& tc, int row_in_tile,
-                                              uint32_t t_row) {
-  const int i = tc.m0 + row_in_tile;
+__device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileCoord& tc, int i, uint32_t t_row) {
   const bool row_ok = i < p.M;
   float s = 1.f;
   if (KIND == GEMM_GRAM && p.scale != nullptr) {
@@ -207,7 +214,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileCoo
 }
 
 template <int KIND>
-__global__ void __launch_bounds__(NUM_THREADS, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     ns_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -224,26 +231,31 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
+  const uint32_t rank = cluster_ctarank();  // 0: issues the MMAs; 1: its peer
+  const int64_t pair_id = blockIdx.x >> 1;
+  const int64_t num_pairs = gridDim.x >> 1;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&full_bar[s], 1);
-      mbar_init(&empty_bar[s], 1);
+      mbar_init(&full_bar[s], 1);   // used in the even CTA: its producer's arrive + both CTAs' bytes
+      mbar_init(&empty_bar[s], 1);  // one multicast commit per use
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull_bar[a], 1);
-      mbar_init(&tempty_bar[a], 4);  // one arrival per epilogue warp
+      mbar_init(&tempty_bar[a], 2 * EPI_WARPS);  // even CTA: one arrival per epilogue warp of both CTAs
     }
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
   if (warp == 1) {
-    tmem_alloc(tmem_holder, TMEM_COLS);
-    tmem_relinquish();
+    tmem_alloc_pair(tmem_holder, TMEM_COLS);
+    tmem_relinquish_pair();
   }
+  // Both CTAs' barriers must exist before either signals the other.
   tc_fence_before_sync();
   __syncthreads();
+  cluster_sync_all();
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_holder;
   const int num_kb = (p.K + BK - 1) / BK;
@@ -256,24 +268,26 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       uint32_t phase = 0;
       uint32_t issued = 0, issued_parity = 0;
       bool ok = true;
-      for (int64_t tile = blockIdx.x; ok && tile < p.total_tiles; tile += gridDim.x) {
+      for (int64_t tile = pair_id; ok && tile < p.total_tiles; tile += num_pairs) {
         const TileCoord tc = tile_coord<KIND>(p, tile);
-        if (!tc.valid) continue;
+        const int m_cta = tc.m0 + static_cast<int>(rank) * BM;
+        const int n_cta = tc.n0 + static_cast<int>(rank) * BN_HALF;
         for (int kb = 0; kb < num_kb; ++kb) {
           if (!wait_bounded(&empty_bar[stage], phase ^ 1u, abort_flag, p.err, p.timeout_ns)) {
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&full_bar[stage], STAGE_BYTES);
+          if (rank == 0) mbar_arrive_expect_tx(&full_bar[stage], PAIR_STAGE_BYTES);
+          const uint32_t bar = mapa_shared(smem_u32(&full_bar[stage]), 0);
           uint8_t* a_dst = sA + stage * A_TILE_BYTES;
           uint8_t* b_dst = sB + stage * B_TILE_BYTES;
-          tma_load_3d(a_dst, &tmA, &full_bar[stage], kb * BK, tc.m0, tc.mat);
+          tma_load_3d_pair(a_dst, &tmA, bar, kb * BK, m_cta, tc.mat);
           if (KIND == GEMM_COMBINE) {
 #pragma unroll
-            for (int q = 0; q < BN / 64; ++q)
-              tma_load_3d(b_dst + q * MN_CHUNK_BYTES, &tmB, &full_bar[stage], tc.n0 + q * 64, kb * BK, tc.mat);
+            for (int q = 0; q < BN_HALF / 64; ++q)
+              tma_load_3d_pair(b_dst + q * MN_CHUNK_BYTES, &tmB, bar, n_cta + q * 64, kb * BK, tc.mat);
           } else {
-            tma_load_3d(b_dst, &tmB, &full_bar[stage], kb * BK, tc.n0, tc.mat);
+            tma_load_3d_pair(b_dst, &tmB, bar, kb * BK, n_cta, tc.mat);
           }
           issued |= 1u << stage;
           issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
@@ -283,23 +297,27 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
         }
       }
-      if (!ok) {
-        // Let every load already in flight land before the CTA exits.
-        for (int s = 0; s < STAGES; ++s)
-          if (issued & (1u << s)) wait_drain(&full_bar[s], (issued_parity >> s) & 1u, 50000000ull);
+      if (!ok && issued) {
+        // Let every load already in flight land before the CTA exits. The
+        // even CTA can watch its full barriers; the odd CTA's loads complete
+        // on the peer's barrier, so it waits a fixed, ample time instead.
+        if (rank == 0) {
+          for (int s = 0; s < STAGES; ++s)
+            if (issued & (1u << s)) wait_drain(&full_bar[s], (issued_parity >> s) & 1u, 50000000ull);
+        } else {
+          spin_for_ns(2000000ull);
+        }
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16_f32(BM, BN, false, KIND == GEMM_COMBINE);
+    if (lane == 0 && rank == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(PAIR_M, BN, false, KIND == GEMM_COMBINE);
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true, issued_any = false;
-      for (int64_t tile = blockIdx.x; ok && tile < p.total_tiles; tile += gridDim.x) {
-        const TileCoord tc = tile_coord<KIND>(p, tile);
-        if (!tc.valid) continue;
+      for (int64_t tile = pair_id; ok && tile < p.total_tiles; tile += num_pairs) {
         if (!wait_bounded(&tempty_bar[acc], acc_phase ^ 1u, abort_flag, p.err, p.timeout_ns)) {
           ok = false;
           break;
@@ -320,17 +338,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const uint64_t bd = (KIND == GEMM_COMBINE)
                                     ? smem_desc_sw128(b_addr + k * UK * 128, MN_CHUNK_BYTES, 1024)
                                     : smem_desc_sw128(b_addr + k * UK * 2, 16, 1024);
-            umma_bf16(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+            umma_bf16_pair(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
           }
           issued_any = true;
-          umma_commit(&empty_bar[stage]);
+          umma_commit_pair_multicast(&empty_bar[stage], 0x3);
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
           }
         }
         if (!ok) break;
-        umma_commit(&tfull_bar[acc]);
+        umma_commit_pair_multicast(&tfull_bar[acc], 0x3);
         if (++acc == 2) {
           acc = 0;
           acc_phase ^= 1u;
@@ -338,26 +356,26 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
       if (!ok && issued_any) {
         // Let every MMA already issued finish before TMEM is released.
-        umma_commit(drain_bar);
+        umma_commit_pair_multicast(drain_bar, 0x1);
         wait_drain(drain_bar, 0, 50000000ull);
       }
     }
   } else {
     const int quarter = warp & 3;  // TMEM lanes [32 * quarter, 32 * quarter + 32) belong to this warp
-    const int row_in_tile = quarter * 32 + lane;
+    const uint32_t tempty_even = mapa_shared(smem_u32(&tempty_bar[0]), 0);
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int64_t tile = blockIdx.x; tile < p.total_tiles; tile += gridDim.x) {
+    for (int64_t tile = pair_id; tile < p.total_tiles; tile += num_pairs) {
       const TileCoord tc = tile_coord<KIND>(p, tile);
-      if (!tc.valid) continue;
       const bool got = wait_bounded(&tfull_bar[acc], acc_phase, abort_flag, p.err, p.timeout_ns);
       if (!__all_sync(0xffffffffu, got)) break;
       tc_fence_after_sync();
+      const int i = tc.m0 + static_cast<int>(rank) * BM + quarter * 32 + lane;
       const uint32_t t_row = tmem_base + static_cast<uint32_t>(acc * BN) + (static_cast<uint32_t>(quarter * 32) << 16);
-      epilogue_tile<KIND>(p, tc, row_in_tile, t_row);
+      epilogue_tile<KIND>(p, tc, i, t_row);
       tc_fence_before_sync();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&tempty_bar[acc]);
+      if (lane == 0) mbar_arrive_cluster(tempty_even + static_cast<uint32_t>(acc * sizeof(uint64_t)));
       if (++acc == 2) {
         acc = 0;
         acc_phase ^= 1u;
@@ -365,10 +383,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
   }
   __syncwarp();
+  // No CTA may leave (or free TMEM) while its peer can still touch its
+  // barriers, shared memory or accumulators.
   tc_fence_before_sync();
   __syncthreads();
+  cluster_sync_all();
   tc_fence_after_sync();
-  if (warp == 1) tmem_dealloc(tmem_base, TMEM_COLS);
+  if (warp == 1) tmem_dealloc_pair(tmem_base, TMEM_COLS);
 }
 
 // ---------------------------------------------------------------- host side
@@ -404,12 +425,40 @@ int encode_3d(CUtensorMap* map, const void* base, int batch, int64_t rows, int64
   return r == CUDA_SUCCESS ? 0 : static_cast<int>(r);
 }
 
+// How many CTA pairs of this kernel fit on the device at once (clusters
+// must sit inside one GPC, so this can be below half the SM count).
+template <int KIND>
+int max_resident_pairs(int num_sms) {
+  static int cached[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
+  if (cached[dev] > 0) return cached[dev];
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(num_sms & ~1));
+  cfg.blockDim = dim3(NUM_THREADS);
+  cfg.dynamicSmemBytes = SMEM_BYTES;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, ns_gemm_kernel<KIND>, &cfg) != cudaSuccess || n <= 0) {
+    cudaGetLastError();  // clear the query's error state
+    n = num_sms / 2;
+  }
+  cached[dev] = n;
+  return n;
+}
+
 template <int KIND>
 cudaError_t launch_kind(const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p, int num_sms,
                         cudaStream_t stream) {
   if (p.total_tiles == 0) return cudaSuccess;
-  const int64_t grid64 = std::min<int64_t>(p.total_tiles, num_sms);
-  ns_gemm_kernel<KIND><<<static_cast<unsigned>(grid64), NUM_THREADS, SMEM_BYTES, stream>>>(a, b, p);
+  const int64_t pairs = std::min<int64_t>(p.total_tiles, max_resident_pairs<KIND>(num_sms));
+  ns_gemm_kernel<KIND><<<static_cast<unsigned>(2 * pairs), NUM_THREADS, SMEM_BYTES, stream>>>(a, b, p);
   return cudaGetLastError();
 }
 
@@ -429,7 +478,7 @@ void set_symmetric_tiles(GemmParams& p, int batch, int64_t r) {
   p.N = static_cast<int>(r);
   p.nb = static_cast<int>((r + BN - 1) / BN);
   p.tiles_m = 0;
-  p.tiles_per_mat = p.nb * (p.nb + 1);  // nb(nb+1)/2 super-blocks x 2 halves
+  p.tiles_per_mat = p.nb * (p.nb + 1) / 2;  // upper-triangle 256 x 256 super-blocks
   p.total_tiles = static_cast<int64_t>(p.tiles_per_mat) * batch;
 }
 
@@ -452,14 +501,11 @@ cudaError_t gemm_setup_attributes() {
 int encode_x_maps(NsMaps* maps, const void* X, int batch, int64_t r, int64_t c, int64_t ldc) {
   int e;
   if ((e = encode_3d(&maps->x_rows128, X, batch, r, c, ldc, BK, BM)) != 0) return e;
-  if ((e = encode_3d(&maps->x_rows256, X, batch, r, c, ldc, BK, BN)) != 0) return e;
   return encode_3d(&maps->x_k64, X, batch, r, c, ldc, 64, BK);
 }
 
 int encode_sym_maps(SymMaps* maps, const void* A, int batch, int64_t r, int64_t ldr) {
-  int e;
-  if ((e = encode_3d(&maps->rows128, A, batch, r, r, ldr, BK, BM)) != 0) return e;
-  return encode_3d(&maps->rows256, A, batch, r, r, ldr, BK, BN);
+  return encode_3d(&maps->rows128, A, batch, r, r, ldr, BK, BM);
 }
 
 cudaError_t launch_gram(const NsMaps& xin, uint16_t* A, const GemmLaunch& g, cudaStream_t stream) {
@@ -470,7 +516,7 @@ cudaError_t launch_gram(const NsMaps& xin, uint16_t* A, const GemmLaunch& g, cud
   p.ld_out = g.ldr;
   p.stride_out = g.r * g.ldr;
   p.aux = nullptr;
-  return launch_kind<GEMM_GRAM>(xin.x_rows128, xin.x_rows256, p, g.num_sms, stream);
+  return launch_kind<GEMM_GRAM>(xin.x_rows128, xin.x_rows128, p, g.num_sms, stream);
 }
 
 cudaError_t launch_poly(const SymMaps& a, const uint16_t* A, uint16_t* B, const GemmLaunch& g,
@@ -485,7 +531,7 @@ cudaError_t launch_poly(const SymMaps& a, const uint16_t* A, uint16_t* B, const 
   p.ld_aux = g.ldr;
   p.stride_aux = g.r * g.ldr;
   p.scale = nullptr;
-  return launch_kind<GEMM_POLY>(a.rows128, a.rows256, p, g.num_sms, stream);
+  return launch_kind<GEMM_POLY>(a.rows128, a.rows128, p, g.num_sms, stream);
 }
 
 cudaError_t launch_combine(const SymMaps& b, const NsMaps& xin, const uint16_t* X, uint16_t* Xout,
@@ -494,7 +540,7 @@ cudaError_t launch_combine(const SymMaps& b, const NsMaps& xin, const uint16_t* 
   p.M = static_cast<int>(g.r);
   p.N = static_cast<int>(g.c);
   p.K = static_cast<int>(g.r);
-  p.tiles_m = static_cast<int>((g.r + BM - 1) / BM);
+  p.tiles_m = static_cast<int>((g.r + PAIR_M - 1) / PAIR_M);
   p.nb = 0;
   const int tiles_n = static_cast<int>((g.c + BN - 1) / BN);
   p.tiles_per_mat = p.tiles_m * tiles_n;
