@@ -252,11 +252,18 @@ def run_ours(args):
     hp = dict(K=ms.K, gamma=ms.gamma, lr=ms.lr, wd=ms.wd, beta=ms.beta, eps=ms.eps)
     gdt = torch.bfloat16 if ms.grad_dtype == synth.GRAD_BF16 else torch.float32
 
-    # state and one gradient set, generated on the device from the seeded recipe
+    # state and one gradient set, generated on the device from the seeded recipe;
+    # the gradients live in one flat buffer (as a training loop's flattened
+    # gradient storage would), so the end-to-end leg moves them in one copy
     Ws, Ms = synth.make_state(ms, device=dev)
+    offs, total = [], 0
+    for (m, n) in ms.shapes:
+        offs.append(total)
+        total += (m * n + 127) // 128 * 128  # keep every matrix 256-byte aligned
+    gflat = torch.empty(total, device=dev, dtype=gdt)
     grads = []
     for i, s in enumerate(ms.shapes):
-        g = torch.empty(s, device=dev, dtype=gdt)
+        g = gflat[offs[i]:offs[i] + s[0] * s[1]].view(s)
         synth.make_grad(s, ms.seed, 0, i, ms.grad_std, ms.grad_dtype, ms.row_sigma, device=dev, out=g)
         grads.append(g)
     torch.cuda.synchronize()
@@ -345,14 +352,13 @@ def run_ours(args):
     # ---- end to end through the public API: pinned host grads in, a row out
     e2e = None
     if not args.no_e2e:
-        host = [g.cpu().pin_memory() for g in grads]
-        h2d = sum(h.numel() * h.element_size() for h in host)
+        hflat = gflat.cpu().pin_memory()
+        h2d = sum(g.numel() * g.element_size() for g in grads)
         out_row = torch.empty(ms.shapes[0][1], dtype=torch.float32).pin_memory()
         d2h = out_row.numel() * 4
         for k in range(2):
             for j in range(ms.K):
-                for g, h in zip(grads, host):
-                    g.copy_(h, non_blocking=True)
+                gflat.copy_(hflat, non_blocking=True)
                 opt.step(k * ms.K + j, mode=mode, **hp)
                 out_row.copy_(Ws[0][0], non_blocking=True)
         torch.cuda.synchronize()
@@ -362,8 +368,7 @@ def run_ours(args):
         e0.record(stream)
         for k in range(args.steps):
             for j in range(ms.K):
-                for g, h in zip(grads, host):
-                    g.copy_(h, non_blocking=True)
+                gflat.copy_(hflat, non_blocking=True)
                 opt.step((args.warmup + args.steps + k) * ms.K + j, mode=mode, **hp)
                 out_row.copy_(Ws[0][0], non_blocking=True)
         e1.record(stream)

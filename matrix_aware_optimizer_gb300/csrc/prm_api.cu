@@ -46,22 +46,38 @@ struct LaunchSet {
   size_t off_partials = 0, off_inv = 0;  // tall RowNorm scratch (relative to workspace base)
 };
 
-// Same wide-orientation shape r x c: one batch for the tensor-core GEMMs.
+// Same wide-orientation shape r x c: one batch for the GRAM and COMBINE
+// GEMMs. Its r x r Gram / polynomial matrices live in the r-class arrays.
 struct NsGroup {
   int64_t r = 0, c = 0, ldc = 0, ldr = 0;
   int count = 0;
-  int64_t slots = 0;  // Frobenius partial slots per matrix
+  int rclass = 0;
+  int64_t base_slot = 0;  // first slot of this group inside its r-class arrays
+  int64_t slots = 0;      // Frobenius partial slots per matrix
   std::vector<LaunchSet> sets;
-  size_t off_x0 = 0, off_x1 = 0, off_a = 0, off_b = 0, off_scale = 0, off_partials = 0, bytes = 0;
+  size_t off_x0 = 0, off_x1 = 0, off_scale = 0, off_partials = 0;
   // tensor maps for the bound workspace
   const void* maps_base = nullptr;
   NsMaps mx0{}, mx1{};
-  SymMaps ma{}, mb{};
+  SymMaps mb{};  // this group's slice of the r-class B array (COMBINE operand)
 };
 
+// All matrices with the same short side r: their A = X X^T and
+// B = b A + c A A sit in one batch, so POLY runs as one launch for the class.
+struct NsRClass {
+  int64_t r = 0, ldr = 0;
+  int count = 0;
+  size_t off_a = 0, off_b = 0;
+  const void* maps_base = nullptr;
+  SymMaps ma{};
+};
+
+// Every group's buffers are live at once: the five NS5 rounds of all groups
+// run in lockstep (GRAM per group, POLY per r-class, COMBINE per group).
 struct NsPlan {
   std::vector<NsGroup> groups;
-  size_t bytes = 0;  // groups run one after another and share the region
+  std::vector<NsRClass> rclasses;
+  size_t bytes = 0;
 };
 
 struct RowNormPlan {
@@ -133,28 +149,40 @@ void build_ns_plan(const std::vector<View>& views, NsPlan& plan) {
     set->vec_ok = set->vec_ok && view_vec_ok(v);
     set->views.push_back(v);
   }
-  plan.bytes = 0;
+  size_t off = 0;
+  std::map<int64_t, int> rindex;
   for (auto& g : plan.groups) {
     g.slots = prep_slots(g.sets.front().rows, g.sets.front().cols);
     for (auto& s : g.sets) g.slots = std::max(g.slots, prep_slots(s.rows, s.cols));
     const size_t xb = align_up(static_cast<size_t>(g.count) * g.r * g.ldc * 2, 256);
-    const size_t ab = align_up(static_cast<size_t>(g.count) * g.r * g.ldr * 2, 256);
-    size_t off = 0;
     g.off_x0 = off;
     off += xb;
     g.off_x1 = off;
     off += xb;
-    g.off_a = off;
-    off += ab;
-    g.off_b = off;
-    off += ab;
     g.off_scale = off;
     off += align_up(static_cast<size_t>(g.count) * 4, 256);
     g.off_partials = off;
     off += align_up(static_cast<size_t>(g.count) * g.slots * 4, 256);
-    g.bytes = off;
-    plan.bytes = std::max(plan.bytes, off);
+    auto it = rindex.find(g.r);
+    if (it == rindex.end()) {
+      NsRClass rc;
+      rc.r = g.r;
+      rc.ldr = g.ldr;
+      plan.rclasses.push_back(rc);
+      it = rindex.emplace(g.r, static_cast<int>(plan.rclasses.size()) - 1).first;
+    }
+    g.rclass = it->second;
+    g.base_slot = plan.rclasses[g.rclass].count;
+    plan.rclasses[g.rclass].count += g.count;
   }
+  for (auto& rc : plan.rclasses) {
+    const size_t ab = align_up(static_cast<size_t>(rc.count) * rc.r * rc.ldr * 2, 256);
+    rc.off_a = off;
+    off += ab;
+    rc.off_b = off;
+    off += ab;
+  }
+  plan.bytes = off;
 }
 
 }  // namespace
@@ -279,15 +307,24 @@ void add_to_sets(std::vector<LaunchSet>& sets, const View& v) {
   sets.push_back(std::move(s));
 }
 
-int bind_maps(prm_ctx* c, NsGroup& g, void* base) {
-  if (g.maps_base == base) return PRM_OK;
+int bind_maps(prm_ctx* c, NsPlan& plan, void* base) {
   char* b = static_cast<char*>(base);
-  int e = encode_x_maps(&g.mx0, b + g.off_x0, g.count, g.r, g.c, g.ldc);
-  if (e == 0) e = encode_x_maps(&g.mx1, b + g.off_x1, g.count, g.r, g.c, g.ldc);
-  if (e == 0) e = encode_sym_maps(&g.ma, b + g.off_a, g.count, g.r, g.ldr);
-  if (e == 0) e = encode_sym_maps(&g.mb, b + g.off_b, g.count, g.r, g.ldr);
-  if (e != 0) return fail(c, PRM_ERR_CUDA, "cuTensorMapEncodeTiled failed (code " + std::to_string(e) + ")");
-  g.maps_base = base;
+  for (auto& rc : plan.rclasses) {
+    if (rc.maps_base == base) continue;
+    if (int e = encode_sym_maps(&rc.ma, b + rc.off_a, rc.count, rc.r, rc.ldr))
+      return fail(c, PRM_ERR_CUDA, "cuTensorMapEncodeTiled failed (code " + std::to_string(e) + ")");
+    rc.maps_base = base;
+  }
+  for (auto& g : plan.groups) {
+    if (g.maps_base == base) continue;
+    const NsRClass& rc = plan.rclasses[g.rclass];
+    const size_t slice = static_cast<size_t>(g.base_slot) * g.r * g.ldr * 2;
+    int e = encode_x_maps(&g.mx0, b + g.off_x0, g.count, g.r, g.c, g.ldc);
+    if (e == 0) e = encode_x_maps(&g.mx1, b + g.off_x1, g.count, g.r, g.c, g.ldc);
+    if (e == 0) e = encode_sym_maps(&g.mb, b + rc.off_b + slice, g.count, g.r, g.ldr);
+    if (e != 0) return fail(c, PRM_ERR_CUDA, "cuTensorMapEncodeTiled failed (code " + std::to_string(e) + ")");
+    g.maps_base = base;
+  }
   return PRM_OK;
 }
 
@@ -296,22 +333,19 @@ int bind_maps(prm_ctx* c, NsGroup& g, void* base) {
 int run_ns(prm_ctx* c, NsPlan& plan, void* base, bool update_momentum, float beta, float decay, float eta,
            const float coeffs[3], int steps, cudaStream_t stream) {
   char* b = static_cast<char*>(base);
+  int rc = bind_maps(c, plan, base);
+  if (rc != PRM_OK) return rc;
+  cudaError_t e;
+  // 1. momentum update, bf16 pack (transposed for tall views), Frobenius norms
   for (auto& g : plan.groups) {
-    int rc = bind_maps(c, g, base);
-    if (rc != PRM_OK) return rc;
-    uint16_t* x0 = reinterpret_cast<uint16_t*>(b + g.off_x0);
-    uint16_t* x1 = reinterpret_cast<uint16_t*>(b + g.off_x1);
-    uint16_t* A = reinterpret_cast<uint16_t*>(b + g.off_a);
-    uint16_t* B = reinterpret_cast<uint16_t*>(b + g.off_b);
     float* scale = reinterpret_cast<float*>(b + g.off_scale);
     float* partials = reinterpret_cast<float*>(b + g.off_partials);
-    cudaError_t e;
-    const double params = static_cast<double>(g.count) * g.r * g.c;
+    uint16_t* x0 = reinterpret_cast<uint16_t*>(b + g.off_x0);
     double prep_bytes = 0;
     for (auto& s : g.sets)
       prep_bytes += static_cast<double>(s.views.size()) * s.rows * s.cols *
                     (update_momentum ? (s.bf16 ? 12.0 : 14.0) : 6.0);
-    size_t ev = c->prof.begin(stream);
+    const size_t ev = c->prof.begin(stream);
     // Views of one group may fill different numbers of partial slots (wide:
     // one per row; tall: one per 64x64 tile): unused slots must read as zero.
     if ((e = cudaMemsetAsync(partials, 0, static_cast<size_t>(g.count) * g.slots * sizeof(float), stream)) !=
@@ -325,6 +359,8 @@ int run_ns(prm_ctx* c, NsPlan& plan, void* base, bool update_momentum, float bet
     if ((e = launch_norm_finish(partials, g.slots, scale, g.count, NS_EPS, stream)) != cudaSuccess)
       return cuda_fail(c, e, "norm launch");
     c->prof.end(ev, PRM_FAMILY_NS_PREP, static_cast<int>(g.sets.size()) + 1, prep_bytes, stream);
+  }
+  auto group_launch = [&](const NsGroup& g) {
     GemmLaunch gl{};
     gl.batch = g.count;
     gl.r = g.r;
@@ -336,32 +372,60 @@ int run_ns(prm_ctx* c, NsPlan& plan, void* base, bool update_momentum, float bet
     gl.cc = coeffs[2];
     gl.err = c->d_err;
     gl.num_sms = c->num_sms;
-    uint16_t* cur = x0;
-    uint16_t* nxt = x1;
-    const NsMaps* mcur = &g.mx0;
-    const NsMaps* mnxt = &g.mx1;
-    for (int it = 0; it < steps; ++it) {
-      gl.scale = it == 0 ? scale : nullptr;
-      ev = c->prof.begin(stream);
-      if ((e = launch_gram(*mcur, A, gl, stream)) != cudaSuccess) return cuda_fail(c, e, "gram launch");
-      c->prof.end(ev, PRM_FAMILY_NS_GRAM, 1, 2.0 * params * g.r, stream);
-      ev = c->prof.begin(stream);
-      if ((e = launch_poly(g.ma, A, B, gl, stream)) != cudaSuccess) return cuda_fail(c, e, "poly launch");
-      c->prof.end(ev, PRM_FAMILY_NS_POLY, 1, 2.0 * g.count * double(g.r) * g.r * g.r, stream);
-      ev = c->prof.begin(stream);
-      if ((e = launch_combine(g.mb, *mcur, cur, nxt, gl, stream)) != cudaSuccess)
-        return cuda_fail(c, e, "combine launch");
-      c->prof.end(ev, PRM_FAMILY_NS_COMBINE, 1, 2.0 * params * g.r, stream);
-      std::swap(cur, nxt);
-      std::swap(mcur, mnxt);
+    return gl;
+  };
+  // 2. five rounds in lockstep over the groups; POLY once per r-class
+  for (int it = 0; it < steps; ++it) {
+    const bool odd = (it & 1) != 0;  // round `it` reads X_it: x0 on even rounds, x1 on odd ones
+    for (auto& g : plan.groups) {
+      GemmLaunch gl = group_launch(g);
+      gl.scale = it == 0 ? reinterpret_cast<float*>(b + g.off_scale) : nullptr;
+      const NsRClass& rcl = plan.rclasses[g.rclass];
+      uint16_t* A = reinterpret_cast<uint16_t*>(b + rcl.off_a) + g.base_slot * g.r * g.ldr;
+      const size_t ev = c->prof.begin(stream);
+      if ((e = launch_gram(odd ? g.mx1 : g.mx0, A, gl, stream)) != cudaSuccess)
+        return cuda_fail(c, e, "gram launch");
+      c->prof.end(ev, PRM_FAMILY_NS_GRAM, 1, 2.0 * g.count * double(g.r) * g.r * g.c, stream);
     }
-    ev = c->prof.begin(stream);
+    for (auto& rcl : plan.rclasses) {
+      GemmLaunch gl{};
+      gl.batch = rcl.count;
+      gl.r = rcl.r;
+      gl.c = rcl.r;
+      gl.ldc = rcl.ldr;
+      gl.ldr = rcl.ldr;
+      gl.cb = coeffs[1];
+      gl.cc = coeffs[2];
+      gl.err = c->d_err;
+      gl.num_sms = c->num_sms;
+      uint16_t* A = reinterpret_cast<uint16_t*>(b + rcl.off_a);
+      uint16_t* B = reinterpret_cast<uint16_t*>(b + rcl.off_b);
+      const size_t ev = c->prof.begin(stream);
+      if ((e = launch_poly(rcl.ma, A, B, gl, stream)) != cudaSuccess) return cuda_fail(c, e, "poly launch");
+      c->prof.end(ev, PRM_FAMILY_NS_POLY, 1, 2.0 * rcl.count * double(rcl.r) * rcl.r * rcl.r, stream);
+    }
+    for (auto& g : plan.groups) {
+      GemmLaunch gl = group_launch(g);
+      gl.scale = it == 0 ? reinterpret_cast<float*>(b + g.off_scale) : nullptr;
+      uint16_t* cur = reinterpret_cast<uint16_t*>(b + (odd ? g.off_x1 : g.off_x0));
+      uint16_t* nxt = reinterpret_cast<uint16_t*>(b + (odd ? g.off_x0 : g.off_x1));
+      const size_t ev = c->prof.begin(stream);
+      if ((e = launch_combine(g.mb, odd ? g.mx1 : g.mx0, cur, nxt, gl, stream)) != cudaSuccess)
+        return cuda_fail(c, e, "combine launch");
+      c->prof.end(ev, PRM_FAMILY_NS_COMBINE, 1, 2.0 * g.count * double(g.r) * g.r * g.c, stream);
+    }
+  }
+  // 3. W <- W (1 - lr wd) - eta s D, D = X_steps (transposed back for tall views)
+  for (auto& g : plan.groups) {
+    const uint16_t* fin = reinterpret_cast<const uint16_t*>(b + ((steps & 1) ? g.off_x1 : g.off_x0));
+    const size_t ev = c->prof.begin(stream);
     for (auto& s : g.sets) {
-      e = launch_apply(s.d_views, static_cast<int>(s.views.size()), s.rows, s.cols, s.vec_ok, cur, g.ldc,
+      e = launch_apply(s.d_views, static_cast<int>(s.views.size()), s.rows, s.cols, s.vec_ok, fin, g.ldc,
                        g.r * g.ldc, decay, eta, stream);
       if (e != cudaSuccess) return cuda_fail(c, e, "apply launch");
     }
-    c->prof.end(ev, PRM_FAMILY_NS_APPLY, static_cast<int>(g.sets.size()), params * 10.0, stream);
+    c->prof.end(ev, PRM_FAMILY_NS_APPLY, static_cast<int>(g.sets.size()),
+                static_cast<double>(g.count) * g.r * g.c * 10.0, stream);
   }
   return PRM_OK;
 }

@@ -67,9 +67,19 @@ __device__ __forceinline__ float load_grad1(const void* G, int64_t off) {
 }
 
 // ------------------------------------------------------------ wide rows
+// Bulk prefetch of `bytes` (multiple of 16, 16-byte aligned) into L2.
+__device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(p)), "r"(bytes)
+               : "memory");
+}
+
 // One CTA per row; each thread keeps NV float4 (or 4*NV floats) of the
-// updated momentum and of W in registers across the block reduction.
-template <int THREADS, int NV, bool BF16, bool VEC>
+// updated momentum in registers across the block reduction. Short rows also
+// hold W in registers (its loads overlap the momentum pass); long rows
+// (PREFETCH_W) instead have the W row pulled into L2 by one bulk prefetch at
+// the start and read after the reduction, which keeps registers -- and so
+// rows in flight per SM -- at the level short rows get.
+template <int THREADS, int NV, bool BF16, bool VEC, bool PREFETCH_W = false>
 __global__ void __launch_bounds__(THREADS) rownorm_wide_kernel(const View* __restrict__ views, int64_t cols,
                                                                StepScalars s) {
   __shared__ float red[33];
@@ -80,7 +90,10 @@ __global__ void __launch_bounds__(THREADS) rownorm_wide_kernel(const View* __res
   const int64_t goff = row * v.ld;
   float ss = 0.f;
   if constexpr (VEC) {
-    float4 m[NV], w[NV];
+    float4 m[NV], w[PREFETCH_W ? 1 : NV];
+    if constexpr (PREFETCH_W) {
+      if (threadIdx.x == 0) prefetch_l2_bulk(Wr, static_cast<uint32_t>(cols * 4));
+    }
 #pragma unroll
     for (int k = 0; k < NV; ++k) {
       const int64_t c = (static_cast<int64_t>(k) * THREADS + threadIdx.x) * 4;
@@ -97,7 +110,7 @@ __global__ void __launch_bounds__(THREADS) rownorm_wide_kernel(const View* __res
         ss = fmaf(mm.z, mm.z, ss);
         ss = fmaf(mm.w, mm.w, ss);
         m[k] = mm;
-        w[k] = __ldcs(reinterpret_cast<const float4*>(Wr + c));
+        if constexpr (!PREFETCH_W) w[k] = __ldcs(reinterpret_cast<const float4*>(Wr + c));
       }
     }
     const float total = block_sum<THREADS>(ss, red);
@@ -106,7 +119,11 @@ __global__ void __launch_bounds__(THREADS) rownorm_wide_kernel(const View* __res
     for (int k = 0; k < NV; ++k) {
       const int64_t c = (static_cast<int64_t>(k) * THREADS + threadIdx.x) * 4;
       if (c < cols) {
-        float4 ww = w[k];
+        float4 ww;
+        if constexpr (PREFETCH_W)
+          ww = __ldcs(reinterpret_cast<const float4*>(Wr + c));
+        else
+          ww = w[PREFETCH_W ? 0 : k];
         ww.x = fmaf(ww.x, s.decay, -coef * m[k].x);
         ww.y = fmaf(ww.y, s.decay, -coef * m[k].y);
         ww.z = fmaf(ww.z, s.decay, -coef * m[k].z);
@@ -269,8 +286,9 @@ template <int THREADS, int NV, bool BF16>
 cudaError_t launch_wide_t(const View* d_views, int count, int64_t rows, int64_t cols, bool vec_ok, StepScalars s,
                           cudaStream_t stream) {
   const dim3 grid(static_cast<unsigned>(rows), static_cast<unsigned>(count));
+  constexpr bool kPrefetch = NV >= 6;  // long rows: W via L2 prefetch instead of registers
   if (vec_ok)
-    rownorm_wide_kernel<THREADS, NV, BF16, true><<<grid, THREADS, 0, stream>>>(d_views, cols, s);
+    rownorm_wide_kernel<THREADS, NV, BF16, true, kPrefetch><<<grid, THREADS, 0, stream>>>(d_views, cols, s);
   else
     rownorm_wide_kernel<THREADS, NV, BF16, false><<<grid, THREADS, 0, stream>>>(d_views, cols, s);
   return cudaGetLastError();
