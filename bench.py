@@ -123,9 +123,26 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------ oracle timing
+def _ns_flops(m, n):
+    r, c = min(m, n), max(m, n)
+    return 5 * (4 * r * r * c + 2 * r ** 3)
+
+
+def _block_shapes(m, n, P):
+    """Shapes of the P MuonBP blocks of an m x n matrix (long side split)."""
+    long_side = n if m <= n else m
+    base = long_side // P
+    sizes = [base] * (P - 1) + [long_side - base * (P - 1)]
+    return [(m, k) if m <= n else (k, n) for k in sizes]
+
+
 def oracle_cycle_estimate(ms, size: str):
     """Times the fp64 oracle on a bounded sample of one K=3 cycle and scales
-    it to the whole matrix set. Returns (ms_per_cycle, sample_text, seconds)."""
+    it to the whole matrix set. Returns (ms_per_cycle, sample_text, seconds).
+    PR-Muon cycles are one NS5 refresh + (K-1) RowNorm steps; MuonBP cycles
+    one full NS5 + (K-1) block-NS5 steps."""
+    if ms.mode == "muonbp":
+        return _oracle_cycle_muonbp(ms)
     import numpy as np
     import torch
 
@@ -188,6 +205,40 @@ def oracle_cycle_estimate(ms, size: str):
         sample = (f"NS5 on one {r0}x{r0} matrix scaled by FLOP count to every shape, RowNorm on 256 "
                   "short-side vectors of each shape scaled by parameter count; one K=3 cycle")
     return total_ms, sample, time.perf_counter() - t_start
+
+
+def _oracle_cycle_muonbp(ms):
+    """MuonBP: NS5 timed on one r0 x r0 matrix (r0 the smallest short side of
+    a block), every full and block NS5 of the cycle scaled by FLOP count."""
+    import numpy as np
+
+    import oracle as O
+    t_start = time.perf_counter()
+    blocks = {s: _block_shapes(s[0], s[1], ms.blocks) for s in set(ms.shapes)}
+    # the reference square: a typical block short side (tiny squares run BLAS far below its rate)
+    r0 = min(1024, max(min(b) for bl in blocks.values() for b in bl))
+    X = np.random.default_rng(0).standard_normal((r0, r0))
+    t0 = time.perf_counter()
+    O.newton_schulz(X)
+    per_flop = (time.perf_counter() - t0) / _ns_flops(r0, r0)
+    total = 0.0
+    for s in ms.shapes:
+        total += per_flop * (_ns_flops(*s) + (ms.K - 1) * sum(_ns_flops(*b) for b in blocks[s]))
+    sample = (f"NS5 on one {r0}x{r0} matrix; one K=3 MuonBP cycle (full NS5 + {ms.K - 1} block-NS5 steps "
+              f"with {ms.blocks} blocks per matrix) scaled by FLOP count")
+    return total * 1e3, sample, time.perf_counter() - t_start
+
+
+def max_over_ranks(value: float, device=None) -> float:
+    """Largest value over the ranks of the default process group (identity
+    when no group is initialised)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device if device is not None else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
 
 
 def host_cores():
@@ -303,11 +354,7 @@ def run_ours(args):
     clk = clocks.stop()
     N.prm_profile(opt.ctx, False)
     opt.sync_status()
-    total_ms = t_start.elapsed_time(t_end)
-    if world > 1:
-        tt = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        total_ms = tt.item()
+    total_ms = max_over_ranks(t_start.elapsed_time(t_end), dev)
     ms_cycle = total_ms / args.steps
     step_ms = [[per[k][j][0].elapsed_time(per[k][j][1]) for j in range(ms.K)] for k in range(args.steps)]
     refresh_ms = statistics.mean(r[0] for r in step_ms)
@@ -388,11 +435,7 @@ def run_ours(args):
                 out_row.copy_(Ws[0][0], non_blocking=True)
         e1.record(stream)
         torch.cuda.synchronize()
-        e2e_ms = e0.elapsed_time(e1) / args.steps
-        if world > 1:
-            tt = torch.tensor([e2e_ms], device=dev)
-            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-            e2e_ms = tt.item()
+        e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, dev)
         e2e = {"value": round(e2e_ms, 3), "unit": UNIT, "h2d_bytes_per_step": h2d * ms.K,
                "d2h_bytes_per_step": d2h * ms.K}
         opt.sync_status()
