@@ -120,25 +120,6 @@ __device__ __forceinline__ TileCoord tile_coord(const GemmParams& p, int64_t til
   return t;
 }
 
-__device__ __forceinline__ void load_bf16x32(const uint16_t* src, bool full, int n_valid, float (&x)[32]) {
-  if (full) {
-    const uint4* s4 = reinterpret_cast<const uint4*>(src);
-#pragma unroll
-    for (int v = 0; v < 4; ++v) {
-      const uint4 u = s4[v];
-      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-      for (int h = 0; h < 4; ++h) {
-        x[v * 8 + 2 * h] = __uint_as_float(w[h] << 16);
-        x[v * 8 + 2 * h + 1] = __uint_as_float(w[h] & 0xFFFF0000u);
-      }
-    }
-  } else {
-#pragma unroll
-    for (int k = 0; k < 32; ++k) x[k] = (k < n_valid) ? __uint_as_float(static_cast<uint32_t>(src[k]) << 16) : 0.f;
-  }
-}
-
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<const uint32_t*>(&h);
@@ -149,8 +130,49 @@ __device__ __forceinline__ uint16_t to_bf16_bits(float v) {
   return *reinterpret_cast<const uint16_t*>(&h);
 }
 
+constexpr int EPI_CHUNKS = BN / 32;  // 32-column chunks per output row of a tile
+
+// The epilogue's second operand (A for POLY, X for COMBINE) for this
+// thread's output row: 8 chunks of 32 bf16 as packed words (element 2h of a
+// chunk in the low half of word h), zero outside the matrix. Issued before
+// the wait for the accumulator, so its latency hides behind the mainloop.
 template <int KIND>
-__device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileCoord& tc, int i, uint32_t t_row) {
+__device__ __forceinline__ void prefetch_aux(const GemmParams& p, const TileCoord& tc, int i,
+                                             uint32_t (&xr)[EPI_CHUNKS][16]) {
+  const bool row_ok = i < p.M;
+  const uint16_t* src = p.aux + static_cast<int64_t>(tc.mat) * p.stride_aux + static_cast<int64_t>(i) * p.ld_aux;
+#pragma unroll
+  for (int q = 0; q < EPI_CHUNKS; ++q) {
+    const int j0 = tc.n0 + q * 32;
+    if (row_ok && j0 + 32 <= p.N) {
+      const uint4* s4 = reinterpret_cast<const uint4*>(src + j0);
+#pragma unroll
+      for (int v = 0; v < 4; ++v) {
+        const uint4 u = s4[v];
+        xr[q][4 * v + 0] = u.x;
+        xr[q][4 * v + 1] = u.y;
+        xr[q][4 * v + 2] = u.z;
+        xr[q][4 * v + 3] = u.w;
+      }
+    } else {
+#pragma unroll
+      for (int h = 0; h < 16; ++h) {
+        const int j = j0 + 2 * h;
+        const uint32_t lo = (row_ok && j < p.N) ? src[j] : 0u;
+        const uint32_t hi = (row_ok && j + 1 < p.N) ? src[j + 1] : 0u;
+        xr[q][h] = lo | (hi << 16);
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ float word_elem(const uint32_t (&w)[16], int k) {
+  return (k & 1) ? __uint_as_float(w[k >> 1] & 0xFFFF0000u) : __uint_as_float(w[k >> 1] << 16);
+}
+
+template <int KIND>
+__device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileCoord& tc, int i, uint32_t t_row,
+                                              const uint32_t (&xr)[EPI_CHUNKS][16]) {
   const bool row_ok = i < p.M;
   float s = 1.f;
   if (KIND == GEMM_GRAM && p.scale != nullptr) {
@@ -159,54 +181,50 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileCoo
   }
   if (KIND == GEMM_COMBINE && p.scale != nullptr) s = p.scale[tc.mat];
   uint16_t* out = p.out + static_cast<int64_t>(tc.mat) * p.stride_out;
-  const uint16_t* aux = (KIND == GEMM_GRAM) ? nullptr : p.aux + static_cast<int64_t>(tc.mat) * p.stride_aux;
 
-#pragma unroll 1
-  for (int q = 0; q < BN / 32; ++q) {
+#pragma unroll
+  for (int q = 0; q < EPI_CHUNKS; ++q) {
     const int j0 = tc.n0 + q * 32;
-    if (j0 >= p.N) break;  // uniform over the warp: depends on the tile only
-    float v[32];
-    tmem_load_32cols(t_row + static_cast<uint32_t>(q * 32), v);
-    const bool full = j0 + 32 <= p.N;
-    const int n_valid = p.N - j0;
-    if (row_ok) {
-      if (KIND == GEMM_GRAM) {
+    if (j0 < p.N) {  // uniform over the warp: depends on the tile only
+      float v[32];
+      tmem_load_32cols(t_row + static_cast<uint32_t>(q * 32), v);
+      const bool full = j0 + 32 <= p.N;
+      const int n_valid = p.N - j0;
+      if (row_ok) {
+        if (KIND == GEMM_GRAM) {
 #pragma unroll
-        for (int k = 0; k < 32; ++k) v[k] *= s;
-      } else {
-        float x[32];
-        load_bf16x32(aux + static_cast<int64_t>(i) * p.ld_aux + j0, full, n_valid, x);
-        if (KIND == GEMM_POLY) {
+          for (int k = 0; k < 32; ++k) v[k] *= s;
+        } else if (KIND == GEMM_POLY) {
 #pragma unroll
-          for (int k = 0; k < 32; ++k) v[k] = p.cb * x[k] + p.cc * v[k];
+          for (int k = 0; k < 32; ++k) v[k] = p.cb * word_elem(xr[q], k) + p.cc * v[k];
         } else {
 #pragma unroll
-          for (int k = 0; k < 32; ++k) v[k] = s * (p.ca * x[k] + v[k]);
+          for (int k = 0; k < 32; ++k) v[k] = s * (p.ca * word_elem(xr[q], k) + v[k]);
         }
-      }
-      uint16_t* dst = out + static_cast<int64_t>(i) * p.ld_out + j0;
-      if (full) {
-        uint4* d4 = reinterpret_cast<uint4*>(dst);
+        uint16_t* dst = out + static_cast<int64_t>(i) * p.ld_out + j0;
+        if (full) {
+          uint4* d4 = reinterpret_cast<uint4*>(dst);
 #pragma unroll
-        for (int w = 0; w < 4; ++w) {
-          uint4 u;
-          u.x = pack_bf16x2(v[8 * w + 0], v[8 * w + 1]);
-          u.y = pack_bf16x2(v[8 * w + 2], v[8 * w + 3]);
-          u.z = pack_bf16x2(v[8 * w + 4], v[8 * w + 5]);
-          u.w = pack_bf16x2(v[8 * w + 6], v[8 * w + 7]);
-          d4[w] = u;
+          for (int w = 0; w < 4; ++w) {
+            uint4 u;
+            u.x = pack_bf16x2(v[8 * w + 0], v[8 * w + 1]);
+            u.y = pack_bf16x2(v[8 * w + 2], v[8 * w + 3]);
+            u.z = pack_bf16x2(v[8 * w + 4], v[8 * w + 5]);
+            u.w = pack_bf16x2(v[8 * w + 6], v[8 * w + 7]);
+            d4[w] = u;
+          }
+        } else {
+#pragma unroll
+          for (int k = 0; k < 32; ++k)
+            if (k < n_valid) dst[k] = to_bf16_bits(v[k]);
         }
-      } else {
+        if (KIND != GEMM_COMBINE && tc.mirror) {
+          // Lower super-block (J, I): out[j][i]. For each j the 32 lanes of a
+          // warp write 32 consecutive i, i.e. 64 contiguous bytes.
 #pragma unroll
-        for (int k = 0; k < 32; ++k)
-          if (k < n_valid) dst[k] = to_bf16_bits(v[k]);
-      }
-      if (KIND != GEMM_COMBINE && tc.mirror) {
-        // Lower super-block (J, I): out[j][i]. For each j the 32 lanes of a
-        // warp write 32 consecutive i, i.e. 64 contiguous bytes.
-#pragma unroll
-        for (int k = 0; k < 32; ++k) {
-          if (k < n_valid) out[static_cast<int64_t>(j0 + k) * p.ld_out + i] = to_bf16_bits(v[k]);
+          for (int k = 0; k < 32; ++k) {
+            if (k < n_valid) out[static_cast<int64_t>(j0 + k) * p.ld_out + i] = to_bf16_bits(v[k]);
+          }
         }
       }
     }
@@ -367,12 +385,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     uint32_t acc_phase = 0;
     for (int64_t tile = pair_id; tile < p.total_tiles; tile += num_pairs) {
       const TileCoord tc = tile_coord<KIND>(p, tile);
+      const int i = tc.m0 + static_cast<int>(rank) * BM + quarter * 32 + lane;
+      uint32_t xr[EPI_CHUNKS][16];
+      if constexpr (KIND != GEMM_GRAM) prefetch_aux<KIND>(p, tc, i, xr);
       const bool got = wait_bounded(&tfull_bar[acc], acc_phase, abort_flag, p.err, p.timeout_ns);
       if (!__all_sync(0xffffffffu, got)) break;
       tc_fence_after_sync();
-      const int i = tc.m0 + static_cast<int>(rank) * BM + quarter * 32 + lane;
       const uint32_t t_row = tmem_base + static_cast<uint32_t>(acc * BN) + (static_cast<uint32_t>(quarter * 32) << 16);
-      epilogue_tile<KIND>(p, tc, i, t_row);
+      epilogue_tile<KIND>(p, tc, i, t_row, xr);
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(tempty_even + static_cast<uint32_t>(acc * sizeof(uint64_t)));
