@@ -22,3 +22,4 @@ from .prmuon import (  # noqa: F401
     muonbp_step,
     run_steps,
 )
+from .adamw import adamw_step  # noqa: F401,E402
