@@ -44,6 +44,7 @@ def parse_args():
     p.add_argument("--workload", default="dit_1p3b", choices=["dit_1p3b", "dit_15b", "dit_1p3b_muonbp", "dit_block_d2048", "dit_1p3b_4blk"])
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-adamw", action="store_true")
     return p.parse_args()
 
 
@@ -278,6 +279,46 @@ def run_reference(args):
 
 
 # ------------------------------------------------------------------ our arm
+# (d, blocks, shared adaLN columns) of each DiT matrix set, for its vector parameters
+DIT_LAYOUT = {"dit_1p3b": (2048, 24, 12288), "dit_1p3b_muonbp": (2048, 24, 12288), "dit_15b": (5120, 48, None),
+              "dit_block_d2048": (2048, 1, 12288), "dit_1p3b_4blk": (2048, 4, None)}
+
+
+def bench_adamw(workload, dev, stream, hbm_peak, steps):
+    """AdamW over the non-matrix parameters: a 256 Mi-element bandwidth sample
+    and the matrix set's own vector parameters (biases, norms)."""
+    import torch
+    from matrix_aware_optimizer_gb300 import synth
+    from matrix_aware_optimizer_gb300.optimizer import adamw_step
+
+    def timed(n):
+        g = torch.Generator(device=dev).manual_seed(7)
+        p = torch.randn(n, generator=g, device=dev) * 0.02
+        m = torch.zeros(n, device=dev)
+        v = torch.zeros(n, device=dev)
+        gr = (torch.randn(n, generator=g, device=dev) * 1e-3).to(torch.bfloat16)
+        for t in range(1, 4):
+            adamw_step(p, m, v, gr, t, lr=1e-4, wd=0.01)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for t in range(4, 4 + steps):
+            adamw_step(p, m, v, gr, t, lr=1e-4, wd=0.01)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / steps
+
+    nb = 256 * 2 ** 20
+    ms_b = timed(nb)
+    gbs = 26.0 * nb / (ms_b * 1e-3) / 1e9
+    d, nbk, ad = DIT_LAYOUT.get(workload, (2048, 24, 12288))
+    nvec = synth.dit_vector_params(d, nbk, ad)
+    ms_v = timed(nvec)
+    return {"sample_params": nb, "ms_per_step": round(ms_b, 4), "achieved_gbs": round(gbs, 1),
+            "frac": round(gbs / hbm_peak, 4), "bytes_per_param": 26,
+            "dit_vector_params": nvec, "dit_vector_ms_per_step": round(ms_v, 4)}
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -461,6 +502,10 @@ def run_ours(args):
                "d2h_bytes_per_step": d2h * ms.K}
         opt.sync_status()
 
+    adam = None
+    if not args.no_adamw:
+        adam = bench_adamw(args.workload, dev, stream, hbm, max(3, args.steps))
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         v, sample, _ = oracle_cycle_estimate(ms, "large")
@@ -482,6 +527,7 @@ def run_ours(args):
         "roofline": roof(top),
         "roofline_kernels": {k: roof(k) for k in fam if fam[k]["records"]},
         "vanilla_muon": vanilla,
+        "adamw": adam,
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": launches,

@@ -175,6 +175,25 @@ PRM_API int prm_rownorm_tall_step_noalloc(float* param, float* momentum, const v
                                           float lr, float wd, float beta, float eps,
                                           float shape_scale, void* stream);
 
+/* ---- AdamW for the non-matrix parameters -----------------------------
+ * [SMDiT] (scaling-study section) keeps biases, normalisation parameters and
+ * other non-matrix parameters on AdamW; its reference [3] (Loshchilov and
+ * Hutter) is decoupled weight decay. The pages print no formula; this is the
+ * plain reading of that reference:
+ *   m <- b1 m + (1 - b1) g ;  v <- b2 v + (1 - b2) g^2
+ *   p <- p (1 - lr wd) - lr (m / (1 - b1^t)) / (sqrt(v / (1 - b2^t)) + eps)
+ * over `n` elements of flat device buffers: param, exp_avg (m), exp_avg_sq (v)
+ * fp32, updated in place; grad (read only) fp32 or bf16 per grad_dtype.
+ * t >= 1 counts steps from 1 (bias correction). Hyper-parameters are doubles:
+ * 1 - b1, 1 - b2 and the bias corrections are formed in double on the host
+ * and rounded once to fp32. Any n >= 0 and any alignment
+ * (16-byte aligned buffers take the vector path). Asynchronous on `stream`.
+ * Errors: INVALID_ARG (t < 1, n < 0, NULL pointer with n > 0, b1 / b2 outside
+ * [0, 1), eps <= 0, non-finite lr / wd), CUDA. */
+PRM_API int prm_adamw_step(float* param, float* exp_avg, float* exp_avg_sq, const void* grad,
+                           int grad_dtype, int64_t n, int64_t t, double lr, double beta1, double beta2,
+                           double eps, double wd, void* stream);
+
 /* ---- kernel timing (benchmarks) --------------------------------------
  * When enabled, every kernel family launched by prm_step is bracketed by a
  * pair of CUDA events recorded on the launching stream, and its algorithmic

@@ -10,7 +10,7 @@ from .native import PrmError, prm_branch  # noqa: F401
 
 def __getattr__(name):
     # torch is only needed by the tensor-level API; keep `import` cheap.
-    if name in ("PeriodicRowMuon", "newton_schulz"):
+    if name in ("PeriodicRowMuon", "newton_schulz", "adamw_step"):
         from . import optimizer
         return getattr(optimizer, name)
     raise AttributeError(name)

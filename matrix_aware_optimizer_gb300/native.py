@@ -78,6 +78,8 @@ SIGNATURES = {
                                c_int64, c_int64, c_void_p]),
     "prm_rownorm_tall_step_noalloc": (c_int, [c_void_p, c_void_p, c_void_p, c_int, c_int64, c_int64, c_float,
                                               c_float, c_float, c_float, c_float, c_float, c_void_p]),
+    "prm_adamw_step": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int64, c_int64, ctypes.c_double,
+                               ctypes.c_double, ctypes.c_double, ctypes.c_double, ctypes.c_double, c_void_p]),
     "prm_newton_schulz_workspace": (c_int, [c_int, c_int64, c_int64, POINTER(c_size_t)]),
     "prm_newton_schulz": (c_int, [c_void_p, c_void_p, c_int, c_int64, c_int64, POINTER(c_float), c_int,
                                   c_void_p, c_size_t, c_void_p]),
@@ -201,6 +203,12 @@ def prm_rownorm_tall_step_noalloc(param: int, momentum: int, grad: int, grad_dty
     check(load().prm_rownorm_tall_step_noalloc(c_void_p(param), c_void_p(momentum), c_void_p(grad), grad_dtype,
                                                rows, cols, gamma, lr, wd, beta, eps, shape_scale,
                                                c_void_p(stream)), "prm_rownorm_tall_step_noalloc")
+
+
+def prm_adamw_step(param: int, exp_avg: int, exp_avg_sq: int, grad: int, grad_dtype: int, n: int, t: int,
+                   lr: float, beta1: float, beta2: float, eps: float, wd: float, stream: int = 0) -> None:
+    check(load().prm_adamw_step(c_void_p(param), c_void_p(exp_avg), c_void_p(exp_avg_sq), c_void_p(grad),
+                                grad_dtype, n, t, lr, beta1, beta2, eps, wd, c_void_p(stream)), "prm_adamw_step")
 
 
 def prm_newton_schulz_workspace(batch: int, m: int, n: int) -> int:

@@ -108,3 +108,22 @@ def newton_schulz(x: torch.Tensor, steps: int = 5, ns_coeffs=None,
     N.prm_newton_schulz(xb.data_ptr(), out.data_ptr(), b, m, n, ns_coeffs, steps, ws.data_ptr(), ws.numel(),
                         _stream_handle(stream))
     return out[0] if squeeze else out
+
+
+def adamw_step(param: torch.Tensor, exp_avg: torch.Tensor, exp_avg_sq: torch.Tensor, grad: torch.Tensor,
+               t: int, lr: float = 1e-4, beta1: float = 0.9, beta2: float = 0.999, eps: float = 1e-8,
+               wd: float = 0.0, stream: Optional[torch.cuda.Stream] = None) -> None:
+    """AdamW step (t >= 1) over flat fp32 CUDA tensors param / exp_avg /
+    exp_avg_sq (updated in place) and a bf16 or fp32 gradient of the same
+    number of elements -- the optimizer of the non-matrix parameters."""
+    for x in (param, exp_avg, exp_avg_sq):
+        if x.dtype != torch.float32 or not x.is_cuda or not x.is_contiguous():
+            raise ValueError("param and moments must be contiguous float32 CUDA tensors")
+    if grad.dtype not in (torch.bfloat16, torch.float32) or not grad.is_contiguous():
+        raise ValueError("grad must be a contiguous bfloat16 or float32 tensor")
+    n = param.numel()
+    if not (exp_avg.numel() == exp_avg_sq.numel() == grad.numel() == n):
+        raise ValueError("all buffers must hold the same number of elements")
+    N.prm_adamw_step(param.data_ptr(), exp_avg.data_ptr(), exp_avg_sq.data_ptr(), grad.data_ptr(),
+                     N.PRM_BF16 if grad.dtype == torch.bfloat16 else N.PRM_FP32, n, t, lr, beta1, beta2, eps, wd,
+                     _stream_handle(stream))

@@ -98,6 +98,14 @@ MATRIX_SETS: Dict[str, MatrixSet] = {
         description="15B-shaped DiT matrix set: 48 blocks at d=5120"),
 }
 
+def dit_vector_params(d: int, nblocks: int, adaln: Optional[int]) -> int:
+    """Number of non-matrix parameters of the DiT sets (left to AdamW): per
+    block the biases of qkv (3d), attention out (d), mlp up (4d) and down
+    (d) plus two normalisation layers' scale and shift (4d); the shared
+    adaLN modulation's bias when there is one."""
+    return nblocks * 13 * d + (adaln or 0)
+
+
 _KIND = {"param": 1, "grad": 2, "rowscale": 3}
 
 
