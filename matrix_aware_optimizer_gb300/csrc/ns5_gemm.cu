@@ -62,7 +62,12 @@ constexpr int NUM_THREADS = 192;
 constexpr int EPI_WARPS = 4;
 constexpr uint32_t TMEM_COLS = 2 * BN;
 constexpr size_t BARRIER_BYTES = 256;
-constexpr size_t SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + BARRIER_BYTES;
+// Per epilogue warp: one 32 x 32 bf16 block for the mirrored stores, rows
+// padded to 40 elements (80 bytes) so that 16-byte row reads are free of
+// bank conflicts.
+constexpr int MIRROR_PITCH = 40;
+constexpr size_t MIRROR_BYTES = 4 * 32 * MIRROR_PITCH * 2;
+constexpr size_t SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + BARRIER_BYTES + MIRROR_BYTES;
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;  // 2 s per individual wait
 
 struct GemmParams {
@@ -172,7 +177,8 @@ __device__ __forceinline__ float word_elem(const uint32_t (&w)[16], int k) {
 
 template <int KIND>
 __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileCoord& tc, int i, uint32_t t_row,
-                                              const uint32_t (&xr)[EPI_CHUNKS][16]) {
+                                              const uint32_t (&xr)[EPI_CHUNKS][16], uint16_t* mirror_tile,
+                                              int lane) {
   const bool row_ok = i < p.M;
   float s = 1.f;
   if (KIND == GEMM_GRAM && p.scale != nullptr) {
@@ -218,14 +224,30 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileCoo
           for (int k = 0; k < 32; ++k)
             if (k < n_valid) dst[k] = to_bf16_bits(v[k]);
         }
-        if (KIND != GEMM_COMBINE && tc.mirror) {
-          // Lower super-block (J, I): out[j][i]. For each j the 32 lanes of a
-          // warp write 32 consecutive i, i.e. 64 contiguous bytes.
+      }
+      if (KIND != GEMM_COMBINE && tc.mirror) {
+        // Lower super-block (J, I): out[j][i] for the warp's 32 rows i and
+        // this chunk's 32 columns j. Transpose the 32 x 32 block through
+        // shared memory so that lane k then writes row j0 + k: 32 consecutive
+        // i as four 16-byte stores.
+        const int i0 = i - lane;
 #pragma unroll
-          for (int k = 0; k < 32; ++k) {
-            if (k < n_valid) out[static_cast<int64_t>(j0 + k) * p.ld_out + i] = to_bf16_bits(v[k]);
+        for (int k = 0; k < 32; ++k) mirror_tile[k * MIRROR_PITCH + lane] = row_ok ? to_bf16_bits(v[k]) : 0;
+        __syncwarp();
+        const int j = j0 + lane;
+        if (j < p.N && i0 < p.M) {
+          const uint4* srow = reinterpret_cast<const uint4*>(mirror_tile + lane * MIRROR_PITCH);
+          uint16_t* drow = out + static_cast<int64_t>(j) * p.ld_out + i0;
+          if (i0 + 32 <= p.M) {
+            uint4* d4 = reinterpret_cast<uint4*>(drow);
+#pragma unroll
+            for (int w = 0; w < 4; ++w) d4[w] = srow[w];
+          } else {
+            const uint16_t* sr = mirror_tile + lane * MIRROR_PITCH;
+            for (int k = 0; i0 + k < p.M; ++k) drow[k] = sr[k];
           }
         }
+        __syncwarp();
       }
     }
   }
@@ -380,6 +402,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     }
   } else {
     const int quarter = warp & 3;  // TMEM lanes [32 * quarter, 32 * quarter + 32) belong to this warp
+    uint16_t* mirror_tile =
+        reinterpret_cast<uint16_t*>(smem + STAGES * STAGE_BYTES + BARRIER_BYTES) + quarter * 32 * MIRROR_PITCH;
     const uint32_t tempty_even = mapa_shared(smem_u32(&tempty_bar[0]), 0);
     int acc = 0;
     uint32_t acc_phase = 0;
@@ -392,7 +416,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       if (!__all_sync(0xffffffffu, got)) break;
       tc_fence_after_sync();
       const uint32_t t_row = tmem_base + static_cast<uint32_t>(acc * BN) + (static_cast<uint32_t>(quarter * 32) << 16);
-      epilogue_tile<KIND>(p, tc, i, t_row, xr);
+      epilogue_tile<KIND>(p, tc, i, t_row, xr, mirror_tile, lane);
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(tempty_even + static_cast<uint32_t>(acc * sizeof(uint64_t)));
