@@ -45,6 +45,8 @@ def parse_args():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-adamw", action="store_true")
+    p.add_argument("--workspace-limit-gb", type=float, default=0.0,
+                   help="cap the NS5 workspace (sequential sub-plans); 0 = no cap")
     return p.parse_args()
 
 
@@ -359,7 +361,8 @@ def run_ours(args):
         synth.make_grad(s, ms.seed, 0, i, ms.grad_std, ms.grad_dtype, ms.row_sigma, device=dev, out=g)
         grads.append(g)
     torch.cuda.synchronize()
-    opt = PeriodicRowMuon(Ws, Ms, grads, muonbp_blocks=blocks)
+    opt = PeriodicRowMuon(Ws, Ms, grads, muonbp_blocks=blocks,
+                          workspace_limit=int(args.workspace_limit_gb * 2 ** 30))
     stream = torch.cuda.current_stream()
 
     def cycle(k, ev_ref=None):
@@ -555,7 +558,8 @@ def run_ours(args):
                    "gamma": ms.gamma, "lr": ms.lr, "wd": ms.wd, "beta": ms.beta, "mode": mode,
                    "muonbp_blocks": blocks, "grad_dtype": ms.grad_dtype,
                    "l2": "inputs larger than L2 (no flush)", "parallelism": f"replicas x{world}",
-                   "step": "one K=3 cycle: refresh + 2 cheap steps"},
+                   "step": "one K=3 cycle: refresh + 2 cheap steps",
+                   "workspace_gb": round(opt.workspace_bytes / 2 ** 30, 2)},
         "ms_refresh_step": round(refresh_ms, 3), "ms_cheap_step": round(cheap_ms, 3),
         "ns5_tflops": round(ns_flop / (ns_ms * 1e-3) / 1e12, 1) if ns_ms else None,
         "rownorm_gbs": round(rn_bytes / (rn_ms * 1e-3) / 1e9, 1) if rn_ms else None,

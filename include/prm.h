@@ -102,9 +102,22 @@ PRM_API int prm_destroy(prm_ctx* ctx);
  * matrix's long side, the last taking the remainder. muonbp_blocks = 0
  * disables MuonBP mode for this registration.
  * The descriptor array is copied (host memory, read only).
+ * Registration resets the workspace binding: call prm_set_workspace again.
  * Errors: INVALID_ARG, SHAPE, ALIGNMENT, CUDA, OOM. */
 PRM_API int prm_register_matrices(prm_ctx* ctx, const prm_matrix_desc* descs, int count,
                           int muonbp_blocks);
+
+/* Caps the workspace that the next prm_register_matrices plans (0, the
+ * default, means no cap: every NS5 group's buffers are live at once and the
+ * five rounds of all groups run in lockstep, so that POLY runs once per short
+ * side r). With a cap, the refresh (and the MuonBP block step) is split into
+ * sequential sub-plans of whole matrices, each sized to fit `max_bytes`; a
+ * sub-plan holds at least one matrix, so a single matrix larger than the cap
+ * still gets the room it needs -- prm_workspace_bytes reports the actual need.
+ * Results do not depend on the split. This is the single-GPU counterpart of
+ * the bucketed refresh of [SMDiT] section "Distributed co-design" (at most a
+ * bounded number of matrices materialised at a time). Errors: INVALID_ARG. */
+PRM_API int prm_set_workspace_limit(prm_ctx* ctx, size_t max_bytes);
 
 /* Bytes of device scratch the registered plan needs (NS5 operands in bf16,
  * Gram / polynomial matrices, norm and column partial sums). *bytes (host)

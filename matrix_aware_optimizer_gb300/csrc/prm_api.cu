@@ -185,6 +185,45 @@ void build_ns_plan(const std::vector<View>& views, NsPlan& plan) {
   plan.bytes = off;
 }
 
+// Splits the views into sequential sub-plans whose workspace fits `limit`
+// bytes (0: one plan for everything). Views are taken in (r, c) order so that
+// same-shape matrices stay together; a sub-plan holds at least one view.
+void build_ns_subplans(const std::vector<View>& views, size_t limit, std::vector<NsPlan>& out) {
+  out.clear();
+  if (views.empty()) return;
+  if (limit == 0) {
+    out.emplace_back();
+    build_ns_plan(views, out.back());
+    return;
+  }
+  std::vector<View> sorted = views;
+  std::stable_sort(sorted.begin(), sorted.end(), [](const View& x, const View& y) {
+    const int64_t rx = std::min(x.rows, x.cols), cx = std::max(x.rows, x.cols);
+    const int64_t ry = std::min(y.rows, y.cols), cy = std::max(y.rows, y.cols);
+    return rx != ry ? rx < ry : cx < cy;
+  });
+  std::vector<View> cur;
+  for (const View& v : sorted) {
+    cur.push_back(v);
+    NsPlan trial;
+    build_ns_plan(cur, trial);
+    if (trial.bytes > limit && cur.size() > 1) {
+      cur.pop_back();
+      out.emplace_back();
+      build_ns_plan(cur, out.back());
+      cur.assign(1, v);
+    }
+  }
+  out.emplace_back();
+  build_ns_plan(cur, out.back());
+}
+
+size_t plans_bytes(const std::vector<NsPlan>& plans) {
+  size_t b = 0;
+  for (const auto& p : plans) b = std::max(b, p.bytes);
+  return b;
+}
+
 }  // namespace
 }  // namespace prm
 
@@ -243,7 +282,8 @@ struct prm_ctx {
   int count = 0;
   int blocks = 0;
   RowNormPlan rn;
-  NsPlan ns_full, ns_blocks;
+  std::vector<NsPlan> ns_full, ns_blocks;  // sequential sub-plans (one unless a workspace cap splits them)
+  size_t ws_limit = 0;                     // prm_set_workspace_limit; 0 = no cap
   bool registered = false;
   void* ws = nullptr;
   size_t ws_bytes = 0;
@@ -283,8 +323,10 @@ void clear_registration(prm_ctx* c) {
   c->rn.wide.clear();
   c->rn.tall.clear();
   c->rn.bytes = 0;
-  free_plan(c->ns_full);
-  free_plan(c->ns_blocks);
+  for (auto& p : c->ns_full) free_plan(p);
+  for (auto& p : c->ns_blocks) free_plan(p);
+  c->ns_full.clear();
+  c->ns_blocks.clear();
   c->count = 0;
   c->blocks = 0;
   c->registered = false;
@@ -612,14 +654,14 @@ int prm_register_matrices(prm_ctx* c, const prm_matrix_desc* d, int count, int m
     off += align_up(s.views.size() * s.cols * 4, 256);
   }
   c->rn.bytes = off;
-  build_ns_plan(full, c->ns_full);
-  if (muonbp_blocks > 0) build_ns_plan(blocks, c->ns_blocks);
+  build_ns_subplans(full, c->ws_limit, c->ns_full);
+  if (muonbp_blocks > 0) build_ns_subplans(blocks, c->ws_limit, c->ns_blocks);
   cudaError_t e = upload_sets(c->rn.wide);
   if (e == cudaSuccess) e = upload_sets(c->rn.tall);
-  for (auto& g : c->ns_full.groups)
-    if (e == cudaSuccess) e = upload_sets(g.sets);
-  for (auto& g : c->ns_blocks.groups)
-    if (e == cudaSuccess) e = upload_sets(g.sets);
+  for (auto* plans : {&c->ns_full, &c->ns_blocks})
+    for (auto& p : *plans)
+      for (auto& g : p.groups)
+        if (e == cudaSuccess) e = upload_sets(g.sets);
   if (e != cudaSuccess) {
     clear_registration(c);
     return cuda_fail(c, e, "uploading launch tables");
@@ -630,9 +672,15 @@ int prm_register_matrices(prm_ctx* c, const prm_matrix_desc* d, int count, int m
   return PRM_OK;
 }
 
+int prm_set_workspace_limit(prm_ctx* c, size_t max_bytes) {
+  if (c == nullptr) return fail(nullptr, PRM_ERR_INVALID_ARG, "ctx is NULL");
+  c->ws_limit = max_bytes;
+  return PRM_OK;
+}
+
 int prm_workspace_bytes(const prm_ctx* c, size_t* bytes) {
   if (c == nullptr || bytes == nullptr) return PRM_ERR_INVALID_ARG;
-  *bytes = c->registered ? std::max({c->rn.bytes, c->ns_full.bytes, c->ns_blocks.bytes}) : 0;
+  *bytes = c->registered ? std::max({c->rn.bytes, plans_bytes(c->ns_full), plans_bytes(c->ns_blocks)}) : 0;
   return PRM_OK;
 }
 
@@ -689,8 +737,12 @@ int prm_step(prm_ctx* c, int64_t t, int K, float gamma, float lr, float wd, floa
   sc.eta = refresh ? lr : lr * gamma;
   sc.eps = eps;
   if (mode == PRM_MODE_PRMUON && !refresh) return run_rownorm(c, c->ws, sc, st);
-  NsPlan& plan = (mode == PRM_MODE_MUONBP && !refresh) ? c->ns_blocks : c->ns_full;
-  return run_ns(c, plan, c->ws, true, beta, sc.decay, sc.eta, coeffs, NS_STEPS, st);
+  std::vector<NsPlan>& plans = (mode == PRM_MODE_MUONBP && !refresh) ? c->ns_blocks : c->ns_full;
+  for (auto& plan : plans) {
+    const int rc = run_ns(c, plan, c->ws, true, beta, sc.decay, sc.eta, coeffs, NS_STEPS, st);
+    if (rc != PRM_OK) return rc;
+  }
+  return PRM_OK;
 }
 
 int prm_sync_status(prm_ctx* c, void* stream) {

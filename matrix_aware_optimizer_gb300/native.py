@@ -63,6 +63,7 @@ SIGNATURES = {
     "prm_destroy": (c_int, [c_void_p]),
     "prm_register_matrices": (c_int, [c_void_p, POINTER(prm_matrix_desc), c_int, c_int]),
     "prm_workspace_bytes": (c_int, [c_void_p, POINTER(c_size_t)]),
+    "prm_set_workspace_limit": (c_int, [c_void_p, c_size_t]),
     "prm_set_workspace": (c_int, [c_void_p, c_void_p, c_size_t]),
     "prm_step": (c_int, [c_void_p, c_int64, c_int, c_float, c_float, c_float, c_float, c_float,
                          POINTER(c_float), c_int, c_void_p]),
@@ -137,6 +138,10 @@ def prm_destroy(ctx) -> None:
 def prm_register_matrices(ctx, descs, muonbp_blocks: int = 0) -> None:
     arr = (prm_matrix_desc * max(1, len(descs)))(*descs)
     check(load().prm_register_matrices(ctx, arr, len(descs), muonbp_blocks), "prm_register_matrices", ctx)
+
+
+def prm_set_workspace_limit(ctx, max_bytes: int) -> None:
+    check(load().prm_set_workspace_limit(ctx, max_bytes), "prm_set_workspace_limit", ctx)
 
 
 def prm_workspace_bytes(ctx) -> int:

@@ -24,11 +24,13 @@ class PeriodicRowMuon:
     muonbp_blocks    : 0, or P > 0 to also plan MuonBP blocks.
     shape_scales     : optional per-matrix step multipliers (default
                        sqrt(max(1, rows / cols))).
+    workspace_limit  : cap in bytes on the NS5 workspace (0 = none): the
+                       refresh then runs in sequential sub-plans that fit it.
     """
 
     def __init__(self, params: Sequence[torch.Tensor], momenta: Sequence[torch.Tensor],
                  grads: Sequence[torch.Tensor], muonbp_blocks: int = 0,
-                 shape_scales: Optional[Sequence[float]] = None):
+                 shape_scales: Optional[Sequence[float]] = None, workspace_limit: int = 0):
         if not (len(params) == len(momenta) == len(grads)):
             raise ValueError("params, momenta and grads must have the same length")
         dev = params[0].device if params else torch.device("cuda", torch.cuda.current_device())
@@ -56,6 +58,7 @@ class PeriodicRowMuon:
         with torch.cuda.device(dev):
             self.ctx = N.prm_create(dev.index if dev.index is not None else torch.cuda.current_device())
             try:
+                N.prm_set_workspace_limit(self.ctx, int(workspace_limit))
                 N.prm_register_matrices(self.ctx, descs, muonbp_blocks)
                 nbytes = N.prm_workspace_bytes(self.ctx)
                 self.workspace = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=dev)
