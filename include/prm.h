@@ -148,7 +148,12 @@ PRM_API int prm_set_workspace(prm_ctx* ctx, void* dev_ptr, size_t bytes);
  * Preconditions: t >= 0, K >= 1 (K = 1 is vanilla Muon), 0 <= beta < 1,
  * eps > 0, finite lr / wd / gamma. Errors: INVALID_ARG, NOT_REGISTERED,
  * WORKSPACE, CUDA (launch failures). A device-side wait that gave up is
- * reported by prm_sync_status(), not here (reading it needs a sync). */
+ * reported by prm_sync_status(), not here (reading it needs a sync).
+ * A step is not atomic: when a CUDA error comes back, the kernels enqueued
+ * before the failing launch still run, so some matrices may hold the updated
+ * W and M and others the old ones; re-running the step would apply the
+ * momentum twice to the former. Every step reuses the one workspace, so
+ * steps on different streams must be ordered by the caller (events). */
 PRM_API int prm_step(prm_ctx* ctx, int64_t t, int K, float gamma, float lr, float wd, float beta,
              float eps, const float* ns_coeffs, int mode, void* stream);
 

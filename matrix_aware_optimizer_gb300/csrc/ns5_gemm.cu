@@ -38,6 +38,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <mutex>
 
 #include "internal.h"
@@ -473,10 +474,11 @@ int encode_3d(CUtensorMap* map, const void* base, int batch, int64_t rows, int64
 // must sit inside one GPC, so this can be below half the SM count).
 template <int KIND>
 int max_resident_pairs(int num_sms) {
-  static int cached[64] = {};
+  static std::atomic<int> cached[64];  // zero-initialised (static storage); races only repeat the query
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
-  if (cached[dev] > 0) return cached[dev];
+  const int known = cached[dev].load(std::memory_order_relaxed);
+  if (known > 0) return known;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(num_sms & ~1));
   cfg.blockDim = dim3(NUM_THREADS);
@@ -493,7 +495,7 @@ int max_resident_pairs(int num_sms) {
     cudaGetLastError();  // clear the query's error state
     n = num_sms / 2;
   }
-  cached[dev] = n;
+  cached[dev].store(n, std::memory_order_relaxed);
   return n;
 }
 
