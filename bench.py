@@ -8,7 +8,8 @@ the hot path: momentum, branch choice, RowNorm, NS5 prep / rounds / output,
 parameter update). The headline value is milliseconds per cycle (lower is
 better) with all state resident in HBM; `e2e` repeats the measurement through
 the public API with the gradients copied in from pinned host memory every
-optimizer step and a small result read back. Inputs (22 GB per optimizer
+optimizer step (double-buffered: the next step's upload overlaps the current
+step) and a small result read back. Inputs (22 GB per optimizer
 step on the 1.3B set) are far larger than L2, so no flush is needed.
 
   python bench.py [--steps K] [--warmup W] [--workload dit_1p3b|dit_15b|dit_1p3b_muonbp]
@@ -41,7 +42,9 @@ def parse_args():
     p.add_argument("--steps", type=int, default=10, help="timed K=3 cycles")
     p.add_argument("--warmup", type=int, default=3, help="untimed K=3 cycles")
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--workload", default="dit_1p3b", choices=["dit_1p3b", "dit_15b", "dit_1p3b_muonbp", "dit_block_d2048", "dit_1p3b_4blk"])
+    p.add_argument("--workload", default="dit_1p3b",
+                   choices=["dit_1p3b", "dit_15b", "dit_1p3b_muonbp", "dit_block_d2048", "dit_1p3b_4blk",
+                            "dit_1p3b_4blk_muonbp"])
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-adamw", action="store_true")
@@ -77,23 +80,34 @@ class ClockSampler:
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
         self.proc = None
-        self.lines = []
+        self.lines = []  # (host monotonic time the line arrived, line)
         self._t = None
+        self.window = None
 
     def start(self):
+        """Starts sampling and returns once the first sample has arrived (at
+        most 3 s), so that the timed region that follows is covered."""
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
-                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except Exception:
             self.proc = None
             return
         self._t = threading.Thread(target=self._read, daemon=True)
         self._t.start()
+        deadline = time.monotonic() + 3.0
+        while not self.lines and time.monotonic() < deadline:
+            time.sleep(0.01)
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.monotonic(), line.strip()))
+
+    def mark(self, t0: float, t1: float):
+        """Host times bracketing the timed region; only samples that arrived in
+        it are summarised (all of them if fewer than three did)."""
+        self.window = (t0, t1)
 
     def stop(self):
         if self.proc is None:
@@ -107,7 +121,12 @@ class ClockSampler:
             self._t.join(timeout=2)
         sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        lines = self.lines
+        if self.window is not None:
+            inside = [x for x in lines if self.window[0] <= x[0] <= self.window[1] + 0.06]
+            if len(inside) >= 3:
+                lines = inside
+        for _, ln in lines:
             parts = [x.strip() for x in ln.split(",")]
             if len(parts) < 9:
                 continue
@@ -283,7 +302,8 @@ def run_reference(args):
 # ------------------------------------------------------------------ our arm
 # (d, blocks, shared adaLN columns) of each DiT matrix set, for its vector parameters
 DIT_LAYOUT = {"dit_1p3b": (2048, 24, 12288), "dit_1p3b_muonbp": (2048, 24, 12288), "dit_15b": (5120, 48, None),
-              "dit_block_d2048": (2048, 1, 12288), "dit_1p3b_4blk": (2048, 4, None)}
+              "dit_block_d2048": (2048, 1, 12288), "dit_1p3b_4blk": (2048, 4, None),
+              "dit_1p3b_4blk_muonbp": (2048, 4, None)}
 
 
 def bench_adamw(workload, dev, stream, hbm_peak, steps):
@@ -378,7 +398,7 @@ def run_ours(args):
         cycle(k)
     opt.sync_status()
 
-    def timed_cycles(first, profile, per_step):
+    def timed_cycles(first, profile, per_step, sampler=None):
         """K cycles of direct prm_step calls between a barrier + synchronize on
         both sides; optionally with the library's per-kernel event timer and
         with events around every step. Returns (ms per cycle, step events)."""
@@ -390,11 +410,14 @@ def run_ours(args):
         if world > 1:
             dist.barrier()
         torch.cuda.synchronize()
+        h0 = time.monotonic()
         t0.record(stream)
         for k in range(args.steps):
             cycle(first + k, per[k] if per else None)
         t1.record(stream)
         torch.cuda.synchronize()
+        if sampler is not None:
+            sampler.mark(h0, time.monotonic())
         if world > 1:
             dist.barrier()
         if profile:
@@ -405,7 +428,7 @@ def run_ours(args):
     # ---- timed region (device-resident inputs): the headline, no library timer
     clocks = ClockSampler(local)
     clocks.start()
-    ms_cycle, per = timed_cycles(args.warmup, False, True)
+    ms_cycle, per = timed_cycles(args.warmup, False, True, sampler=clocks)
     clk = clocks.stop()
     step_ms = [[per[k][j][0].elapsed_time(per[k][j][1]) for j in range(ms.K)] for k in range(args.steps)]
     refresh_ms = statistics.mean(r[0] for r in step_ms)
@@ -501,44 +524,82 @@ def run_ours(args):
     if not args.no_e2e:
         hflat = gflat.cpu().pin_memory()
         h2d = sum(g.numel() * g.element_size() for g in grads)
-        # the step's gradients arrive in four concurrent pieces (four copy streams,
-        # joined back into the optimizer's stream before the step)
+        # Two gradient buffers and two optimizer instances over the same
+        # params / momenta, sharing one workspace (their steps are ordered on
+        # one stream): step s reads buffer s % 2 while the gradients of step
+        # s + 1 stream into the other one. Each upload runs as four concurrent
+        # pieces on four copy streams and waits for the step that last read
+        # its buffer (s - 1); each step waits for its own upload.
+        gflat2 = torch.empty_like(gflat)
+        grads2 = [gflat2[offs[i]:offs[i] + s[0] * s[1]].view(s) for i, s in enumerate(ms.shapes)]
+        opt2 = PeriodicRowMuon(Ws, Ms, grads2, muonbp_blocks=blocks, workspace=opt.workspace,
+                               workspace_limit=int(args.workspace_limit_gb * 2 ** 30))
+        bufs = [(gflat, opt), (gflat2, opt2)]
         copy_streams = [torch.cuda.Stream(device=dev) for _ in range(4)]
         bounds = [total * q // 4 // 128 * 128 for q in range(4)] + [total]
-
-        def upload():
-            fork = torch.cuda.Event()
-            fork.record(stream)
-            for q, cs in enumerate(copy_streams):
-                cs.wait_event(fork)
-                with torch.cuda.stream(cs):
-                    gflat[bounds[q]:bounds[q + 1]].copy_(hflat[bounds[q]:bounds[q + 1]], non_blocking=True)
-                done = torch.cuda.Event()
-                done.record(cs)
-                stream.wait_event(done)
         out_row = torch.empty(ms.shapes[0][1], dtype=torch.float32).pin_memory()
         d2h = out_row.numel() * 4
-        for k in range(2):
-            for j in range(ms.K):
-                upload()
-                opt.step(k * ms.K + j, mode=mode, **hp)
+
+        def run(first_t, nsteps):
+            step_done = {}
+            uploaded = {}
+
+            def upload(s):
+                dst = bufs[s % 2][0]
+                ev = []
+                for q, cs in enumerate(copy_streams):
+                    if s - 2 in step_done:
+                        cs.wait_event(step_done[s - 2])
+                    with torch.cuda.stream(cs):
+                        dst[bounds[q]:bounds[q + 1]].copy_(hflat[bounds[q]:bounds[q + 1]], non_blocking=True)
+                    e = torch.cuda.Event()
+                    e.record(cs)
+                    ev.append(e)
+                uploaded[s] = ev
+
+            upload(0)
+            for s in range(nsteps):
+                if s + 1 < nsteps:
+                    upload(s + 1)
+                for e in uploaded.pop(s):
+                    stream.wait_event(e)
+                bufs[s % 2][1].step(first_t + s, mode=mode, **hp)
+                done = torch.cuda.Event()
+                done.record(stream)
+                step_done[s] = done
                 out_row.copy_(Ws[0][0], non_blocking=True)
+
+        run(0, 2 * ms.K)  # warm-up (t = 0 starts a cycle)
         torch.cuda.synchronize()
         if world > 1:
             dist.barrier()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        for k in range(args.steps):
-            for j in range(ms.K):
-                upload()
-                opt.step((args.warmup + args.steps + k) * ms.K + j, mode=mode, **hp)
-                out_row.copy_(Ws[0][0], non_blocking=True)
+        run((args.warmup + args.steps) * ms.K, args.steps * ms.K)
         e1.record(stream)
         torch.cuda.synchronize()
         e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, dev)
+        # the uploads alone, for the link rate behind the number
+        u0, u1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        u0.record(stream)
+        for q, cs in enumerate(copy_streams):
+            cs.wait_stream(stream)
+            with torch.cuda.stream(cs):
+                gflat[bounds[q]:bounds[q + 1]].copy_(hflat[bounds[q]:bounds[q + 1]], non_blocking=True)
+            stream.wait_stream(cs)
+        u1.record(stream)
+        torch.cuda.synchronize()
+        up_ms = u0.elapsed_time(u1)
         e2e = {"value": round(e2e_ms, 3), "unit": UNIT, "h2d_bytes_per_step": h2d * ms.K,
-               "d2h_bytes_per_step": d2h * ms.K}
+               "d2h_bytes_per_step": d2h * ms.K,
+               "h2d_gbs_alone": round(h2d / up_ms / 1e6, 1),
+               "note": "per step: that step's gradients copied from pinned host memory (four copy streams), "
+                       "the step, one parameter row read back; double-buffered gradients, so the upload "
+                       "of step s + 1 overlaps step s"}
         opt.sync_status()
+        opt2.sync_status()
+        opt2.close()
+        del gflat2, grads2
 
     adam = None
     if not args.no_adamw:

@@ -142,7 +142,7 @@ PRM_API int prm_set_workspace(prm_ctx* ctx, void* dev_ptr, size_t bytes);
  *   W <- W * (1 - lr * wd) - eta * s * D           (decoupled weight decay)
  * NS5: X = M / (||M||_F + 1e-7) (transposed if tall), then five rounds of
  * A = X X^T, B = b A + c A A, X <- a X + B X, in bf16 operands with fp32
- * accumulation. ns_coeffs (host, 3 floats: a, b, c) may be NULL for the
+ * accumulation (evaluated as X <- (a I + B) X, one bf16 product per round). ns_coeffs (host, 3 floats: a, b, c) may be NULL for the
  * default quintic (3.4445, -4.7750, 2.0315) -- the pages print no
  * coefficients, so this default is a stated choice.
  * Preconditions: t >= 0, K >= 1 (K = 1 is vanilla Muon), 0 <= beta < 1,
@@ -167,6 +167,22 @@ PRM_API int prm_branch(int64_t t, int K, int mode);
  * inside the NS5 kernels set when they give up. Returns PRM_OK, TIMEOUT or
  * CUDA; clears the word. */
 PRM_API int prm_sync_status(prm_ctx* ctx, void* stream);
+
+/* Test and debugging aid: writes to host_out (host, rows * cols floats,
+ * row-major) the direction D of the most recent prm_step for registered
+ * matrix `idx` -- NS5(M_t) on a refresh / full step, the NS5 of each MuonBP
+ * block on a block step, R_eps(M_t) on a RowNorm step ([SMDiT] Fig. 3 and
+ * Fig. 4), before the step size s * eta is applied. D is recomputed from the
+ * matrix's momentum with the step's own kernels, so the momentum must still
+ * hold M_t: call it before the next step and before anything else writes the
+ * momentum. The NS5 directions equal the ones the step applied bit for bit;
+ * the RowNorm direction is the fp32 quotient M / max(||v||, eps), which the
+ * step folds into one coefficient with s * eta. Synchronises the device,
+ * allocates and frees its own scratch (the matrix's size twice, plus the NS5
+ * workspace of that one matrix) and runs on the legacy default stream; not
+ * for use inside a stream capture. Errors: INVALID_ARG (NULL, idx out of
+ * range, no step since registration), NOT_REGISTERED, OOM, CUDA, TIMEOUT. */
+PRM_API int prm_debug_last_direction(prm_ctx* ctx, int idx, float* host_out);
 
 /* ---- allocation-free RowNorm step for one tall matrix -------------------
  * The pages have no counterpart to this call; it exists for callers that
@@ -251,20 +267,22 @@ PRM_API const char* prm_last_error(const prm_ctx* ctx);
  * All pointers are device, 16-byte aligned; bf16 values are passed as
  * uint16_t bit patterns. `scale` (device, batch floats) may be NULL for 1.
  * [SMDiT] section "Periodic Row-wise Muon": one NS5 round is
- * A = X X^T, B = b A + c A A, X' = a X + B X. */
+ * A = X X^T, B = b A + c A A, X' = a X + B X. The library evaluates it as
+ * A = X X^T, P = a I + b A + c A A, X' = P X (the same product, with the
+ * a X term carried on P's diagonal), so the three calls below are GRAM,
+ * POLY and COMBINE of that form. */
 
 /* A[i] = scale[i]^2 * X[i] X[i]^T  (symmetric; tensor cores, tcgen05). */
 PRM_API int prm_ns_gram(const uint16_t* X, uint16_t* A, const float* scale, int batch, int64_t r,
                 int64_t c, int64_t ldc, int64_t ldr, void* stream);
 
-/* B[i] = b * A[i] + c * A[i] A[i]   (A symmetric). */
-PRM_API int prm_ns_poly(const uint16_t* A, uint16_t* B, float b, float c, int batch, int64_t r,
-                int64_t ldr, void* stream);
+/* P[i] = a * I + b * A[i] + c * A[i] A[i]   (A symmetric; P out, bf16). */
+PRM_API int prm_ns_poly(const uint16_t* A, uint16_t* P, float a, float b, float c, int batch,
+                int64_t r, int64_t ldr, void* stream);
 
-/* Xout[i] = scale[i] * (a * X[i] + B[i] X[i])  (Xout must not alias X). */
-PRM_API int prm_ns_combine(const uint16_t* X, const uint16_t* B, uint16_t* Xout, const float* scale,
-                   float a, int batch, int64_t r, int64_t c, int64_t ldc, int64_t ldr,
-                   void* stream);
+/* Xout[i] = scale[i] * P[i] X[i]  (Xout must not alias X). */
+PRM_API int prm_ns_combine(const uint16_t* X, const uint16_t* P, uint16_t* Xout, const float* scale,
+                   int batch, int64_t r, int64_t c, int64_t ldc, int64_t ldr, void* stream);
 
 /* Bytes of workspace prm_newton_schulz needs for `batch` matrices of m x n. */
 PRM_API int prm_newton_schulz_workspace(int batch, int64_t m, int64_t n, size_t* bytes);

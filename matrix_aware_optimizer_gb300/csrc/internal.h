@@ -96,8 +96,8 @@ struct GemmLaunch {
 cudaError_t launch_gram(const NsMaps& xin, uint16_t* A, const GemmLaunch& g, cudaStream_t stream);
 cudaError_t launch_poly(const SymMaps& a, const uint16_t* A, uint16_t* B, const GemmLaunch& g,
                         cudaStream_t stream);
-cudaError_t launch_combine(const SymMaps& b, const NsMaps& xin, const uint16_t* X,
-                           uint16_t* Xout, const GemmLaunch& g, cudaStream_t stream);
+cudaError_t launch_combine(const SymMaps& b, const NsMaps& xin, uint16_t* Xout, const GemmLaunch& g,
+                           cudaStream_t stream);
 
 // Largest dynamic shared memory the GEMM kernels request (for set-up checks).
 size_t gemm_smem_bytes();

@@ -5,10 +5,14 @@
 //
 //   GRAM    : A  = s^2 * X X^T          (r x r, symmetric; upper super-blocks
 //                                         computed, lower ones mirrored)
-//   POLY    : B  = b A + c A A           (A symmetric, so A A = A A^T; same
+//   POLY    : P  = a I + b A + c A A     (A symmetric, so A A = A A^T; same
 //                                         triangle scheme, polynomial fused
 //                                         into the epilogue)
-//   COMBINE : X' = s * (a X + B X)       (r x c; axpy fused into the epilogue)
+//   COMBINE : X' = s * P X               (r x c; scaling in the epilogue)
+//
+// The round X' = a X + (b A + c A A) X is evaluated as (a I + b A + c A A) X:
+// the a X term rides along the diagonal of P instead of being re-read from
+// memory by the COMBINE epilogue.
 //
 // Each launch covers every matrix of a same-shape batch: the tile queue runs
 // over (matrix, tile) pairs, so small r x r products still fill the GPU.
@@ -29,9 +33,9 @@
 //                accumulators); in the even CTA one lane issues the MMAs
 //   warps 2..5 : epilogue -- tcgen05.ld of this CTA's 128 accumulator rows
 //                (one TMEM lane = one output row per thread), fused scaling /
-//                polynomial / axpy with the second operand tile read from
-//                global memory, bf16 stores (plus mirrored stores for
-//                symmetric outputs)
+//                polynomial (POLY reads A for its b A term from global
+//                memory), bf16 stores (plus mirrored stores for symmetric
+//                outputs)
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cudaTypedefs.h>
@@ -63,12 +67,16 @@ constexpr int NUM_THREADS = 192;
 constexpr int EPI_WARPS = 4;
 constexpr uint32_t TMEM_COLS = 2 * BN;
 constexpr size_t BARRIER_BYTES = 256;
-// Per epilogue warp: one 32 x 32 bf16 block for the mirrored stores, rows
-// padded to 40 elements (80 bytes) so that 16-byte row reads are free of
-// bank conflicts.
-constexpr int MIRROR_PITCH = 40;
-constexpr size_t MIRROR_BYTES = 4 * 32 * MIRROR_PITCH * 2;
-constexpr size_t SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + BARRIER_BYTES + MIRROR_BYTES;
+// Per epilogue warp: a 32 x 32 bf16 staging block (64-byte rows) through
+// which every output chunk leaves, so that each global store instruction
+// writes 8 rows of 64 contiguous bytes (whole 32-byte sectors) instead of 32
+// rows of 16 bytes. The 16-byte chunk c of block row rho sits at chunk
+// c ^ ((rho >> 1) & 3): row-per-lane writes and 8-rows-per-instruction reads
+// are then both free of bank conflicts.
+constexpr int STAGE_ROW_BYTES = 64;
+constexpr size_t EPI_STAGE_BYTES = 32 * STAGE_ROW_BYTES;
+constexpr size_t EPI_SMEM_BYTES = 4 * EPI_STAGE_BYTES;
+constexpr size_t SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + BARRIER_BYTES + EPI_SMEM_BYTES;
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;  // 2 s per individual wait
 
 struct GemmParams {
@@ -81,7 +89,7 @@ struct GemmParams {
   int64_t total_tiles;
   uint16_t* out;
   int64_t ld_out, stride_out;
-  const uint16_t* aux;  // POLY: A; COMBINE: X
+  const uint16_t* aux;  // POLY: A (for b A); unused otherwise
   int64_t ld_aux, stride_aux;
   const float* scale;
   float ca, cb, cc;
@@ -131,15 +139,9 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<const uint32_t*>(&h);
 }
 
-__device__ __forceinline__ uint16_t to_bf16_bits(float v) {
-  const __nv_bfloat16 h = __float2bfloat16_rn(v);
-  return *reinterpret_cast<const uint16_t*>(&h);
-}
-
 constexpr int EPI_CHUNKS = BN / 32;  // 32-column chunks per output row of a tile
 
-// The epilogue's second operand (A for POLY, X for COMBINE) for this
-// thread's output row: 8 chunks of 32 bf16 as packed words (element 2h of a
+// The POLY epilogue's second operand (A) for this thread's output row: 8 chunks of 32 bf16 as packed words (element 2h of a
 // chunk in the low half of word h), zero outside the matrix. Issued before
 // the wait for the accumulator, so its latency hides behind the mainloop.
 template <int KIND>
@@ -176,11 +178,40 @@ __device__ __forceinline__ float word_elem(const uint32_t (&w)[16], int k) {
   return (k & 1) ? __uint_as_float(w[k >> 1] & 0xFFFF0000u) : __uint_as_float(w[k >> 1] << 16);
 }
 
+__device__ __forceinline__ uint32_t stage_off(int row, int chunk) {
+  return static_cast<uint32_t>(row * STAGE_ROW_BYTES + ((chunk ^ ((row >> 1) & 3)) << 4));
+}
+
+// Writes the warp's staged 32 x 32 block: block row rho goes to global row
+// row0 + rho (pitch ld), columns col0 .. col0 + 31; rows >= row_end and
+// columns >= col_end are left alone.
+__device__ __forceinline__ void flush_stage(const uint8_t* stage, uint16_t* base, int64_t ld, int row0, int row_end,
+                                            int col0, int col_end, int lane) {
+  const int c = lane & 3;
+  const int jc = col0 + 8 * c;
+#pragma unroll
+  for (int it = 0; it < 4; ++it) {
+    const int rho = 8 * it + (lane >> 2);
+    const uint4 u = *reinterpret_cast<const uint4*>(stage + stage_off(rho, c));
+    const int row = row0 + rho;
+    if (row < row_end) {
+      uint16_t* dst = base + static_cast<int64_t>(row) * ld + jc;
+      if (jc + 8 <= col_end) {
+        *reinterpret_cast<uint4*>(dst) = u;
+      } else {
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+          if (jc + e < col_end) dst[e] = static_cast<uint16_t>(w[e >> 1] >> ((e & 1) * 16));
+      }
+    }
+  }
+}
+
 template <int KIND>
 __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileCoord& tc, int i, uint32_t t_row,
-                                              const uint32_t (&xr)[EPI_CHUNKS][16], uint16_t* mirror_tile,
-                                              int lane) {
-  const bool row_ok = i < p.M;
+                                              const uint32_t (&xr)[EPI_CHUNKS][16], uint8_t* stage, int lane) {
+  const int i0 = i - lane;  // first output row of this warp
   float s = 1.f;
   if (KIND == GEMM_GRAM && p.scale != nullptr) {
     const float q = p.scale[tc.mat];
@@ -195,59 +226,38 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileCoo
     if (j0 < p.N) {  // uniform over the warp: depends on the tile only
       float v[32];
       tmem_load_32cols(t_row + static_cast<uint32_t>(q * 32), v);
-      const bool full = j0 + 32 <= p.N;
-      const int n_valid = p.N - j0;
-      if (row_ok) {
-        if (KIND == GEMM_GRAM) {
+      if (KIND == GEMM_POLY) {
 #pragma unroll
-          for (int k = 0; k < 32; ++k) v[k] *= s;
-        } else if (KIND == GEMM_POLY) {
-#pragma unroll
-          for (int k = 0; k < 32; ++k) v[k] = p.cb * word_elem(xr[q], k) + p.cc * v[k];
-        } else {
-#pragma unroll
-          for (int k = 0; k < 32; ++k) v[k] = s * (p.ca * word_elem(xr[q], k) + v[k]);
-        }
-        uint16_t* dst = out + static_cast<int64_t>(i) * p.ld_out + j0;
-        if (full) {
-          uint4* d4 = reinterpret_cast<uint4*>(dst);
-#pragma unroll
-          for (int w = 0; w < 4; ++w) {
-            uint4 u;
-            u.x = pack_bf16x2(v[8 * w + 0], v[8 * w + 1]);
-            u.y = pack_bf16x2(v[8 * w + 2], v[8 * w + 3]);
-            u.z = pack_bf16x2(v[8 * w + 4], v[8 * w + 5]);
-            u.w = pack_bf16x2(v[8 * w + 6], v[8 * w + 7]);
-            d4[w] = u;
-          }
-        } else {
+        for (int k = 0; k < 32; ++k) v[k] = p.cb * word_elem(xr[q], k) + p.cc * v[k];
+        if (j0 == i0) {  // this chunk holds the warp's 32 diagonal elements (warp-uniform)
 #pragma unroll
           for (int k = 0; k < 32; ++k)
-            if (k < n_valid) dst[k] = to_bf16_bits(v[k]);
+            if (k == lane) v[k] += p.ca;
         }
+      } else {
+#pragma unroll
+        for (int k = 0; k < 32; ++k) v[k] *= s;
       }
+      uint32_t w[16];
+#pragma unroll
+      for (int h = 0; h < 16; ++h) w[h] = pack_bf16x2(v[2 * h], v[2 * h + 1]);
+      // this lane's row i, columns j0 .. j0 + 31
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+        *reinterpret_cast<uint4*>(stage + stage_off(lane, c)) =
+            make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+      __syncwarp();
+      flush_stage(stage, out, p.ld_out, i0, p.M, j0, p.N, lane);
+      __syncwarp();
       if (KIND != GEMM_COMBINE && tc.mirror) {
-        // Lower super-block (J, I): out[j][i] for the warp's 32 rows i and
-        // this chunk's 32 columns j. Transpose the 32 x 32 block through
-        // shared memory so that lane k then writes row j0 + k: 32 consecutive
-        // i as four 16-byte stores.
-        const int i0 = i - lane;
+        // Lower super-block (J, I): out[j][i] for this chunk's 32 columns j
+        // and the warp's 32 rows i, staged transposed (block row = j).
 #pragma unroll
-        for (int k = 0; k < 32; ++k) mirror_tile[k * MIRROR_PITCH + lane] = row_ok ? to_bf16_bits(v[k]) : 0;
+        for (int k = 0; k < 32; ++k)
+          *reinterpret_cast<uint16_t*>(stage + stage_off(k, lane >> 3) + (lane & 7) * 2) =
+              static_cast<uint16_t>(w[k >> 1] >> ((k & 1) * 16));
         __syncwarp();
-        const int j = j0 + lane;
-        if (j < p.N && i0 < p.M) {
-          const uint4* srow = reinterpret_cast<const uint4*>(mirror_tile + lane * MIRROR_PITCH);
-          uint16_t* drow = out + static_cast<int64_t>(j) * p.ld_out + i0;
-          if (i0 + 32 <= p.M) {
-            uint4* d4 = reinterpret_cast<uint4*>(drow);
-#pragma unroll
-            for (int w = 0; w < 4; ++w) d4[w] = srow[w];
-          } else {
-            const uint16_t* sr = mirror_tile + lane * MIRROR_PITCH;
-            for (int k = 0; i0 + k < p.M; ++k) drow[k] = sr[k];
-          }
-        }
+        flush_stage(stage, out, p.ld_out, j0, p.N, i0, p.M, lane);
         __syncwarp();
       }
     }
@@ -403,8 +413,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     }
   } else {
     const int quarter = warp & 3;  // TMEM lanes [32 * quarter, 32 * quarter + 32) belong to this warp
-    uint16_t* mirror_tile =
-        reinterpret_cast<uint16_t*>(smem + STAGES * STAGE_BYTES + BARRIER_BYTES) + quarter * 32 * MIRROR_PITCH;
+    uint8_t* stage = smem + STAGES * STAGE_BYTES + BARRIER_BYTES + quarter * EPI_STAGE_BYTES;
     const uint32_t tempty_even = mapa_shared(smem_u32(&tempty_bar[0]), 0);
     int acc = 0;
     uint32_t acc_phase = 0;
@@ -412,15 +421,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       const TileCoord tc = tile_coord<KIND>(p, tile);
       const int i = tc.m0 + static_cast<int>(rank) * BM + quarter * 32 + lane;
       uint32_t xr[EPI_CHUNKS][16];
-      if constexpr (KIND != GEMM_GRAM) prefetch_aux<KIND>(p, tc, i, xr);
+      if constexpr (KIND == GEMM_POLY) prefetch_aux<KIND>(p, tc, i, xr);
       const bool got = wait_bounded(&tfull_bar[acc], acc_phase, abort_flag, p.err, p.timeout_ns);
       if (!__all_sync(0xffffffffu, got)) break;
       tc_fence_after_sync();
       const uint32_t t_row = tmem_base + static_cast<uint32_t>(acc * BN) + (static_cast<uint32_t>(quarter * 32) << 16);
-      epilogue_tile<KIND>(p, tc, i, t_row, xr, mirror_tile, lane);
+      epilogue_tile<KIND>(p, tc, i, t_row, xr, stage, lane);
       tc_fence_before_sync();
       __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(tempty_even + static_cast<uint32_t>(acc * sizeof(uint64_t)));
+      if (lane == 0) mbar_arrive_remote(tempty_even + static_cast<uint32_t>(acc * sizeof(uint64_t)));
       if (++acc == 2) {
         acc = 0;
         acc_phase ^= 1u;
@@ -580,8 +589,8 @@ cudaError_t launch_poly(const SymMaps& a, const uint16_t* A, uint16_t* B, const 
   return launch_kind<GEMM_POLY>(a.rows128, a.rows128, p, g.num_sms, stream);
 }
 
-cudaError_t launch_combine(const SymMaps& b, const NsMaps& xin, const uint16_t* X, uint16_t* Xout,
-                           const GemmLaunch& g, cudaStream_t stream) {
+cudaError_t launch_combine(const SymMaps& b, const NsMaps& xin, uint16_t* Xout, const GemmLaunch& g,
+                           cudaStream_t stream) {
   GemmParams p = base_params(g);
   p.M = static_cast<int>(g.r);
   p.N = static_cast<int>(g.c);
@@ -594,9 +603,7 @@ cudaError_t launch_combine(const SymMaps& b, const NsMaps& xin, const uint16_t* 
   p.out = Xout;
   p.ld_out = g.ldc;
   p.stride_out = g.r * g.ldc;
-  p.aux = X;
-  p.ld_aux = g.ldc;
-  p.stride_aux = g.r * g.ldc;
+  p.aux = nullptr;
   return launch_kind<GEMM_COMBINE>(b.rows128, xin.x_k64, p, g.num_sms, stream);
 }
 

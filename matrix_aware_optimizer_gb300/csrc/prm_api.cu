@@ -284,6 +284,14 @@ struct prm_ctx {
   RowNormPlan rn;
   std::vector<NsPlan> ns_full, ns_blocks;  // sequential sub-plans (one unless a workspace cap splits them)
   size_t ws_limit = 0;                     // prm_set_workspace_limit; 0 = no cap
+  std::vector<View> full;                  // registered matrices, in registration order
+  struct {
+    bool valid = false;
+    int64_t t = 0;
+    int K = 1, mode = PRM_MODE_PRMUON;
+    float eps = 0.f;
+    float coeffs[3] = {0.f, 0.f, 0.f};
+  } last;                                  // the most recent prm_step (prm_debug_last_direction)
   bool registered = false;
   void* ws = nullptr;
   size_t ws_bytes = 0;
@@ -327,9 +335,34 @@ void clear_registration(prm_ctx* c) {
   for (auto& p : c->ns_blocks) free_plan(p);
   c->ns_full.clear();
   c->ns_blocks.clear();
+  c->full.clear();
+  c->last.valid = false;
   c->count = 0;
   c->blocks = 0;
   c->registered = false;
+}
+
+// MuonBP blocks of one matrix: P contiguous pieces along the long side, the
+// last one taking the remainder ("MuonBP: Faster Muon via Block-Periodic
+// Orthogonalization", abstract: each device orthogonalises its own block).
+void make_blocks(const View& v, int P, std::vector<View>& out) {
+  const bool wide = v.rows <= v.cols;
+  const int64_t L = wide ? v.cols : v.rows;
+  const int64_t base = L / P;
+  for (int k = 0; k < P; ++k) {
+    const int64_t lo = k * base, hi = (k == P - 1) ? L : lo + base;
+    const int64_t off = wide ? lo : lo * v.ld;
+    View b = v;
+    b.W = v.W + off;
+    b.M = v.M + off;
+    b.G = v.grad_bf16 ? static_cast<const void*>(static_cast<const uint16_t*>(v.G) + off)
+                      : static_cast<const void*>(static_cast<const float*>(v.G) + off);
+    if (wide)
+      b.cols = hi - lo;
+    else
+      b.rows = hi - lo;
+    out.push_back(b);
+  }
 }
 
 void add_to_sets(std::vector<LaunchSet>& sets, const View& v) {
@@ -436,6 +469,7 @@ int run_ns(prm_ctx* c, NsPlan& plan, void* base, bool update_momentum, float bet
       gl.c = rcl.r;
       gl.ldc = rcl.ldr;
       gl.ldr = rcl.ldr;
+      gl.ca = coeffs[0];
       gl.cb = coeffs[1];
       gl.cc = coeffs[2];
       gl.err = c->d_err;
@@ -449,10 +483,9 @@ int run_ns(prm_ctx* c, NsPlan& plan, void* base, bool update_momentum, float bet
     for (auto& g : plan.groups) {
       GemmLaunch gl = group_launch(g);
       gl.scale = it == 0 ? reinterpret_cast<float*>(b + g.off_scale) : nullptr;
-      uint16_t* cur = reinterpret_cast<uint16_t*>(b + (odd ? g.off_x1 : g.off_x0));
       uint16_t* nxt = reinterpret_cast<uint16_t*>(b + (odd ? g.off_x0 : g.off_x1));
       const size_t ev = c->prof.begin(stream);
-      if ((e = launch_combine(g.mb, odd ? g.mx1 : g.mx0, cur, nxt, gl, stream)) != cudaSuccess)
+      if ((e = launch_combine(g.mb, odd ? g.mx1 : g.mx0, nxt, gl, stream)) != cudaSuccess)
         return cuda_fail(c, e, "combine launch");
       c->prof.end(ev, PRM_FAMILY_NS_COMBINE, 1, 2.0 * g.count * double(g.r) * g.r * g.c, stream);
     }
@@ -619,29 +652,9 @@ int prm_register_matrices(prm_ctx* c, const prm_matrix_desc* d, int count, int m
   if (muonbp_blocks > 0) {
     for (int i = 0; i < count; ++i) {
       const View& v = full[i];
-      const bool wide = v.rows <= v.cols;
-      const int64_t L = wide ? v.cols : v.rows;
-      if (L < muonbp_blocks)
+      if ((v.rows <= v.cols ? v.cols : v.rows) < muonbp_blocks)
         return fail(c, PRM_ERR_SHAPE, "matrix " + std::to_string(i) + ": long side shorter than muonbp_blocks");
-      const int64_t base = L / muonbp_blocks;
-      for (int k = 0; k < muonbp_blocks; ++k) {
-        const int64_t lo = k * base, hi = (k == muonbp_blocks - 1) ? L : lo + base;
-        View b = v;
-        if (wide) {
-          b.W = v.W + lo;
-          b.M = v.M + lo;
-          b.G = v.grad_bf16 ? static_cast<const void*>(static_cast<const uint16_t*>(v.G) + lo)
-                            : static_cast<const void*>(static_cast<const float*>(v.G) + lo);
-          b.cols = hi - lo;
-        } else {
-          b.W = v.W + lo * v.ld;
-          b.M = v.M + lo * v.ld;
-          b.G = v.grad_bf16 ? static_cast<const void*>(static_cast<const uint16_t*>(v.G) + lo * v.ld)
-                            : static_cast<const void*>(static_cast<const float*>(v.G) + lo * v.ld);
-          b.rows = hi - lo;
-        }
-        blocks.push_back(b);
-      }
+      make_blocks(v, muonbp_blocks, blocks);
     }
   }
   // RowNorm launch sets (whole matrices), tall scratch laid out back to back.
@@ -666,6 +679,7 @@ int prm_register_matrices(prm_ctx* c, const prm_matrix_desc* d, int count, int m
     clear_registration(c);
     return cuda_fail(c, e, "uploading launch tables");
   }
+  c->full = std::move(full);
   c->count = count;
   c->blocks = muonbp_blocks;
   c->registered = true;
@@ -736,13 +750,137 @@ int prm_step(prm_ctx* c, int64_t t, int K, float gamma, float lr, float wd, floa
   sc.decay = 1.f - lr * wd;
   sc.eta = refresh ? lr : lr * gamma;
   sc.eps = eps;
-  if (mode == PRM_MODE_PRMUON && !refresh) return run_rownorm(c, c->ws, sc, st);
-  std::vector<NsPlan>& plans = (mode == PRM_MODE_MUONBP && !refresh) ? c->ns_blocks : c->ns_full;
-  for (auto& plan : plans) {
-    const int rc = run_ns(c, plan, c->ws, true, beta, sc.decay, sc.eta, coeffs, NS_STEPS, st);
+  c->last.valid = false;
+  if (mode == PRM_MODE_PRMUON && !refresh) {
+    const int rc = run_rownorm(c, c->ws, sc, st);
     if (rc != PRM_OK) return rc;
+  } else {
+    std::vector<NsPlan>& plans = (mode == PRM_MODE_MUONBP && !refresh) ? c->ns_blocks : c->ns_full;
+    for (auto& plan : plans) {
+      const int rc = run_ns(c, plan, c->ws, true, beta, sc.decay, sc.eta, coeffs, NS_STEPS, st);
+      if (rc != PRM_OK) return rc;
+    }
   }
+  c->last.valid = true;
+  c->last.t = t;
+  c->last.K = K;
+  c->last.mode = mode;
+  c->last.eps = eps;
+  for (int i = 0; i < 3; ++i) c->last.coeffs[i] = coeffs[i];
   return PRM_OK;
+}
+
+// Recomputes the direction D of the last step for one matrix from its
+// momentum (which, after the step, is the M_t the direction was taken from)
+// with the step's own kernels, on scratch buffers: the NS5 branch runs the
+// prep / GEMM / apply launches with the apply writing D instead of updating W;
+// the RowNorm branch runs the RowNorm kernels on a copy of M with beta = 1,
+// G = 0, W = 0, decay = 1 and eta * s = -1, so that the "update" leaves
+// W = M / max(||v||, eps) = D.
+int prm_debug_last_direction(prm_ctx* c, int idx, float* host_out) {
+  if (c == nullptr) return fail(nullptr, PRM_ERR_INVALID_ARG, "ctx is NULL");
+  if (!c->registered) return fail(c, PRM_ERR_NOT_REGISTERED, "no matrices registered");
+  if (idx < 0 || idx >= c->count) return fail(c, PRM_ERR_INVALID_ARG, "matrix index out of range");
+  if (host_out == nullptr) return fail(c, PRM_ERR_INVALID_ARG, "host_out is NULL");
+  if (!c->last.valid) return fail(c, PRM_ERR_INVALID_ARG, "no step has been taken since registration");
+  DeviceGuard guard(c->device);
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_fail(c, e, "device synchronize");
+  const View& v = c->full[idx];
+  const size_t n = static_cast<size_t>(v.rows) * v.cols;
+  const bool refresh = c->last.t % c->last.K == 0;
+  const cudaStream_t st = nullptr;
+  std::vector<void*> scratch;  // freed on every return path
+  auto dev_alloc = [&](size_t bytes) -> void* {
+    void* p = nullptr;
+    if (cudaMalloc(&p, bytes < 256 ? 256 : bytes) != cudaSuccess) return nullptr;
+    scratch.push_back(p);
+    return p;
+  };
+  auto finish = [&](int rc) {
+    for (void* p : scratch) cudaFree(p);
+    return rc;
+  };
+  float* d_out = static_cast<float*>(dev_alloc(n * sizeof(float)));
+  if (d_out == nullptr) return finish(fail(c, PRM_ERR_OOM, "no device memory for the direction"));
+  if (c->last.mode == PRM_MODE_PRMUON && !refresh) {
+    float* d_m = static_cast<float*>(dev_alloc(n * sizeof(float)));
+    float* d_g = static_cast<float*>(dev_alloc(n * sizeof(float)));
+    if (d_m == nullptr || d_g == nullptr) return finish(fail(c, PRM_ERR_OOM, "no device memory for scratch"));
+    if ((e = cudaMemcpy(d_m, v.M, n * sizeof(float), cudaMemcpyDeviceToDevice)) != cudaSuccess ||
+        (e = cudaMemset(d_g, 0, n * sizeof(float))) != cudaSuccess ||
+        (e = cudaMemset(d_out, 0, n * sizeof(float))) != cudaSuccess)
+      return finish(cuda_fail(c, e, "scratch set-up"));
+    View dv = v;
+    dv.W = d_out;
+    dv.M = d_m;
+    dv.G = d_g;
+    dv.grad_bf16 = 0;
+    dv.shape_scale = 1.f;
+    std::vector<LaunchSet> sets;
+    add_to_sets(sets, dv);
+    if ((e = upload_sets(sets)) != cudaSuccess) {
+      free_sets(sets);
+      return finish(cuda_fail(c, e, "uploading the launch table"));
+    }
+    StepScalars sc;
+    sc.beta = 1.f;
+    sc.decay = 1.f;
+    sc.eta = -1.f;
+    sc.eps = c->last.eps;
+    const LaunchSet& s = sets.front();
+    if (v.rows <= v.cols) {
+      e = launch_rownorm_wide(s.d_views, 1, v.rows, v.cols, s.vec_ok, false, sc, st);
+    } else {
+      const size_t pb = static_cast<size_t>(tall_row_blocks(v.rows)) * v.cols * sizeof(float);
+      float* d_part = static_cast<float*>(dev_alloc(pb));
+      float* d_inv = static_cast<float*>(dev_alloc(static_cast<size_t>(v.cols) * sizeof(float)));
+      if (d_part == nullptr || d_inv == nullptr) {
+        free_sets(sets);
+        return finish(fail(c, PRM_ERR_OOM, "no device memory for scratch"));
+      }
+      e = launch_rownorm_tall(s.d_views, 1, v.rows, v.cols, s.vec_ok, false, sc, d_part, d_inv, st);
+    }
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    free_sets(sets);
+    if (e != cudaSuccess) return finish(cuda_fail(c, e, "rownorm direction"));
+  } else {
+    // NS5 of the whole matrix (refresh / full step) or of each MuonBP block.
+    std::vector<View> parts;
+    if (refresh)
+      parts.push_back(v);
+    else
+      make_blocks(v, c->blocks, parts);
+    for (View& p : parts) {
+      p.out = d_out + (p.M - v.M);  // same offset and pitch as the block inside M
+      p.W = nullptr;
+    }
+    NsPlan plan;
+    build_ns_plan(parts, plan);
+    for (auto& g : plan.groups) {
+      if ((e = upload_sets(g.sets)) != cudaSuccess) {
+        free_plan(plan);
+        return finish(cuda_fail(c, e, "uploading launch tables"));
+      }
+    }
+    void* ws = dev_alloc(plan.bytes);
+    if (ws == nullptr) {
+      free_plan(plan);
+      return finish(fail(c, PRM_ERR_OOM, "no device memory for the NS5 workspace"));
+    }
+    prm_ctx tmp;
+    tmp.num_sms = c->num_sms;
+    tmp.d_err = c->d_err;
+    int rc = run_ns(&tmp, plan, ws, false, 0.f, 1.f, 1.f, c->last.coeffs, NS_STEPS, st);
+    e = cudaStreamSynchronize(st);
+    free_plan(plan);
+    tmp.d_err = nullptr;
+    if (rc != PRM_OK) return finish(fail(c, rc, tmp.err));
+    if (e != cudaSuccess) return finish(cuda_fail(c, e, "NS5 direction"));
+  }
+  if ((e = cudaMemcpy(host_out, d_out, n * sizeof(float), cudaMemcpyDeviceToHost)) != cudaSuccess)
+    return finish(cuda_fail(c, e, "copying the direction to the host"));
+  return finish(PRM_OK);
 }
 
 int prm_sync_status(prm_ctx* c, void* stream) {
@@ -822,7 +960,7 @@ int prm_ns_gram(const uint16_t* X, uint16_t* A, const float* scale, int batch, i
   return launch_gram(mx, A, g, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PRM_OK : PRM_ERR_CUDA;
 }
 
-int prm_ns_poly(const uint16_t* A, uint16_t* B, float b, float cc, int batch, int64_t r, int64_t ldr,
+int prm_ns_poly(const uint16_t* A, uint16_t* B, float a, float b, float cc, int batch, int64_t r, int64_t ldr,
                 void* stream) {
   if (A == nullptr || B == nullptr || batch < 0 || r < 1 || ldr < r) return PRM_ERR_INVALID_ARG;
   if (ldr % 8 || !aligned16(A) || !aligned16(B)) return PRM_ERR_ALIGNMENT;
@@ -838,6 +976,7 @@ int prm_ns_poly(const uint16_t* A, uint16_t* B, float b, float cc, int batch, in
   g.c = r;
   g.ldc = ldr;
   g.ldr = ldr;
+  g.ca = a;
   g.cb = b;
   g.cc = cc;
   g.err = ds->d_err;
@@ -845,8 +984,8 @@ int prm_ns_poly(const uint16_t* A, uint16_t* B, float b, float cc, int batch, in
   return launch_poly(ma, A, B, g, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PRM_OK : PRM_ERR_CUDA;
 }
 
-int prm_ns_combine(const uint16_t* X, const uint16_t* B, uint16_t* Xout, const float* scale, float a, int batch,
-                   int64_t r, int64_t c, int64_t ldc, int64_t ldr, void* stream) {
+int prm_ns_combine(const uint16_t* X, const uint16_t* B, uint16_t* Xout, const float* scale, int batch, int64_t r,
+                   int64_t c, int64_t ldc, int64_t ldr, void* stream) {
   if (X == nullptr || B == nullptr || Xout == nullptr || batch < 0 || r < 1 || c < r || ldc < c || ldr < r)
     return PRM_ERR_INVALID_ARG;
   if (X == Xout) return PRM_ERR_INVALID_ARG;
@@ -866,11 +1005,9 @@ int prm_ns_combine(const uint16_t* X, const uint16_t* B, uint16_t* Xout, const f
   g.ldc = ldc;
   g.ldr = ldr;
   g.scale = scale;
-  g.ca = a;
   g.err = ds->d_err;
   g.num_sms = ds->num_sms;
-  return launch_combine(mb, mx, X, Xout, g, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PRM_OK
-                                                                                                : PRM_ERR_CUDA;
+  return launch_combine(mb, mx, Xout, g, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PRM_OK : PRM_ERR_CUDA;
 }
 
 static void standalone_group(int batch, int64_t m, int64_t n, NsPlan& plan) {

@@ -183,9 +183,13 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t saddr, uint32_t rank) {
   return out;
 }
 
-// Arrive (release, cluster scope) on an mbarrier given by a shared::cluster address.
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+// Arrive on an mbarrier given by a shared::cluster address (possibly in the
+// peer CTA) with the default CTA-scope release: the arrival only has to order
+// this thread's completed tcgen05.ld reads before the barrier's consumer, so it
+// must not wait for the thread's global stores to become visible cluster-wide
+// (which a cluster-scope release would).
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 
 __device__ __forceinline__ void cluster_sync_all() {

@@ -69,14 +69,15 @@ SIGNATURES = {
                          POINTER(c_float), c_int, c_void_p]),
     "prm_branch": (c_int, [c_int64, c_int, c_int]),
     "prm_sync_status": (c_int, [c_void_p, c_void_p]),
+    "prm_debug_last_direction": (c_int, [c_void_p, c_int, c_void_p]),
     "prm_last_error": (c_char_p, [c_void_p]),
     "prm_profile": (c_int, [c_void_p, c_int]),
     "prm_profile_read": (c_int, [c_void_p, c_int, POINTER(ctypes.c_double), POINTER(c_int64), POINTER(c_int64),
                                  POINTER(ctypes.c_double)]),
     "prm_ns_gram": (c_int, [c_void_p, c_void_p, c_void_p, c_int, c_int64, c_int64, c_int64, c_int64, c_void_p]),
-    "prm_ns_poly": (c_int, [c_void_p, c_void_p, c_float, c_float, c_int, c_int64, c_int64, c_void_p]),
-    "prm_ns_combine": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_float, c_int, c_int64, c_int64,
-                               c_int64, c_int64, c_void_p]),
+    "prm_ns_poly": (c_int, [c_void_p, c_void_p, c_float, c_float, c_float, c_int, c_int64, c_int64, c_void_p]),
+    "prm_ns_combine": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int64, c_int64, c_int64,
+                               c_int64, c_void_p]),
     "prm_rownorm_tall_step_noalloc": (c_int, [c_void_p, c_void_p, c_void_p, c_int, c_int64, c_int64, c_float,
                                               c_float, c_float, c_float, c_float, c_float, c_void_p]),
     "prm_adamw_step": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int64, c_int64, ctypes.c_double,
@@ -174,6 +175,11 @@ def prm_sync_status(ctx, stream: int = 0) -> int:
     return load().prm_sync_status(ctx, c_void_p(stream))
 
 
+def prm_debug_last_direction(ctx, idx: int, host_out: int) -> None:
+    """host_out: address of rows * cols writable host floats."""
+    check(load().prm_debug_last_direction(ctx, idx, c_void_p(host_out)), "prm_debug_last_direction", ctx)
+
+
 def prm_profile(ctx, enable: bool) -> None:
     check(load().prm_profile(ctx, 1 if enable else 0), "prm_profile", ctx)
 
@@ -192,14 +198,14 @@ def prm_ns_gram(X: int, A: int, scale: int, batch: int, r: int, c: int, ldc: int
                              c_void_p(stream)), "prm_ns_gram")
 
 
-def prm_ns_poly(A: int, B: int, b: float, cc: float, batch: int, r: int, ldr: int, stream: int = 0):
-    check(load().prm_ns_poly(c_void_p(A), c_void_p(B), b, cc, batch, r, ldr, c_void_p(stream)), "prm_ns_poly")
+def prm_ns_poly(A: int, P: int, a: float, b: float, cc: float, batch: int, r: int, ldr: int, stream: int = 0):
+    check(load().prm_ns_poly(c_void_p(A), c_void_p(P), a, b, cc, batch, r, ldr, c_void_p(stream)), "prm_ns_poly")
 
 
-def prm_ns_combine(X: int, B: int, Xout: int, scale: int, a: float, batch: int, r: int, c: int, ldc: int,
-                   ldr: int, stream: int = 0):
-    check(load().prm_ns_combine(c_void_p(X), c_void_p(B), c_void_p(Xout), c_void_p(scale), a, batch, r, c,
-                                ldc, ldr, c_void_p(stream)), "prm_ns_combine")
+def prm_ns_combine(X: int, P: int, Xout: int, scale: int, batch: int, r: int, c: int, ldc: int, ldr: int,
+                   stream: int = 0):
+    check(load().prm_ns_combine(c_void_p(X), c_void_p(P), c_void_p(Xout), c_void_p(scale), batch, r, c, ldc, ldr,
+                                c_void_p(stream)), "prm_ns_combine")
 
 
 def prm_rownorm_tall_step_noalloc(param: int, momentum: int, grad: int, grad_dtype: int, rows: int, cols: int,

@@ -26,11 +26,18 @@ class PeriodicRowMuon:
                        sqrt(max(1, rows / cols))).
     workspace_limit  : cap in bytes on the NS5 workspace (0 = none): the
                        refresh then runs in sequential sub-plans that fit it.
+    workspace        : optional uint8 CUDA tensor to use as the scratch instead
+                       of allocating one (at least workspace_bytes large).
+                       Optimizers whose steps are ordered on one stream may
+                       share it -- e.g. two instances over the same params and
+                       momenta with two gradient buffers, alternating steps so
+                       that one buffer fills while the other is consumed.
     """
 
     def __init__(self, params: Sequence[torch.Tensor], momenta: Sequence[torch.Tensor],
                  grads: Sequence[torch.Tensor], muonbp_blocks: int = 0,
-                 shape_scales: Optional[Sequence[float]] = None, workspace_limit: int = 0):
+                 shape_scales: Optional[Sequence[float]] = None, workspace_limit: int = 0,
+                 workspace: Optional[torch.Tensor] = None):
         if not (len(params) == len(momenta) == len(grads)):
             raise ValueError("params, momenta and grads must have the same length")
         dev = params[0].device if params else torch.device("cuda", torch.cuda.current_device())
@@ -61,7 +68,14 @@ class PeriodicRowMuon:
                 N.prm_set_workspace_limit(self.ctx, int(workspace_limit))
                 N.prm_register_matrices(self.ctx, descs, muonbp_blocks)
                 nbytes = N.prm_workspace_bytes(self.ctx)
-                self.workspace = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=dev)
+                if workspace is None:
+                    self.workspace = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=dev)
+                else:
+                    if (workspace.dtype != torch.uint8 or workspace.device != dev or not workspace.is_contiguous()
+                            or workspace.numel() < nbytes):
+                        raise ValueError(f"workspace must be a contiguous uint8 tensor on {dev} "
+                                         f"of at least {nbytes} bytes")
+                    self.workspace = workspace
                 N.prm_set_workspace(self.ctx, self.workspace.data_ptr(), self.workspace.numel())
             except Exception:
                 N.prm_destroy(self.ctx)
@@ -82,6 +96,14 @@ class PeriodicRowMuon:
 
     def sync_status(self, stream: Optional[torch.cuda.Stream] = None) -> None:
         N.check(N.prm_sync_status(self.ctx, _stream_handle(stream)), "prm_sync_status", self.ctx)
+
+    def last_direction(self, idx: int) -> torch.Tensor:
+        """Direction D of the last step for matrix idx (before s * eta), as a
+        CPU fp32 tensor; the momentum must still hold that step's M_t."""
+        rows, cols = self._tensors[0][idx].shape
+        out = torch.empty(rows, cols, dtype=torch.float32)
+        N.prm_debug_last_direction(self.ctx, idx, out.data_ptr())
+        return out
 
     def close(self) -> None:
         if getattr(self, "ctx", None) is not None:

@@ -91,6 +91,13 @@ MATRIX_SETS: Dict[str, MatrixSet] = {
         mode="muonbp", blocks=8, lr=0.02 * 0.8, gamma=1.25,
         description="MuonBP on the 1.3B set: 8 blocks per matrix along the long side; "
                     "lr_block=0.02 (block steps), lr_full=0.016 (every 3rd step)"),
+    "dit_1p3b_4blk_muonbp": MatrixSet(
+        name="dit_1p3b_4blk_muonbp",
+        shapes=_dit_set(2048, 4, None),
+        grad_dtype=GRAD_BF16, grad_std=1e-3, steps=30,
+        mode="muonbp", blocks=8, lr=0.02 * 0.8, gamma=1.25,
+        description="MuonBP on 4 blocks of the 1.3B-shaped set: a profiling case with the full "
+                    "set's block shapes (768, 256 and 1024 x 2048 NS5 groups) on a few GB"),
     "dit_15b": MatrixSet(
         name="dit_15b",
         shapes=_dit_set(5120, 48, None),

@@ -64,11 +64,11 @@ def test_poly_matches_fp32_matmul(batch, r, c):
     A[:, :, :r] = Asym
     Ad = A.cuda()
     Bd = torch.full((batch, r, ldr), float("nan"), dtype=torch.bfloat16, device="cuda")
-    N.prm_ns_poly(Ad.data_ptr(), Bd.data_ptr(), B_C, C_C, batch, r, ldr, torch.cuda.current_stream().cuda_stream)
+    N.prm_ns_poly(Ad.data_ptr(), Bd.data_ptr(), A_C, B_C, C_C, batch, r, ldr, torch.cuda.current_stream().cuda_stream)
     torch.cuda.synchronize()
     B = Bd.float().cpu()[:, :, :r]
     Af = Asym.float()
-    ref = B_C * Af + C_C * (Af @ Af)
+    ref = A_C * torch.eye(r) + B_C * Af + C_C * (Af @ Af)
     for i in range(batch):
         assert torch.isfinite(B[i]).all()
         assert rel_frob(B[i].numpy(), ref[i].numpy()) < 4e-3
@@ -80,18 +80,18 @@ def test_combine_matches_fp32_matmul(batch, r, c):
     ldc, ldr = _pitch(c), _pitch(r)
     X = _rand_bf16(batch, r, c, ldc, gen, 1.0 / np.sqrt(c))
     Braw = torch.randn(batch, r, r, generator=gen) / np.sqrt(r)
-    Bsym = ((Braw + Braw.transpose(1, 2)) / 2).to(torch.bfloat16)
+    Bsym = ((Braw + Braw.transpose(1, 2)) / 2 + A_C * torch.eye(r)).to(torch.bfloat16)
     B = torch.zeros(batch, r, ldr, dtype=torch.bfloat16)
     B[:, :, :r] = Bsym
     scale = torch.rand(batch, generator=gen) + 0.5
     Xd, Bd, sd = X.cuda(), B.cuda(), scale.cuda()
     Od = torch.full((batch, r, ldc), float("nan"), dtype=torch.bfloat16, device="cuda")
-    N.prm_ns_combine(Xd.data_ptr(), Bd.data_ptr(), Od.data_ptr(), sd.data_ptr(), A_C, batch, r, c, ldc, ldr,
+    N.prm_ns_combine(Xd.data_ptr(), Bd.data_ptr(), Od.data_ptr(), sd.data_ptr(), batch, r, c, ldc, ldr,
                      torch.cuda.current_stream().cuda_stream)
     torch.cuda.synchronize()
     O_ = Od.float().cpu()[:, :, :c]
     Xf = X.float()[:, :, :c]
-    ref = scale[:, None, None] * (A_C * Xf + Bsym.float() @ Xf)
+    ref = scale[:, None, None] * (Bsym.float() @ Xf)
     for i in range(batch):
         assert torch.isfinite(O_[i]).all()
         assert rel_frob(O_[i].numpy(), ref[i].numpy()) < 4e-3
@@ -106,7 +106,7 @@ def test_combine_is_not_symmetric_in_disguise():
     B = torch.triu(torch.randn(1, r, r, generator=gen) * 0.05).to(torch.bfloat16)
     Xd, Bd = X.cuda(), B.cuda()
     Od = torch.empty(1, r, c, dtype=torch.bfloat16, device="cuda")
-    N.prm_ns_combine(Xd.data_ptr(), Bd.data_ptr(), Od.data_ptr(), 0, 0.0, 1, r, c, c, r,
+    N.prm_ns_combine(Xd.data_ptr(), Bd.data_ptr(), Od.data_ptr(), 0, 1, r, c, c, r,
                      torch.cuda.current_stream().cuda_stream)
     torch.cuda.synchronize()
     ref = B.float() @ X.float()
