@@ -76,9 +76,11 @@ enum GemmKind { GEMM_GRAM = 0, GEMM_POLY = 1, GEMM_COMBINE = 2 };
 struct NsMaps {
   CUtensorMap x_rows128;   // X as K-major operand, 128-row box
   CUtensorMap x_k64;       // X as MN-major operand, 64 x 64 box
+  CUtensorMap store;       // X as a GEMM output, 32 x 32 box (epilogue stores)
 };
 struct SymMaps {
   CUtensorMap rows128;     // A or B as K-major operand, 128-row box
+  CUtensorMap store;       // A or B as a GEMM output, 32 x 32 box
 };
 
 int encode_x_maps(NsMaps* maps, const void* X, int batch, int64_t r, int64_t c, int64_t ldc);
@@ -93,10 +95,13 @@ struct GemmLaunch {
   int num_sms;
 };
 
-cudaError_t launch_gram(const NsMaps& xin, uint16_t* A, const GemmLaunch& g, cudaStream_t stream);
-cudaError_t launch_poly(const SymMaps& a, const uint16_t* A, uint16_t* B, const GemmLaunch& g,
+// Output maps: GRAM writes matrices [out_z0, out_z0 + batch) of `aout`
+// (the r-class array of A), POLY the r-class array of B, COMBINE `xout`.
+cudaError_t launch_gram(const NsMaps& xin, const SymMaps& aout, int out_z0, const GemmLaunch& g,
                         cudaStream_t stream);
-cudaError_t launch_combine(const SymMaps& b, const NsMaps& xin, uint16_t* Xout, const GemmLaunch& g,
+cudaError_t launch_poly(const SymMaps& a, const uint16_t* A, const SymMaps& bout, const GemmLaunch& g,
+                        cudaStream_t stream);
+cudaError_t launch_combine(const SymMaps& b, const NsMaps& xin, const NsMaps& xout, const GemmLaunch& g,
                            cudaStream_t stream);
 
 // Largest dynamic shared memory the GEMM kernels request (for set-up checks).

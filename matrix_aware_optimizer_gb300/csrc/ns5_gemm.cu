@@ -34,8 +34,9 @@
 //   warps 2..5 : epilogue -- tcgen05.ld of this CTA's 128 accumulator rows
 //                (one TMEM lane = one output row per thread), fused scaling /
 //                polynomial (POLY reads A for its b A term from global
-//                memory), bf16 stores (plus mirrored stores for symmetric
-//                outputs)
+//                memory), bf16 results staged per 32 x 32 box in shared
+//                memory and written by TMA stores (plus the transposed box
+//                for the mirrored half of symmetric outputs)
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cudaTypedefs.h>
@@ -67,16 +68,19 @@ constexpr int NUM_THREADS = 192;
 constexpr int EPI_WARPS = 4;
 constexpr uint32_t TMEM_COLS = 2 * BN;
 constexpr size_t BARRIER_BYTES = 256;
-// Per epilogue warp: a 32 x 32 bf16 staging block (64-byte rows) through
-// which every output chunk leaves, so that each global store instruction
-// writes 8 rows of 64 contiguous bytes (whole 32-byte sectors) instead of 32
-// rows of 16 bytes. The 16-byte chunk c of block row rho sits at chunk
-// c ^ ((rho >> 1) & 3): row-per-lane writes and 8-rows-per-instruction reads
-// are then both free of bank conflicts.
+// Epilogue staging: per epilogue warp four 32 x 32 bf16 boxes (64-byte rows;
+// two for the tile's own chunks, two for the mirrored ones, used in
+// alternation) from which TMA stores write the output. The boxes follow the
+// output maps' 64-byte swizzle: the 16-byte chunk c of box row rho sits at
+// chunk c ^ ((rho >> 1) & 3) (address bits [5:4] ^= bits [8:7] of a
+// 512-byte aligned box), which also keeps the row-per-lane writes free of
+// bank conflicts.
 constexpr int STAGE_ROW_BYTES = 64;
-constexpr size_t EPI_STAGE_BYTES = 32 * STAGE_ROW_BYTES;
-constexpr size_t EPI_SMEM_BYTES = 4 * EPI_STAGE_BYTES;
-constexpr size_t SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + BARRIER_BYTES + EPI_SMEM_BYTES;
+constexpr uint32_t EPI_BUF_BYTES = 32 * STAGE_ROW_BYTES;
+constexpr uint32_t EPI_WARP_BYTES = 4 * EPI_BUF_BYTES;
+constexpr size_t EPI_SMEM_BYTES = EPI_WARPS * EPI_WARP_BYTES;
+constexpr size_t SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + EPI_SMEM_BYTES + BARRIER_BYTES;
+static_assert(SMEM_BYTES <= 232448, "dynamic shared memory above the 227 KB per-block limit");
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;  // 2 s per individual wait
 
 struct GemmParams {
@@ -87,8 +91,7 @@ struct GemmParams {
   int nb;             // GRAM/POLY: ceil(M / 256) super-blocks per side
   int tiles_per_mat;
   int64_t total_tiles;
-  uint16_t* out;
-  int64_t ld_out, stride_out;
+  int out_z0;           // first matrix of the output map this launch writes
   const uint16_t* aux;  // POLY: A (for b A); unused otherwise
   int64_t ld_aux, stride_aux;
   const float* scale;
@@ -182,35 +185,14 @@ __device__ __forceinline__ uint32_t stage_off(int row, int chunk) {
   return static_cast<uint32_t>(row * STAGE_ROW_BYTES + ((chunk ^ ((row >> 1) & 3)) << 4));
 }
 
-// Writes the warp's staged 32 x 32 block: block row rho goes to global row
-// row0 + rho (pitch ld), columns col0 .. col0 + 31; rows >= row_end and
-// columns >= col_end are left alone.
-__device__ __forceinline__ void flush_stage(const uint8_t* stage, uint16_t* base, int64_t ld, int row0, int row_end,
-                                            int col0, int col_end, int lane) {
-  const int c = lane & 3;
-  const int jc = col0 + 8 * c;
-#pragma unroll
-  for (int it = 0; it < 4; ++it) {
-    const int rho = 8 * it + (lane >> 2);
-    const uint4 u = *reinterpret_cast<const uint4*>(stage + stage_off(rho, c));
-    const int row = row0 + rho;
-    if (row < row_end) {
-      uint16_t* dst = base + static_cast<int64_t>(row) * ld + jc;
-      if (jc + 8 <= col_end) {
-        *reinterpret_cast<uint4*>(dst) = u;
-      } else {
-        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-        for (int e = 0; e < 8; ++e)
-          if (jc + e < col_end) dst[e] = static_cast<uint16_t>(w[e >> 1] >> ((e & 1) * 16));
-      }
-    }
-  }
-}
-
+// One tile's epilogue for this warp's 32 accumulator rows. `nchunk` counts
+// the warp's chunks across tiles: its parity picks the staging boxes, whose
+// previous stores (two chunks back) must have read them before they are
+// rewritten.
 template <int KIND>
-__device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileCoord& tc, int i, uint32_t t_row,
-                                              const uint32_t (&xr)[EPI_CHUNKS][16], uint8_t* stage, int lane) {
+__device__ __forceinline__ void epilogue_tile(const GemmParams& p, const CUtensorMap* tm_out, const TileCoord& tc,
+                                              int i, uint32_t t_row, const uint32_t (&xr)[EPI_CHUNKS][16],
+                                              uint8_t* stage, int lane, uint32_t& nchunk) {
   const int i0 = i - lane;  // first output row of this warp
   float s = 1.f;
   if (KIND == GEMM_GRAM && p.scale != nullptr) {
@@ -218,7 +200,8 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileCoo
     s = q * q;
   }
   if (KIND == GEMM_COMBINE && p.scale != nullptr) s = p.scale[tc.mat];
-  uint16_t* out = p.out + static_cast<int64_t>(tc.mat) * p.stride_out;
+  const int z = p.out_z0 + tc.mat;
+  const bool rows_in = i0 < p.M;  // warp-uniform
 
 #pragma unroll
   for (int q = 0; q < EPI_CHUNKS; ++q) {
@@ -241,24 +224,33 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileCoo
       uint32_t w[16];
 #pragma unroll
       for (int h = 0; h < 16; ++h) w[h] = pack_bf16x2(v[2 * h], v[2 * h + 1]);
+      const bool mirror = KIND != GEMM_COMBINE && tc.mirror;
+      uint8_t* bd = stage + (nchunk & 1u) * EPI_BUF_BYTES;
+      uint8_t* bm = stage + (2u + (nchunk & 1u)) * EPI_BUF_BYTES;
+      ++nchunk;
+      if (lane == 0) bulk_wait_group_read<1>();
+      __syncwarp();
       // this lane's row i, columns j0 .. j0 + 31
 #pragma unroll
       for (int c = 0; c < 4; ++c)
-        *reinterpret_cast<uint4*>(stage + stage_off(lane, c)) =
+        *reinterpret_cast<uint4*>(bd + stage_off(lane, c)) =
             make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
-      __syncwarp();
-      flush_stage(stage, out, p.ld_out, i0, p.M, j0, p.N, lane);
-      __syncwarp();
-      if (KIND != GEMM_COMBINE && tc.mirror) {
+      if (mirror) {
         // Lower super-block (J, I): out[j][i] for this chunk's 32 columns j
-        // and the warp's 32 rows i, staged transposed (block row = j).
+        // and the warp's 32 rows i, staged transposed (box row = j).
 #pragma unroll
         for (int k = 0; k < 32; ++k)
-          *reinterpret_cast<uint16_t*>(stage + stage_off(k, lane >> 3) + (lane & 7) * 2) =
+          *reinterpret_cast<uint16_t*>(bm + stage_off(k, lane >> 3) + (lane & 7) * 2) =
               static_cast<uint16_t>(w[k >> 1] >> ((k & 1) * 16));
-        __syncwarp();
-        flush_stage(stage, out, p.ld_out, j0, p.N, i0, p.M, lane);
-        __syncwarp();
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        if (rows_in) {
+          tma_store_3d(tm_out, bd, j0, i0, z);
+          if (mirror) tma_store_3d(tm_out, bm, i0, j0, z);
+        }
+        bulk_commit_group();
       }
     }
   }
@@ -267,12 +259,13 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const TileCoo
 template <int KIND>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     ns_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const GemmParams p) {
+                   const __grid_constant__ CUtensorMap tmOut, const GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
   uint8_t* sB = smem + STAGES * A_TILE_BYTES;
-  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  uint8_t* sEpi = smem + STAGES * STAGE_BYTES;  // 1024-byte aligned
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(sEpi + EPI_SMEM_BYTES);
   uint64_t* empty_bar = full_bar + STAGES;
   uint64_t* tfull_bar = empty_bar + STAGES;
   uint64_t* tempty_bar = tfull_bar + 2;
@@ -413,7 +406,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     }
   } else {
     const int quarter = warp & 3;  // TMEM lanes [32 * quarter, 32 * quarter + 32) belong to this warp
-    uint8_t* stage = smem + STAGES * STAGE_BYTES + BARRIER_BYTES + quarter * EPI_STAGE_BYTES;
+    uint8_t* stage = sEpi + quarter * EPI_WARP_BYTES;
+    uint32_t nchunk = 0;
+    if (lane == 0) tma_prefetch_desc(&tmOut);
     const uint32_t tempty_even = mapa_shared(smem_u32(&tempty_bar[0]), 0);
     int acc = 0;
     uint32_t acc_phase = 0;
@@ -426,7 +421,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       if (!__all_sync(0xffffffffu, got)) break;
       tc_fence_after_sync();
       const uint32_t t_row = tmem_base + static_cast<uint32_t>(acc * BN) + (static_cast<uint32_t>(quarter * 32) << 16);
-      epilogue_tile<KIND>(p, tc, i, t_row, xr, stage, lane);
+      epilogue_tile<KIND>(p, &tmOut, tc, i, t_row, xr, stage, lane, nchunk);
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive_remote(tempty_even + static_cast<uint32_t>(acc * sizeof(uint64_t)));
@@ -435,6 +430,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         acc_phase ^= 1u;
       }
     }
+    // the staging boxes must stay valid until every issued store has run
+    if (lane == 0) bulk_wait_group_all();
   }
   __syncwarp();
   // No CTA may leave (or free TMEM) while its peer can still touch its
@@ -462,10 +459,11 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 }
 
 // 3-D bf16 tensor map over `batch` row-major matrices of rows x cols with row
-// pitch ld (elements); box = box_inner x box_rows x 1, 128-byte swizzle,
-// out-of-range elements read as zero.
+// pitch ld (elements); box = box_inner x box_rows x 1. Loads use the 128-byte
+// swizzle (out-of-range elements read as zero); the epilogue's 32 x 32 store
+// boxes the 64-byte one (out-of-range elements are not written).
 int encode_3d(CUtensorMap* map, const void* base, int batch, int64_t rows, int64_t cols, int64_t ld,
-              uint32_t box_inner, uint32_t box_rows) {
+              uint32_t box_inner, uint32_t box_rows, CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
   auto enc = tensor_map_encoder();
   if (enc == nullptr) return -1;
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows),
@@ -474,7 +472,7 @@ int encode_3d(CUtensorMap* map, const void* base, int batch, int64_t rows, int64
   cuuint32_t box[3] = {box_inner, box_rows, 1};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? 0 : static_cast<int>(r);
 }
@@ -509,11 +507,11 @@ int max_resident_pairs(int num_sms) {
 }
 
 template <int KIND>
-cudaError_t launch_kind(const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p, int num_sms,
-                        cudaStream_t stream) {
+cudaError_t launch_kind(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& out, const GemmParams& p,
+                        int num_sms, cudaStream_t stream) {
   if (p.total_tiles == 0) return cudaSuccess;
   const int64_t pairs = std::min<int64_t>(p.total_tiles, max_resident_pairs<KIND>(num_sms));
-  ns_gemm_kernel<KIND><<<static_cast<unsigned>(2 * pairs), NUM_THREADS, SMEM_BYTES, stream>>>(a, b, p);
+  ns_gemm_kernel<KIND><<<static_cast<unsigned>(2 * pairs), NUM_THREADS, SMEM_BYTES, stream>>>(a, b, out, p);
   return cudaGetLastError();
 }
 
@@ -556,40 +554,40 @@ cudaError_t gemm_setup_attributes() {
 int encode_x_maps(NsMaps* maps, const void* X, int batch, int64_t r, int64_t c, int64_t ldc) {
   int e;
   if ((e = encode_3d(&maps->x_rows128, X, batch, r, c, ldc, BK, BM)) != 0) return e;
-  return encode_3d(&maps->x_k64, X, batch, r, c, ldc, 64, BK);
+  if ((e = encode_3d(&maps->x_k64, X, batch, r, c, ldc, 64, BK)) != 0) return e;
+  return encode_3d(&maps->store, X, batch, r, c, ldc, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
 int encode_sym_maps(SymMaps* maps, const void* A, int batch, int64_t r, int64_t ldr) {
-  return encode_3d(&maps->rows128, A, batch, r, r, ldr, BK, BM);
+  int e;
+  if ((e = encode_3d(&maps->rows128, A, batch, r, r, ldr, BK, BM)) != 0) return e;
+  return encode_3d(&maps->store, A, batch, r, r, ldr, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
-cudaError_t launch_gram(const NsMaps& xin, uint16_t* A, const GemmLaunch& g, cudaStream_t stream) {
+cudaError_t launch_gram(const NsMaps& xin, const SymMaps& aout, int out_z0, const GemmLaunch& g,
+                        cudaStream_t stream) {
   GemmParams p = base_params(g);
   set_symmetric_tiles(p, g.batch, g.r);
   p.K = static_cast<int>(g.c);
-  p.out = A;
-  p.ld_out = g.ldr;
-  p.stride_out = g.r * g.ldr;
+  p.out_z0 = out_z0;
   p.aux = nullptr;
-  return launch_kind<GEMM_GRAM>(xin.x_rows128, xin.x_rows128, p, g.num_sms, stream);
+  return launch_kind<GEMM_GRAM>(xin.x_rows128, xin.x_rows128, aout.store, p, g.num_sms, stream);
 }
 
-cudaError_t launch_poly(const SymMaps& a, const uint16_t* A, uint16_t* B, const GemmLaunch& g,
+cudaError_t launch_poly(const SymMaps& a, const uint16_t* A, const SymMaps& bout, const GemmLaunch& g,
                         cudaStream_t stream) {
   GemmParams p = base_params(g);
   set_symmetric_tiles(p, g.batch, g.r);
   p.K = static_cast<int>(g.r);
-  p.out = B;
-  p.ld_out = g.ldr;
-  p.stride_out = g.r * g.ldr;
+  p.out_z0 = 0;
   p.aux = A;
   p.ld_aux = g.ldr;
   p.stride_aux = g.r * g.ldr;
   p.scale = nullptr;
-  return launch_kind<GEMM_POLY>(a.rows128, a.rows128, p, g.num_sms, stream);
+  return launch_kind<GEMM_POLY>(a.rows128, a.rows128, bout.store, p, g.num_sms, stream);
 }
 
-cudaError_t launch_combine(const SymMaps& b, const NsMaps& xin, uint16_t* Xout, const GemmLaunch& g,
+cudaError_t launch_combine(const SymMaps& b, const NsMaps& xin, const NsMaps& xout, const GemmLaunch& g,
                            cudaStream_t stream) {
   GemmParams p = base_params(g);
   p.M = static_cast<int>(g.r);
@@ -600,11 +598,9 @@ cudaError_t launch_combine(const SymMaps& b, const NsMaps& xin, uint16_t* Xout, 
   const int tiles_n = static_cast<int>((g.c + BN - 1) / BN);
   p.tiles_per_mat = p.tiles_m * tiles_n;
   p.total_tiles = static_cast<int64_t>(p.tiles_per_mat) * g.batch;
-  p.out = Xout;
-  p.ld_out = g.ldc;
-  p.stride_out = g.r * g.ldc;
+  p.out_z0 = 0;
   p.aux = nullptr;
-  return launch_kind<GEMM_COMBINE>(b.rows128, xin.x_k64, p, g.num_sms, stream);
+  return launch_kind<GEMM_COMBINE>(b.rows128, xin.x_k64, xout.store, p, g.num_sms, stream);
 }
 
 }  // namespace prm

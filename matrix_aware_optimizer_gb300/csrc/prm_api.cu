@@ -69,7 +69,8 @@ struct NsRClass {
   int count = 0;
   size_t off_a = 0, off_b = 0;
   const void* maps_base = nullptr;
-  SymMaps ma{};
+  SymMaps ma{};  // the r-class A array (GRAM output, POLY operand)
+  SymMaps mb{};  // the r-class B array (POLY output)
 };
 
 // Every group's buffers are live at once: the five NS5 rounds of all groups
@@ -386,8 +387,9 @@ int bind_maps(prm_ctx* c, NsPlan& plan, void* base) {
   char* b = static_cast<char*>(base);
   for (auto& rc : plan.rclasses) {
     if (rc.maps_base == base) continue;
-    if (int e = encode_sym_maps(&rc.ma, b + rc.off_a, rc.count, rc.r, rc.ldr))
-      return fail(c, PRM_ERR_CUDA, "cuTensorMapEncodeTiled failed (code " + std::to_string(e) + ")");
+    int e = encode_sym_maps(&rc.ma, b + rc.off_a, rc.count, rc.r, rc.ldr);
+    if (e == 0) e = encode_sym_maps(&rc.mb, b + rc.off_b, rc.count, rc.r, rc.ldr);
+    if (e != 0) return fail(c, PRM_ERR_CUDA, "cuTensorMapEncodeTiled failed (code " + std::to_string(e) + ")");
     rc.maps_base = base;
   }
   for (auto& g : plan.groups) {
@@ -456,9 +458,8 @@ int run_ns(prm_ctx* c, NsPlan& plan, void* base, bool update_momentum, float bet
       GemmLaunch gl = group_launch(g);
       gl.scale = it == 0 ? reinterpret_cast<float*>(b + g.off_scale) : nullptr;
       const NsRClass& rcl = plan.rclasses[g.rclass];
-      uint16_t* A = reinterpret_cast<uint16_t*>(b + rcl.off_a) + g.base_slot * g.r * g.ldr;
       const size_t ev = c->prof.begin(stream);
-      if ((e = launch_gram(odd ? g.mx1 : g.mx0, A, gl, stream)) != cudaSuccess)
+      if ((e = launch_gram(odd ? g.mx1 : g.mx0, rcl.ma, g.base_slot, gl, stream)) != cudaSuccess)
         return cuda_fail(c, e, "gram launch");
       c->prof.end(ev, PRM_FAMILY_NS_GRAM, 1, 2.0 * g.count * double(g.r) * g.r * g.c, stream);
     }
@@ -474,18 +475,16 @@ int run_ns(prm_ctx* c, NsPlan& plan, void* base, bool update_momentum, float bet
       gl.cc = coeffs[2];
       gl.err = c->d_err;
       gl.num_sms = c->num_sms;
-      uint16_t* A = reinterpret_cast<uint16_t*>(b + rcl.off_a);
-      uint16_t* B = reinterpret_cast<uint16_t*>(b + rcl.off_b);
+      const uint16_t* A = reinterpret_cast<const uint16_t*>(b + rcl.off_a);
       const size_t ev = c->prof.begin(stream);
-      if ((e = launch_poly(rcl.ma, A, B, gl, stream)) != cudaSuccess) return cuda_fail(c, e, "poly launch");
+      if ((e = launch_poly(rcl.ma, A, rcl.mb, gl, stream)) != cudaSuccess) return cuda_fail(c, e, "poly launch");
       c->prof.end(ev, PRM_FAMILY_NS_POLY, 1, 2.0 * rcl.count * double(rcl.r) * rcl.r * rcl.r, stream);
     }
     for (auto& g : plan.groups) {
       GemmLaunch gl = group_launch(g);
       gl.scale = it == 0 ? reinterpret_cast<float*>(b + g.off_scale) : nullptr;
-      uint16_t* nxt = reinterpret_cast<uint16_t*>(b + (odd ? g.off_x0 : g.off_x1));
       const size_t ev = c->prof.begin(stream);
-      if ((e = launch_combine(g.mb, odd ? g.mx1 : g.mx0, nxt, gl, stream)) != cudaSuccess)
+      if ((e = launch_combine(g.mb, odd ? g.mx1 : g.mx0, odd ? g.mx0 : g.mx1, gl, stream)) != cudaSuccess)
         return cuda_fail(c, e, "combine launch");
       c->prof.end(ev, PRM_FAMILY_NS_COMBINE, 1, 2.0 * g.count * double(g.r) * g.r * g.c, stream);
     }
@@ -947,7 +946,9 @@ int prm_ns_gram(const uint16_t* X, uint16_t* A, const float* scale, int batch, i
   int rc = device_state(&ds);
   if (rc != PRM_OK) return rc;
   NsMaps mx;
-  if (encode_x_maps(&mx, X, batch, r, c, ldc) != 0) return PRM_ERR_CUDA;
+  SymMaps ma;
+  if (encode_x_maps(&mx, X, batch, r, c, ldc) != 0 || encode_sym_maps(&ma, A, batch, r, ldr) != 0)
+    return PRM_ERR_CUDA;
   GemmLaunch g{};
   g.batch = batch;
   g.r = r;
@@ -957,7 +958,7 @@ int prm_ns_gram(const uint16_t* X, uint16_t* A, const float* scale, int batch, i
   g.scale = scale;
   g.err = ds->d_err;
   g.num_sms = ds->num_sms;
-  return launch_gram(mx, A, g, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PRM_OK : PRM_ERR_CUDA;
+  return launch_gram(mx, ma, 0, g, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PRM_OK : PRM_ERR_CUDA;
 }
 
 int prm_ns_poly(const uint16_t* A, uint16_t* B, float a, float b, float cc, int batch, int64_t r, int64_t ldr,
@@ -968,8 +969,9 @@ int prm_ns_poly(const uint16_t* A, uint16_t* B, float a, float b, float cc, int 
   DeviceState* ds;
   int rc = device_state(&ds);
   if (rc != PRM_OK) return rc;
-  SymMaps ma;
-  if (encode_sym_maps(&ma, A, batch, r, ldr) != 0) return PRM_ERR_CUDA;
+  SymMaps ma, mb;
+  if (encode_sym_maps(&ma, A, batch, r, ldr) != 0 || encode_sym_maps(&mb, B, batch, r, ldr) != 0)
+    return PRM_ERR_CUDA;
   GemmLaunch g{};
   g.batch = batch;
   g.r = r;
@@ -981,7 +983,7 @@ int prm_ns_poly(const uint16_t* A, uint16_t* B, float a, float b, float cc, int 
   g.cc = cc;
   g.err = ds->d_err;
   g.num_sms = ds->num_sms;
-  return launch_poly(ma, A, B, g, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PRM_OK : PRM_ERR_CUDA;
+  return launch_poly(ma, A, mb, g, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PRM_OK : PRM_ERR_CUDA;
 }
 
 int prm_ns_combine(const uint16_t* X, const uint16_t* B, uint16_t* Xout, const float* scale, int batch, int64_t r,
@@ -994,9 +996,10 @@ int prm_ns_combine(const uint16_t* X, const uint16_t* B, uint16_t* Xout, const f
   DeviceState* ds;
   int rc = device_state(&ds);
   if (rc != PRM_OK) return rc;
-  NsMaps mx;
+  NsMaps mx, mo;
   SymMaps mb;
-  if (encode_x_maps(&mx, X, batch, r, c, ldc) != 0 || encode_sym_maps(&mb, B, batch, r, ldr) != 0)
+  if (encode_x_maps(&mx, X, batch, r, c, ldc) != 0 || encode_sym_maps(&mb, B, batch, r, ldr) != 0 ||
+      encode_x_maps(&mo, Xout, batch, r, c, ldc) != 0)
     return PRM_ERR_CUDA;
   GemmLaunch g{};
   g.batch = batch;
@@ -1007,7 +1010,7 @@ int prm_ns_combine(const uint16_t* X, const uint16_t* B, uint16_t* Xout, const f
   g.scale = scale;
   g.err = ds->d_err;
   g.num_sms = ds->num_sms;
-  return launch_combine(mb, mx, Xout, g, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PRM_OK : PRM_ERR_CUDA;
+  return launch_combine(mb, mx, mo, g, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PRM_OK : PRM_ERR_CUDA;
 }
 
 static void standalone_group(int batch, int64_t m, int64_t n, NsPlan& plan) {
