@@ -8,8 +8,8 @@ the hot path: momentum, branch choice, RowNorm, NS5 prep / rounds / output,
 parameter update). The headline value is milliseconds per cycle (lower is
 better) with all state resident in HBM; `e2e` repeats the measurement through
 the public API with the gradients copied in from pinned host memory every
-optimizer step (double-buffered: the next step's upload overlaps the current
-step) and a small result read back. Inputs (22 GB per optimizer
+optimizer step (rotating gradient buffers: the uploads of the next steps
+overlap the current one) and a small result read back. Inputs (22 GB per optimizer
 step on the 1.3B set) are far larger than L2, so no flush is needed.
 
   python bench.py [--steps K] [--warmup W] [--workload dit_1p3b|dit_15b|dit_1p3b_muonbp]
@@ -524,32 +524,61 @@ def run_ours(args):
     if not args.no_e2e:
         hflat = gflat.cpu().pin_memory()
         h2d = sum(g.numel() * g.element_size() for g in grads)
-        # Two gradient buffers and two optimizer instances over the same
-        # params / momenta, sharing one workspace (their steps are ordered on
-        # one stream): step s reads buffer s % 2 while the gradients of step
-        # s + 1 stream into the other one. Each upload runs as four concurrent
-        # pieces on four copy streams and waits for the step that last read
-        # its buffer (s - 1); each step waits for its own upload.
-        gflat2 = torch.empty_like(gflat)
-        grads2 = [gflat2[offs[i]:offs[i] + s[0] * s[1]].view(s) for i, s in enumerate(ms.shapes)]
-        opt2 = PeriodicRowMuon(Ws, Ms, grads2, muonbp_blocks=blocks, workspace=opt.workspace,
-                               workspace_limit=int(args.workspace_limit_gb * 2 ** 30))
-        bufs = [(gflat, opt), (gflat2, opt2)]
-        copy_streams = [torch.cuda.Stream(device=dev) for _ in range(4)]
-        bounds = [total * q // 4 // 128 * 128 for q in range(4)] + [total]
+        gbytes = gflat.numel() * gflat.element_size()
+        # NBUF gradient buffers, one optimizer instance per buffer over the same
+        # params / momenta, all sharing one workspace (their steps are ordered
+        # on one stream): step s reads buffer s % NBUF while the gradients of
+        # the next steps stream into the others. Each upload runs as pieces on
+        # several copy streams and waits for the step that last read its
+        # buffer (s - NBUF); each step waits for its own upload, and its one-row
+        # read-back runs on a stream of its own.
+        free_b, _ = torch.cuda.mem_get_info(dev)
+        nbuf = max(2, min(4, 1 + int((free_b - (4 << 30)) // max(gbytes, 1))))
+        extra = [torch.empty_like(gflat) for _ in range(nbuf - 1)]
+        opts = [opt]
+        for buf in extra:
+            gl = [buf[offs[i]:offs[i] + s[0] * s[1]].view(s) for i, s in enumerate(ms.shapes)]
+            opts.append(PeriodicRowMuon(Ws, Ms, gl, muonbp_blocks=blocks, workspace=opt.workspace,
+                                        workspace_limit=int(args.workspace_limit_gb * 2 ** 30)))
+        bufs = list(zip([gflat] + extra, opts))
         out_row = torch.empty(ms.shapes[0][1], dtype=torch.float32).pin_memory()
         d2h = out_row.numel() * 4
+        d2h_stream = torch.cuda.Stream(device=dev)  # the read-back never holds up the next step
 
-        def run(first_t, nsteps):
+        def upload_alone(nstreams):
+            css = [torch.cuda.Stream(device=dev) for _ in range(nstreams)]
+            bnd = [total * q // nstreams // 128 * 128 for q in range(nstreams)] + [total]
+            best = None
+            for _ in range(3):
+                u0, u1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                u0.record(stream)
+                for q, cs in enumerate(css):
+                    cs.wait_stream(stream)
+                    with torch.cuda.stream(cs):
+                        gflat[bnd[q]:bnd[q + 1]].copy_(hflat[bnd[q]:bnd[q + 1]], non_blocking=True)
+                    stream.wait_stream(cs)
+                u1.record(stream)
+                torch.cuda.synchronize()
+                t_ = u0.elapsed_time(u1)
+                best = t_ if best is None else min(best, t_)
+            return best
+
+        # the host link rate behind the number, and the copy-stream count used
+        up_ms = {n: upload_alone(n) for n in (4, 8)}
+        ncopy = min(up_ms, key=up_ms.get)
+        copy_streams = [torch.cuda.Stream(device=dev) for _ in range(ncopy)]
+        bounds = [total * q // ncopy // 128 * 128 for q in range(ncopy)] + [total]
+
+        def run(first_t, nsteps, per=None):
             step_done = {}
             uploaded = {}
 
             def upload(s):
-                dst = bufs[s % 2][0]
+                dst = bufs[s % nbuf][0]
                 ev = []
                 for q, cs in enumerate(copy_streams):
-                    if s - 2 in step_done:
-                        cs.wait_event(step_done[s - 2])
+                    if s - nbuf in step_done:
+                        cs.wait_event(step_done[s - nbuf])
                     with torch.cuda.stream(cs):
                         dst[bounds[q]:bounds[q + 1]].copy_(hflat[bounds[q]:bounds[q + 1]], non_blocking=True)
                     e = torch.cuda.Event()
@@ -557,49 +586,56 @@ def run_ours(args):
                     ev.append(e)
                 uploaded[s] = ev
 
-            upload(0)
+            for s in range(min(nbuf - 1, nsteps)):
+                upload(s)
             for s in range(nsteps):
-                if s + 1 < nsteps:
-                    upload(s + 1)
+                if s + nbuf - 1 < nsteps:
+                    upload(s + nbuf - 1)
                 for e in uploaded.pop(s):
                     stream.wait_event(e)
-                bufs[s % 2][1].step(first_t + s, mode=mode, **hp)
+                if per is not None:
+                    per[s][0].record(stream)
+                bufs[s % nbuf][1].step(first_t + s, mode=mode, **hp)
+                if per is not None:
+                    per[s][1].record(stream)
                 done = torch.cuda.Event()
                 done.record(stream)
                 step_done[s] = done
-                out_row.copy_(Ws[0][0], non_blocking=True)
+                d2h_stream.wait_event(done)
+                with torch.cuda.stream(d2h_stream):
+                    out_row.copy_(Ws[0][0], non_blocking=True)
+            stream.wait_stream(d2h_stream)
 
         run(0, 2 * ms.K)  # warm-up (t = 0 starts a cycle)
         torch.cuda.synchronize()
         if world > 1:
             dist.barrier()
+        nst = args.steps * ms.K
+        per = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(nst)]
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        run((args.warmup + args.steps) * ms.K, args.steps * ms.K)
+        run((args.warmup + args.steps) * ms.K, nst, per)
         e1.record(stream)
         torch.cuda.synchronize()
         e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, dev)
-        # the uploads alone, for the link rate behind the number
-        u0, u1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        u0.record(stream)
-        for q, cs in enumerate(copy_streams):
-            cs.wait_stream(stream)
-            with torch.cuda.stream(cs):
-                gflat[bounds[q]:bounds[q + 1]].copy_(hflat[bounds[q]:bounds[q + 1]], non_blocking=True)
-            stream.wait_stream(cs)
-        u1.record(stream)
-        torch.cuda.synchronize()
-        up_ms = u0.elapsed_time(u1)
+        # where the time went: the steps themselves, and the waits between them
+        # (a step waiting for its gradients)
+        busy = sum(a.elapsed_time(b) for a, b in per) / args.steps
+        waits = [per[s][1].elapsed_time(per[s + 1][0]) for s in range(nst - 1)]
         e2e = {"value": round(e2e_ms, 3), "unit": UNIT, "h2d_bytes_per_step": h2d * ms.K,
                "d2h_bytes_per_step": d2h * ms.K,
-               "h2d_gbs_alone": round(h2d / up_ms / 1e6, 1),
-               "note": "per step: that step's gradients copied from pinned host memory (four copy streams), "
-                       "the step, one parameter row read back; double-buffered gradients, so the upload "
-                       "of step s + 1 overlaps step s"}
-        opt.sync_status()
-        opt2.sync_status()
-        opt2.close()
-        del gflat2, grads2
+               "h2d_gbs_alone": round(h2d / up_ms[ncopy] / 1e6, 1), "copy_streams": ncopy,
+               "gradient_buffers": nbuf, "steps_ms_per_cycle": round(busy, 3),
+               "waits_ms_per_cycle": round(sum(waits) / args.steps, 3),
+               "longest_wait_ms": round(max(waits) if waits else 0.0, 3),
+               "note": "per optimizer step: that step's gradients copied from pinned host memory (copy streams in "
+                       "parallel), the step, one parameter row read back; the gradient buffers rotate so that "
+                       "the uploads of the next steps overlap the current one"}
+        for o in opts:
+            o.sync_status()
+        for o in opts[1:]:
+            o.close()
+        del extra, opts, bufs
 
     adam = None
     if not args.no_adamw:

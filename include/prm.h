@@ -57,6 +57,7 @@ extern "C" {
 /* ---- enums ------------------------------------------------------------ */
 #define PRM_FP32 0   /* gradient element type: float32 */
 #define PRM_BF16 1   /* gradient element type: bfloat16 */
+#define PRM_FP16 2   /* float16: the Gram-stage output of the standalone NS5 stages */
 
 #define PRM_MODE_PRMUON 0   /* [SMDiT] Fig. 3: NS5 when t % K == 0, else gamma * R_eps */
 #define PRM_MODE_MUONBP 1   /* [MuonBP]: full NS5 when t % K == 0, else NS5 per block */
@@ -142,7 +143,8 @@ PRM_API int prm_set_workspace(prm_ctx* ctx, void* dev_ptr, size_t bytes);
  *   W <- W * (1 - lr * wd) - eta * s * D           (decoupled weight decay)
  * NS5: X = M / (||M||_F + 1e-7) (transposed if tall), then five rounds of
  * A = X X^T, B = b A + c A A, X <- a X + B X, in bf16 operands with fp32
- * accumulation (evaluated as X <- (a I + B) X, one bf16 product per round). ns_coeffs (host, 3 floats: a, b, c) may be NULL for the
+ * accumulation (evaluated as X <- P X with P = a I + B formed as a completed
+ * square, see the standalone stages below). ns_coeffs (host, 3 floats: a, b, c) may be NULL for the
  * default quintic (3.4445, -4.7750, 2.0315) -- the pages print no
  * coefficients, so this default is a stated choice.
  * Preconditions: t >= 0, K >= 1 (K = 1 is vanilla Muon), 0 <= beta < 1,
@@ -268,16 +270,28 @@ PRM_API const char* prm_last_error(const prm_ctx* ctx);
  * uint16_t bit patterns. `scale` (device, batch floats) may be NULL for 1.
  * [SMDiT] section "Periodic Row-wise Muon": one NS5 round is
  * A = X X^T, B = b A + c A A, X' = a X + B X. The library evaluates it as
- * A = X X^T, P = a I + b A + c A A, X' = P X (the same product, with the
- * a X term carried on P's diagonal), so the three calls below are GRAM,
- * POLY and COMBINE of that form. */
+ * X' = P X with P = a I + b A + c A A written as a completed square: for
+ * c != 0, C = sqrt|c| A + sgn(c) b / (2 sqrt|c|) I and
+ * P = sgn(c) C C + (a - b^2 / (4c)) I (exact: C is a polynomial in A); for
+ * c = 0, P = b A + a I comes straight from the Gram stage. The three calls
+ * below are those stages:
+ *   prm_ns_gram(gain = sqrt|c|, diag = sgn(c) b / (2 sqrt|c|), PRM_FP16) -> C
+ *   prm_ns_poly(gain = sgn(c), diag = a - b^2 / (4c), PRM_FP16)          -> P
+ *   prm_ns_combine                                                       -> X'
+ * (for c = 0: prm_ns_gram(gain = b, diag = a, PRM_BF16) -> P, then
+ * prm_ns_combine). C is kept in fp16: its diagonal holds the shift
+ * b / (2 sqrt|c|), next to which bf16 would lose most of sqrt|c| A_ii. */
 
-/* A[i] = scale[i]^2 * X[i] X[i]^T  (symmetric; tensor cores, tcgen05). */
-PRM_API int prm_ns_gram(const uint16_t* X, uint16_t* A, const float* scale, int batch, int64_t r,
-                int64_t c, int64_t ldc, int64_t ldr, void* stream);
+/* C[i] = gain * scale[i]^2 * X[i] X[i]^T + diag * I  (symmetric; tensor
+ * cores, tcgen05), written as out_dtype (PRM_BF16 or PRM_FP16). Errors:
+ * INVALID_ARG (also non-finite gain / diag, other out_dtype), ALIGNMENT,
+ * CUDA, UNSUPPORTED. */
+PRM_API int prm_ns_gram(const uint16_t* X, uint16_t* C, const float* scale, float gain, float diag,
+                int out_dtype, int batch, int64_t r, int64_t c, int64_t ldc, int64_t ldr, void* stream);
 
-/* P[i] = a * I + b * A[i] + c * A[i] A[i]   (A symmetric; P out, bf16). */
-PRM_API int prm_ns_poly(const uint16_t* A, uint16_t* P, float a, float b, float c, int batch,
+/* P[i] = gain * C[i] C[i] + diag * I   (C symmetric, of type in_dtype:
+ * PRM_BF16 or PRM_FP16; P bf16, must not alias C). */
+PRM_API int prm_ns_poly(const uint16_t* C, uint16_t* P, float gain, float diag, int in_dtype, int batch,
                 int64_t r, int64_t ldr, void* stream);
 
 /* Xout[i] = scale[i] * P[i] X[i]  (Xout must not alias X). */

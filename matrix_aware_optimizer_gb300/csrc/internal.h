@@ -90,17 +90,19 @@ struct GemmLaunch {
   int batch;
   int64_t r, c, ldc, ldr;
   const float* scale;     // per-matrix scale or nullptr
-  float ca, cb, cc;       // NS coefficients a, b, c
+  float gain, diag;       // GRAM / POLY epilogue: gain * acc + diag on the diagonal
+  bool in_fp16;           // operands fp16 (POLY reading C) instead of bf16
+  bool out_fp16;          // output packed as fp16 (GRAM writing C) instead of bf16
   int* err;               // device error word
   int num_sms;
 };
 
-// Output maps: GRAM writes matrices [out_z0, out_z0 + batch) of `aout`
-// (the r-class array of A), POLY the r-class array of B, COMBINE `xout`.
-cudaError_t launch_gram(const NsMaps& xin, const SymMaps& aout, int out_z0, const GemmLaunch& g,
+// GRAM: C = gain * scale^2 * X X^T + diag * I into matrices
+// [out_z0, out_z0 + batch) of `cout` (an r-class array); POLY: P = gain * C C
+// + diag * I over the r-class; COMBINE: Xout = scale * P X.
+cudaError_t launch_gram(const NsMaps& xin, const SymMaps& cout, int out_z0, const GemmLaunch& g,
                         cudaStream_t stream);
-cudaError_t launch_poly(const SymMaps& a, const uint16_t* A, const SymMaps& bout, const GemmLaunch& g,
-                        cudaStream_t stream);
+cudaError_t launch_poly(const SymMaps& c, const SymMaps& pout, const GemmLaunch& g, cudaStream_t stream);
 cudaError_t launch_combine(const SymMaps& b, const NsMaps& xin, const NsMaps& xout, const GemmLaunch& g,
                            cudaStream_t stream);
 

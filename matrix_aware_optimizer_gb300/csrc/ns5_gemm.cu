@@ -3,16 +3,24 @@
 // Transformers", PaperDaily walkthrough, section "Periodic Row-wise Muon":
 // NS5 is five rounds of matrix products and scalings):
 //
-//   GRAM    : A  = s^2 * X X^T          (r x r, symmetric; upper super-blocks
-//                                         computed, lower ones mirrored)
-//   POLY    : P  = a I + b A + c A A     (A symmetric, so A A = A A^T; same
-//                                         triangle scheme, polynomial fused
-//                                         into the epilogue)
-//   COMBINE : X' = s * P X               (r x c; scaling in the epilogue)
+//   GRAM    : C  = gain * s^2 * X X^T + diag * I   (r x r, symmetric; upper
+//                                         super-blocks computed, lower ones mirrored)
+//   POLY    : P  = gain * C C + diag * I          (C symmetric, so C C = C C^T;
+//                                         same triangle scheme)
+//   COMBINE : X' = s * P X                         (r x c; scaling in the epilogue)
 //
-// The round X' = a X + (b A + c A A) X is evaluated as (a I + b A + c A A) X:
-// the a X term rides along the diagonal of P instead of being re-read from
-// memory by the COMBINE epilogue.
+// One round X' = a X + (b A + c A A) X, A = X X^T, is evaluated as P X with
+// P = a I + b A + c A A written as a completed square: for c != 0, with
+// C = sqrt|c| A + sgn(c) b / (2 sqrt|c|) I, P = sgn(c) C C + (a - b^2 / (4c)) I
+// (C is a polynomial in A, so it commutes with A and the identity is exact).
+// GRAM therefore writes C (gain sqrt|c|, diag sgn(c) b / (2 sqrt|c|)) and
+// POLY squares it (gain sgn(c), diag a - b^2 / (4c)): no epilogue re-reads an
+// operand from memory. C is stored in fp16, not bf16: its diagonal carries
+// the shift b / (2 sqrt|c|) (-1.68 for the default quintic), next to which
+// bf16's 8-bit significand would drop most of sqrt|c| A_ii, while fp16's
+// 11 bits keep it (in emulation the fp16 form is as accurate as evaluating
+// a X + B X with bf16 A, the bf16 one about 30 % less accurate). For c = 0,
+// GRAM writes P = b A + a I directly (bf16) and POLY is skipped.
 //
 // Each launch covers every matrix of a same-shape batch: the tile queue runs
 // over (matrix, tile) pairs, so small r x r products still fill the GPU.
@@ -32,13 +40,13 @@
 //   warp 1     : TMEM allocation for the pair (512 columns: two 128x256 fp32
 //                accumulators); in the even CTA one lane issues the MMAs
 //   warps 2..5 : epilogue -- tcgen05.ld of this CTA's 128 accumulator rows
-//                (one TMEM lane = one output row per thread), fused scaling /
-//                polynomial (POLY reads A for its b A term from global
-//                memory), bf16 results staged per 32 x 32 box in shared
-//                memory and written by TMA stores (plus the transposed box
-//                for the mirrored half of symmetric outputs)
+//                (one TMEM lane = one output row per thread), fused scaling
+//                and diagonal shift, bf16 results staged per 32 x 32 box in
+//                shared memory and written by TMA stores (plus the
+//                transposed box for the mirrored half of symmetric outputs)
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
@@ -92,10 +100,10 @@ struct GemmParams {
   int tiles_per_mat;
   int64_t total_tiles;
   int out_z0;           // first matrix of the output map this launch writes
-  const uint16_t* aux;  // POLY: A (for b A); unused otherwise
-  int64_t ld_aux, stride_aux;
-  const float* scale;
-  float ca, cb, cc;
+  const float* scale;   // per-matrix s (GRAM: s^2 applied; COMBINE: s), or nullptr
+  float gain, diag;     // GRAM / POLY: out = gain * (scale^2) * acc + diag * [i == j]
+  int in_fp16;          // operands are fp16 (POLY reading C); else bf16
+  int out_fp16;         // output is packed as fp16 (GRAM writing C); else bf16
   int* err;
   uint64_t timeout_ns;
 };
@@ -137,49 +145,17 @@ __device__ __forceinline__ TileCoord tile_coord(const GemmParams& p, int64_t til
   return t;
 }
 
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  const __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<const uint32_t*>(&h);
 }
 
 constexpr int EPI_CHUNKS = BN / 32;  // 32-column chunks per output row of a tile
-
-// The POLY epilogue's second operand (A) for this thread's output row: 8 chunks of 32 bf16 as packed words (element 2h of a
-// chunk in the low half of word h), zero outside the matrix. Issued before
-// the wait for the accumulator, so its latency hides behind the mainloop.
-template <int KIND>
-__device__ __forceinline__ void prefetch_aux(const GemmParams& p, const TileCoord& tc, int i,
-                                             uint32_t (&xr)[EPI_CHUNKS][16]) {
-  const bool row_ok = i < p.M;
-  const uint16_t* src = p.aux + static_cast<int64_t>(tc.mat) * p.stride_aux + static_cast<int64_t>(i) * p.ld_aux;
-#pragma unroll
-  for (int q = 0; q < EPI_CHUNKS; ++q) {
-    const int j0 = tc.n0 + q * 32;
-    if (row_ok && j0 + 32 <= p.N) {
-      const uint4* s4 = reinterpret_cast<const uint4*>(src + j0);
-#pragma unroll
-      for (int v = 0; v < 4; ++v) {
-        const uint4 u = s4[v];
-        xr[q][4 * v + 0] = u.x;
-        xr[q][4 * v + 1] = u.y;
-        xr[q][4 * v + 2] = u.z;
-        xr[q][4 * v + 3] = u.w;
-      }
-    } else {
-#pragma unroll
-      for (int h = 0; h < 16; ++h) {
-        const int j = j0 + 2 * h;
-        const uint32_t lo = (row_ok && j < p.N) ? src[j] : 0u;
-        const uint32_t hi = (row_ok && j + 1 < p.N) ? src[j + 1] : 0u;
-        xr[q][h] = lo | (hi << 16);
-      }
-    }
-  }
-}
-
-__device__ __forceinline__ float word_elem(const uint32_t (&w)[16], int k) {
-  return (k & 1) ? __uint_as_float(w[k >> 1] & 0xFFFF0000u) : __uint_as_float(w[k >> 1] << 16);
-}
 
 __device__ __forceinline__ uint32_t stage_off(int row, int chunk) {
   return static_cast<uint32_t>(row * STAGE_ROW_BYTES + ((chunk ^ ((row >> 1) & 3)) << 4));
@@ -191,8 +167,7 @@ __device__ __forceinline__ uint32_t stage_off(int row, int chunk) {
 // rewritten.
 template <int KIND>
 __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const CUtensorMap* tm_out, const TileCoord& tc,
-                                              int i, uint32_t t_row, const uint32_t (&xr)[EPI_CHUNKS][16],
-                                              uint8_t* stage, int lane, uint32_t& nchunk) {
+                                              int i, uint32_t t_row, uint8_t* stage, int lane, uint32_t& nchunk) {
   const int i0 = i - lane;  // first output row of this warp
   float s = 1.f;
   if (KIND == GEMM_GRAM && p.scale != nullptr) {
@@ -200,6 +175,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const CUtenso
     s = q * q;
   }
   if (KIND == GEMM_COMBINE && p.scale != nullptr) s = p.scale[tc.mat];
+  if (KIND != GEMM_COMBINE) s *= p.gain;
   const int z = p.out_z0 + tc.mat;
   const bool rows_in = i0 < p.M;  // warp-uniform
 
@@ -209,21 +185,17 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const CUtenso
     if (j0 < p.N) {  // uniform over the warp: depends on the tile only
       float v[32];
       tmem_load_32cols(t_row + static_cast<uint32_t>(q * 32), v);
-      if (KIND == GEMM_POLY) {
 #pragma unroll
-        for (int k = 0; k < 32; ++k) v[k] = p.cb * word_elem(xr[q], k) + p.cc * v[k];
-        if (j0 == i0) {  // this chunk holds the warp's 32 diagonal elements (warp-uniform)
+      for (int k = 0; k < 32; ++k) v[k] *= s;
+      if (KIND != GEMM_COMBINE && j0 == i0) {  // the warp's 32 diagonal elements (warp-uniform)
 #pragma unroll
-          for (int k = 0; k < 32; ++k)
-            if (k == lane) v[k] += p.ca;
-        }
-      } else {
-#pragma unroll
-        for (int k = 0; k < 32; ++k) v[k] *= s;
+        for (int k = 0; k < 32; ++k)
+          if (k == lane) v[k] += p.diag;
       }
       uint32_t w[16];
 #pragma unroll
-      for (int h = 0; h < 16; ++h) w[h] = pack_bf16x2(v[2 * h], v[2 * h + 1]);
+      for (int h = 0; h < 16; ++h)
+        w[h] = p.out_fp16 ? pack_f16x2(v[2 * h], v[2 * h + 1]) : pack_bf16x2(v[2 * h], v[2 * h + 1]);
       const bool mirror = KIND != GEMM_COMBINE && tc.mirror;
       uint8_t* bd = stage + (nchunk & 1u) * EPI_BUF_BYTES;
       uint8_t* bm = stage + (2u + (nchunk & 1u)) * EPI_BUF_BYTES;
@@ -355,7 +327,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     }
   } else if (warp == 1) {
     if (lane == 0 && rank == 0) {
-      constexpr uint32_t idesc = idesc_bf16_f32(PAIR_M, BN, false, KIND == GEMM_COMBINE);
+      const uint32_t idesc = idesc_f16kind_f32(PAIR_M, BN, false, KIND == GEMM_COMBINE, p.in_fp16 != 0);
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
@@ -415,13 +387,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     for (int64_t tile = pair_id; tile < p.total_tiles; tile += num_pairs) {
       const TileCoord tc = tile_coord<KIND>(p, tile);
       const int i = tc.m0 + static_cast<int>(rank) * BM + quarter * 32 + lane;
-      uint32_t xr[EPI_CHUNKS][16];
-      if constexpr (KIND == GEMM_POLY) prefetch_aux<KIND>(p, tc, i, xr);
       const bool got = wait_bounded(&tfull_bar[acc], acc_phase, abort_flag, p.err, p.timeout_ns);
       if (!__all_sync(0xffffffffu, got)) break;
       tc_fence_after_sync();
       const uint32_t t_row = tmem_base + static_cast<uint32_t>(acc * BN) + (static_cast<uint32_t>(quarter * 32) << 16);
-      epilogue_tile<KIND>(p, &tmOut, tc, i, t_row, xr, stage, lane, nchunk);
+      epilogue_tile<KIND>(p, &tmOut, tc, i, t_row, stage, lane, nchunk);
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive_remote(tempty_even + static_cast<uint32_t>(acc * sizeof(uint64_t)));
@@ -518,9 +488,10 @@ cudaError_t launch_kind(const CUtensorMap& a, const CUtensorMap& b, const CUtens
 GemmParams base_params(const GemmLaunch& g) {
   GemmParams p{};
   p.scale = g.scale;
-  p.ca = g.ca;
-  p.cb = g.cb;
-  p.cc = g.cc;
+  p.gain = g.gain;
+  p.diag = g.diag;
+  p.in_fp16 = g.in_fp16 ? 1 : 0;
+  p.out_fp16 = g.out_fp16 ? 1 : 0;
   p.err = g.err;
   p.timeout_ns = WAIT_LIMIT_NS;
   return p;
@@ -570,21 +541,16 @@ cudaError_t launch_gram(const NsMaps& xin, const SymMaps& aout, int out_z0, cons
   set_symmetric_tiles(p, g.batch, g.r);
   p.K = static_cast<int>(g.c);
   p.out_z0 = out_z0;
-  p.aux = nullptr;
   return launch_kind<GEMM_GRAM>(xin.x_rows128, xin.x_rows128, aout.store, p, g.num_sms, stream);
 }
 
-cudaError_t launch_poly(const SymMaps& a, const uint16_t* A, const SymMaps& bout, const GemmLaunch& g,
-                        cudaStream_t stream) {
+cudaError_t launch_poly(const SymMaps& c, const SymMaps& pout, const GemmLaunch& g, cudaStream_t stream) {
   GemmParams p = base_params(g);
   set_symmetric_tiles(p, g.batch, g.r);
   p.K = static_cast<int>(g.r);
   p.out_z0 = 0;
-  p.aux = A;
-  p.ld_aux = g.ldr;
-  p.stride_aux = g.r * g.ldr;
   p.scale = nullptr;
-  return launch_kind<GEMM_POLY>(a.rows128, a.rows128, bout.store, p, g.num_sms, stream);
+  return launch_kind<GEMM_POLY>(c.rows128, c.rows128, pout.store, p, g.num_sms, stream);
 }
 
 cudaError_t launch_combine(const SymMaps& b, const NsMaps& xin, const NsMaps& xout, const GemmLaunch& g,
@@ -599,7 +565,6 @@ cudaError_t launch_combine(const SymMaps& b, const NsMaps& xin, const NsMaps& xo
   p.tiles_per_mat = p.tiles_m * tiles_n;
   p.total_tiles = static_cast<int64_t>(p.tiles_per_mat) * g.batch;
   p.out_z0 = 0;
-  p.aux = nullptr;
   return launch_kind<GEMM_COMBINE>(b.rows128, xin.x_k64, xout.store, p, g.num_sms, stream);
 }
 

@@ -59,7 +59,8 @@ struct NsGroup {
   // tensor maps for the bound workspace
   const void* maps_base = nullptr;
   NsMaps mx0{}, mx1{};
-  SymMaps mb{};  // this group's slice of the r-class B array (COMBINE operand)
+  SymMaps mb{};  // this group's slice of the r-class B array (P; COMBINE operand)
+  SymMaps ma{};  // this group's slice of the r-class A array (P when POLY is skipped, c = 0)
 };
 
 // All matrices with the same short side r: their A = X X^T and
@@ -69,8 +70,8 @@ struct NsRClass {
   int count = 0;
   size_t off_a = 0, off_b = 0;
   const void* maps_base = nullptr;
-  SymMaps ma{};  // the r-class A array (GRAM output, POLY operand)
-  SymMaps mb{};  // the r-class B array (POLY output)
+  SymMaps ma{};  // the r-class A array (GRAM output C, POLY operand)
+  SymMaps mb{};  // the r-class B array (POLY output P)
 };
 
 // Every group's buffers are live at once: the five NS5 rounds of all groups
@@ -399,6 +400,7 @@ int bind_maps(prm_ctx* c, NsPlan& plan, void* base) {
     int e = encode_x_maps(&g.mx0, b + g.off_x0, g.count, g.r, g.c, g.ldc);
     if (e == 0) e = encode_x_maps(&g.mx1, b + g.off_x1, g.count, g.r, g.c, g.ldc);
     if (e == 0) e = encode_sym_maps(&g.mb, b + rc.off_b + slice, g.count, g.r, g.ldr);
+    if (e == 0) e = encode_sym_maps(&g.ma, b + rc.off_a + slice, g.count, g.r, g.ldr);
     if (e != 0) return fail(c, PRM_ERR_CUDA, "cuTensorMapEncodeTiled failed (code " + std::to_string(e) + ")");
     g.maps_base = base;
   }
@@ -437,6 +439,16 @@ int run_ns(prm_ctx* c, NsPlan& plan, void* base, bool update_momentum, float bet
       return cuda_fail(c, e, "norm launch");
     c->prof.end(ev, PRM_FAMILY_NS_PREP, static_cast<int>(g.sets.size()) + 1, prep_bytes, stream);
   }
+  // P = a I + b A + c A A as a completed square (see ns5_gemm.cu): GRAM
+  // writes C = sqrt|c| A + sgn(c) b / (2 sqrt|c|) I, POLY P = sgn(c) C C +
+  // (a - b^2 / (4c)) I; for c = 0 GRAM writes P = b A + a I and POLY is skipped.
+  const double ca = coeffs[0], cb = coeffs[1], cc = coeffs[2];
+  const bool square = cc != 0.0;
+  const double root = square ? std::sqrt(std::fabs(cc)) : 0.0, sg = cc > 0.0 ? 1.0 : -1.0;
+  const float gram_gain = static_cast<float>(square ? root : cb);
+  const float gram_diag = static_cast<float>(square ? sg * cb / (2.0 * root) : ca);
+  const float poly_gain = static_cast<float>(sg);
+  const float poly_diag = static_cast<float>(square ? ca - cb * cb / (4.0 * cc) : 0.0);
   auto group_launch = [&](const NsGroup& g) {
     GemmLaunch gl{};
     gl.batch = g.count;
@@ -444,9 +456,6 @@ int run_ns(prm_ctx* c, NsPlan& plan, void* base, bool update_momentum, float bet
     gl.c = g.c;
     gl.ldc = g.ldc;
     gl.ldr = g.ldr;
-    gl.ca = coeffs[0];
-    gl.cb = coeffs[1];
-    gl.cc = coeffs[2];
     gl.err = c->d_err;
     gl.num_sms = c->num_sms;
     return gl;
@@ -457,34 +466,39 @@ int run_ns(prm_ctx* c, NsPlan& plan, void* base, bool update_momentum, float bet
     for (auto& g : plan.groups) {
       GemmLaunch gl = group_launch(g);
       gl.scale = it == 0 ? reinterpret_cast<float*>(b + g.off_scale) : nullptr;
+      gl.gain = gram_gain;
+      gl.diag = gram_diag;
+      gl.out_fp16 = square;  // C (fp16) for POLY; P (bf16) for COMBINE when c = 0
       const NsRClass& rcl = plan.rclasses[g.rclass];
       const size_t ev = c->prof.begin(stream);
       if ((e = launch_gram(odd ? g.mx1 : g.mx0, rcl.ma, g.base_slot, gl, stream)) != cudaSuccess)
         return cuda_fail(c, e, "gram launch");
       c->prof.end(ev, PRM_FAMILY_NS_GRAM, 1, 2.0 * g.count * double(g.r) * g.r * g.c, stream);
     }
-    for (auto& rcl : plan.rclasses) {
-      GemmLaunch gl{};
-      gl.batch = rcl.count;
-      gl.r = rcl.r;
-      gl.c = rcl.r;
-      gl.ldc = rcl.ldr;
-      gl.ldr = rcl.ldr;
-      gl.ca = coeffs[0];
-      gl.cb = coeffs[1];
-      gl.cc = coeffs[2];
-      gl.err = c->d_err;
-      gl.num_sms = c->num_sms;
-      const uint16_t* A = reinterpret_cast<const uint16_t*>(b + rcl.off_a);
-      const size_t ev = c->prof.begin(stream);
-      if ((e = launch_poly(rcl.ma, A, rcl.mb, gl, stream)) != cudaSuccess) return cuda_fail(c, e, "poly launch");
-      c->prof.end(ev, PRM_FAMILY_NS_POLY, 1, 2.0 * rcl.count * double(rcl.r) * rcl.r * rcl.r, stream);
+    if (square) {
+      for (auto& rcl : plan.rclasses) {
+        GemmLaunch gl{};
+        gl.batch = rcl.count;
+        gl.r = rcl.r;
+        gl.c = rcl.r;
+        gl.ldc = rcl.ldr;
+        gl.ldr = rcl.ldr;
+        gl.gain = poly_gain;
+        gl.diag = poly_diag;
+        gl.in_fp16 = true;
+        gl.err = c->d_err;
+        gl.num_sms = c->num_sms;
+        const size_t ev = c->prof.begin(stream);
+        if ((e = launch_poly(rcl.ma, rcl.mb, gl, stream)) != cudaSuccess) return cuda_fail(c, e, "poly launch");
+        c->prof.end(ev, PRM_FAMILY_NS_POLY, 1, 2.0 * rcl.count * double(rcl.r) * rcl.r * rcl.r, stream);
+      }
     }
     for (auto& g : plan.groups) {
       GemmLaunch gl = group_launch(g);
       gl.scale = it == 0 ? reinterpret_cast<float*>(b + g.off_scale) : nullptr;
       const size_t ev = c->prof.begin(stream);
-      if ((e = launch_combine(g.mb, odd ? g.mx1 : g.mx0, odd ? g.mx0 : g.mx1, gl, stream)) != cudaSuccess)
+      if ((e = launch_combine(square ? g.mb : g.ma, odd ? g.mx1 : g.mx0, odd ? g.mx0 : g.mx1, gl, stream)) !=
+          cudaSuccess)
         return cuda_fail(c, e, "combine launch");
       c->prof.end(ev, PRM_FAMILY_NS_COMBINE, 1, 2.0 * g.count * double(g.r) * g.r * g.c, stream);
     }
@@ -937,17 +951,18 @@ const char* prm_last_error(const prm_ctx* c) {
 }
 
 // ---------------------------------------------------------------- standalone
-int prm_ns_gram(const uint16_t* X, uint16_t* A, const float* scale, int batch, int64_t r, int64_t c, int64_t ldc,
-                int64_t ldr, void* stream) {
-  if (X == nullptr || A == nullptr || batch < 0 || r < 1 || c < r || ldc < c || ldr < r) return PRM_ERR_INVALID_ARG;
-  if (ldc % 8 || ldr % 8 || !aligned16(X) || !aligned16(A)) return PRM_ERR_ALIGNMENT;
+int prm_ns_gram(const uint16_t* X, uint16_t* C, const float* scale, float gain, float diag, int out_dtype,
+                int batch, int64_t r, int64_t c, int64_t ldc, int64_t ldr, void* stream) {
+  if (X == nullptr || C == nullptr || batch < 0 || r < 1 || c < r || ldc < c || ldr < r) return PRM_ERR_INVALID_ARG;
+  if (!finite(gain) || !finite(diag) || (out_dtype != PRM_BF16 && out_dtype != PRM_FP16)) return PRM_ERR_INVALID_ARG;
+  if (ldc % 8 || ldr % 8 || !aligned16(X) || !aligned16(C)) return PRM_ERR_ALIGNMENT;
   if (batch == 0) return PRM_OK;
   DeviceState* ds;
   int rc = device_state(&ds);
   if (rc != PRM_OK) return rc;
   NsMaps mx;
-  SymMaps ma;
-  if (encode_x_maps(&mx, X, batch, r, c, ldc) != 0 || encode_sym_maps(&ma, A, batch, r, ldr) != 0)
+  SymMaps mc;
+  if (encode_x_maps(&mx, X, batch, r, c, ldc) != 0 || encode_sym_maps(&mc, C, batch, r, ldr) != 0)
     return PRM_ERR_CUDA;
   GemmLaunch g{};
   g.batch = batch;
@@ -956,21 +971,26 @@ int prm_ns_gram(const uint16_t* X, uint16_t* A, const float* scale, int batch, i
   g.ldc = ldc;
   g.ldr = ldr;
   g.scale = scale;
+  g.gain = gain;
+  g.diag = diag;
+  g.out_fp16 = out_dtype == PRM_FP16;
   g.err = ds->d_err;
   g.num_sms = ds->num_sms;
-  return launch_gram(mx, ma, 0, g, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PRM_OK : PRM_ERR_CUDA;
+  return launch_gram(mx, mc, 0, g, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PRM_OK : PRM_ERR_CUDA;
 }
 
-int prm_ns_poly(const uint16_t* A, uint16_t* B, float a, float b, float cc, int batch, int64_t r, int64_t ldr,
-                void* stream) {
-  if (A == nullptr || B == nullptr || batch < 0 || r < 1 || ldr < r) return PRM_ERR_INVALID_ARG;
-  if (ldr % 8 || !aligned16(A) || !aligned16(B)) return PRM_ERR_ALIGNMENT;
+int prm_ns_poly(const uint16_t* C, uint16_t* P, float gain, float diag, int in_dtype, int batch, int64_t r,
+                int64_t ldr, void* stream) {
+  if (C == nullptr || P == nullptr || batch < 0 || r < 1 || ldr < r) return PRM_ERR_INVALID_ARG;
+  if (C == P || !finite(gain) || !finite(diag) || (in_dtype != PRM_BF16 && in_dtype != PRM_FP16))
+    return PRM_ERR_INVALID_ARG;
+  if (ldr % 8 || !aligned16(C) || !aligned16(P)) return PRM_ERR_ALIGNMENT;
   if (batch == 0) return PRM_OK;
   DeviceState* ds;
   int rc = device_state(&ds);
   if (rc != PRM_OK) return rc;
-  SymMaps ma, mb;
-  if (encode_sym_maps(&ma, A, batch, r, ldr) != 0 || encode_sym_maps(&mb, B, batch, r, ldr) != 0)
+  SymMaps mc, mp;
+  if (encode_sym_maps(&mc, C, batch, r, ldr) != 0 || encode_sym_maps(&mp, P, batch, r, ldr) != 0)
     return PRM_ERR_CUDA;
   GemmLaunch g{};
   g.batch = batch;
@@ -978,12 +998,12 @@ int prm_ns_poly(const uint16_t* A, uint16_t* B, float a, float b, float cc, int 
   g.c = r;
   g.ldc = ldr;
   g.ldr = ldr;
-  g.ca = a;
-  g.cb = b;
-  g.cc = cc;
+  g.gain = gain;
+  g.diag = diag;
+  g.in_fp16 = in_dtype == PRM_FP16;
   g.err = ds->d_err;
   g.num_sms = ds->num_sms;
-  return launch_poly(ma, A, mb, g, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PRM_OK : PRM_ERR_CUDA;
+  return launch_poly(mc, mp, g, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PRM_OK : PRM_ERR_CUDA;
 }
 
 int prm_ns_combine(const uint16_t* X, const uint16_t* B, uint16_t* Xout, const float* scale, int batch, int64_t r,
@@ -1043,7 +1063,10 @@ int prm_newton_schulz(const float* in, float* out, int batch, int64_t m, int64_t
   if (batch == 0) return PRM_OK;
   float coeffs[3] = {DEFAULT_COEFFS[0], DEFAULT_COEFFS[1], DEFAULT_COEFFS[2]};
   if (ns_coeffs)
-    for (int i = 0; i < 3; ++i) coeffs[i] = ns_coeffs[i];
+    for (int i = 0; i < 3; ++i) {
+      if (!finite(ns_coeffs[i])) return PRM_ERR_INVALID_ARG;
+      coeffs[i] = ns_coeffs[i];
+    }
   DeviceState* ds;
   int rc = device_state(&ds);
   if (rc != PRM_OK) return rc;

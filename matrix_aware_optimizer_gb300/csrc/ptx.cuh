@@ -291,11 +291,13 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
   return d;
 }
 
-// Instruction descriptor of tcgen05.mma kind::f16 with bf16 A/B and fp32 D.
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn_major, bool b_mn_major) {
+// Instruction descriptor of tcgen05.mma kind::f16 with fp32 D and A / B both
+// bf16 or both fp16 (one MMA never mixes the two).
+__host__ __device__ constexpr uint32_t idesc_f16kind_f32(int M, int N, bool a_mn_major, bool b_mn_major,
+                                                         bool operands_fp16) {
   return (1u << 4)                                  // D format: f32
-         | (1u << 7)                                // A format: bf16
-         | (1u << 10)                               // B format: bf16
+         | ((operands_fp16 ? 0u : 1u) << 7)         // A format: 0 f16, 1 bf16
+         | ((operands_fp16 ? 0u : 1u) << 10)        // B format: 0 f16, 1 bf16
          | ((a_mn_major ? 1u : 0u) << 15)           // A major-ness
          | ((b_mn_major ? 1u : 0u) << 16)           // B major-ness
          | ((static_cast<uint32_t>(N) >> 3) << 17)  // N / 8

@@ -32,6 +32,7 @@ FAMILY_NAMES = ["rownorm_wide", "rownorm_tall", "ns_prep", "ns_gram", "ns_poly",
 
 PRM_FP32 = 0
 PRM_BF16 = 1
+PRM_FP16 = 2
 PRM_MODE_PRMUON = 0
 PRM_MODE_MUONBP = 1
 
@@ -74,8 +75,9 @@ SIGNATURES = {
     "prm_profile": (c_int, [c_void_p, c_int]),
     "prm_profile_read": (c_int, [c_void_p, c_int, POINTER(ctypes.c_double), POINTER(c_int64), POINTER(c_int64),
                                  POINTER(ctypes.c_double)]),
-    "prm_ns_gram": (c_int, [c_void_p, c_void_p, c_void_p, c_int, c_int64, c_int64, c_int64, c_int64, c_void_p]),
-    "prm_ns_poly": (c_int, [c_void_p, c_void_p, c_float, c_float, c_float, c_int, c_int64, c_int64, c_void_p]),
+    "prm_ns_gram": (c_int, [c_void_p, c_void_p, c_void_p, c_float, c_float, c_int, c_int, c_int64, c_int64,
+                            c_int64, c_int64, c_void_p]),
+    "prm_ns_poly": (c_int, [c_void_p, c_void_p, c_float, c_float, c_int, c_int, c_int64, c_int64, c_void_p]),
     "prm_ns_combine": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int64, c_int64, c_int64,
                                c_int64, c_void_p]),
     "prm_rownorm_tall_step_noalloc": (c_int, [c_void_p, c_void_p, c_void_p, c_int, c_int64, c_int64, c_float,
@@ -193,13 +195,16 @@ def prm_profile_read(ctx, family: int = -1):
     return ms.value, n.value, k.value, w.value
 
 
-def prm_ns_gram(X: int, A: int, scale: int, batch: int, r: int, c: int, ldc: int, ldr: int, stream: int = 0):
-    check(load().prm_ns_gram(c_void_p(X), c_void_p(A), c_void_p(scale), batch, r, c, ldc, ldr,
-                             c_void_p(stream)), "prm_ns_gram")
+def prm_ns_gram(X: int, C: int, scale: int, gain: float, diag: float, out_dtype: int, batch: int, r: int, c: int,
+                ldc: int, ldr: int, stream: int = 0):
+    check(load().prm_ns_gram(c_void_p(X), c_void_p(C), c_void_p(scale), gain, diag, out_dtype, batch, r, c, ldc,
+                             ldr, c_void_p(stream)), "prm_ns_gram")
 
 
-def prm_ns_poly(A: int, P: int, a: float, b: float, cc: float, batch: int, r: int, ldr: int, stream: int = 0):
-    check(load().prm_ns_poly(c_void_p(A), c_void_p(P), a, b, cc, batch, r, ldr, c_void_p(stream)), "prm_ns_poly")
+def prm_ns_poly(C: int, P: int, gain: float, diag: float, in_dtype: int, batch: int, r: int, ldr: int,
+                stream: int = 0):
+    check(load().prm_ns_poly(c_void_p(C), c_void_p(P), gain, diag, in_dtype, batch, r, ldr, c_void_p(stream)),
+          "prm_ns_poly")
 
 
 def prm_ns_combine(X: int, P: int, Xout: int, scale: int, batch: int, r: int, c: int, ldc: int, ldr: int,

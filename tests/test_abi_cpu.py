@@ -70,9 +70,12 @@ def test_null_context_calls_return_status(lib):
 
 def test_standalone_argument_checks(lib):
     # rejected before any device work
-    assert lib.prm_ns_gram(None, None, None, 1, 8, 8, 8, 8, None) == N.PRM_ERR_INVALID_ARG
+    assert lib.prm_ns_gram(None, None, None, 1.0, 0.0, N.PRM_BF16, 1, 8, 8, 8, 8, None) == N.PRM_ERR_INVALID_ARG
+    assert lib.prm_ns_gram(16, 32, None, float("nan"), 0.0, N.PRM_BF16, 1, 8, 8, 8, 8, None) == N.PRM_ERR_INVALID_ARG
+    assert lib.prm_ns_gram(16, 32, None, 1.0, 0.0, N.PRM_FP32, 1, 8, 8, 8, 8, None) == N.PRM_ERR_INVALID_ARG
     assert lib.prm_ns_combine(16, 32, 16, None, 1, 8, 8, 8, 8, None) == N.PRM_ERR_INVALID_ARG  # aliasing
-    assert lib.prm_ns_poly(16, 32, 1.0, 1.0, 1.0, 1, 8, 12, None) == N.PRM_ERR_ALIGNMENT  # pitch % 8
+    assert lib.prm_ns_poly(16, 16, 1.0, 1.0, N.PRM_FP16, 1, 8, 8, None) == N.PRM_ERR_INVALID_ARG  # aliasing
+    assert lib.prm_ns_poly(16, 32, 1.0, 1.0, N.PRM_FP16, 1, 8, 12, None) == N.PRM_ERR_ALIGNMENT  # pitch % 8
     n = ctypes.c_size_t()
     assert lib.prm_newton_schulz_workspace(0, 4, 4, ctypes.byref(n)) == N.PRM_OK and n.value == 0
     assert lib.prm_newton_schulz_workspace(2, 0, 4, ctypes.byref(n)) == N.PRM_ERR_INVALID_ARG

@@ -4,7 +4,7 @@ update the step actually applied.
 
   D vs oracle (teacher-forced, relative Frobenius):
     RowNorm branch                   <= 1e-5  (fp32 quotient of a 1e-6 momentum)
-    NS5 branch (full or per block)   <= 2e-2  (4e-2 for a short side below 16)
+    NS5 branch (full or per block)   <= 2e-2  (1e-1 for a short side below 16)
   D vs the applied update: W_t = W_{t-1} (1 - lr wd) - eta s D within 2 ulp of
   W_t plus 8 roundings of the step term, everywhere -- the NS5 direction is
   bf16, so any other bf16 value would move W by hundreds of such units."""
@@ -23,7 +23,7 @@ pytestmark = pytest.mark.gpu
 
 TOL_D_ROWNORM = 1e-5
 TOL_D_NS5 = 2e-2
-TOL_D_NS5_TINY = 4e-2
+TOL_D_NS5_TINY = 1e-1  # short side < 16: the derived bound of test_gpu_parity
 
 
 @pytest.fixture(scope="module", autouse=True)

@@ -13,6 +13,11 @@ from .gpu_helpers import ensure_built, rel_frob
 pytestmark = pytest.mark.gpu
 
 A_C, B_C, C_C = 3.4445, -4.7750, 2.0315
+# the completed-square stage constants of the default quintic
+GRAM_GAIN = np.sqrt(C_C)
+GRAM_DIAG = B_C / (2 * np.sqrt(C_C))
+POLY_GAIN = 1.0
+POLY_DIAG = A_C - B_C ** 2 / (4 * C_C)
 SHAPES = [(3, 256, 512), (2, 384, 1000), (1, 64, 96), (2, 1024, 3072), (1, 40, 104), (4, 128, 128)]
 
 
@@ -32,20 +37,22 @@ def _lib():
     N.load()
 
 
+@pytest.mark.parametrize("out_dtype", [torch.float16, torch.bfloat16])
 @pytest.mark.parametrize("batch,r,c", SHAPES)
-def test_gram_matches_fp32_matmul(batch, r, c):
+def test_gram_matches_fp32_matmul(batch, r, c, out_dtype):
     gen = torch.Generator().manual_seed(r * 7 + c)
     ldc, ldr = _pitch(c), _pitch(r)
     X = _rand_bf16(batch, r, c, ldc, gen, 1.0 / np.sqrt(c))
     scale = torch.rand(batch, generator=gen) + 0.5
     Xd, sd = X.cuda(), scale.cuda()
-    Ad = torch.full((batch, r, ldr), float("nan"), dtype=torch.bfloat16, device="cuda")
-    N.prm_ns_gram(Xd.data_ptr(), Ad.data_ptr(), sd.data_ptr(), batch, r, c, ldc, ldr,
+    Ad = torch.full((batch, r, ldr), float("nan"), dtype=out_dtype, device="cuda")
+    N.prm_ns_gram(Xd.data_ptr(), Ad.data_ptr(), sd.data_ptr(), GRAM_GAIN, GRAM_DIAG,
+                  N.PRM_FP16 if out_dtype == torch.float16 else N.PRM_BF16, batch, r, c, ldc, ldr,
                   torch.cuda.current_stream().cuda_stream)
     torch.cuda.synchronize()
     A = Ad.float().cpu()[:, :, :r]
     Xf = X.float()[:, :, :c]
-    ref = (scale ** 2)[:, None, None] * (Xf @ Xf.transpose(1, 2))
+    ref = GRAM_GAIN * (scale ** 2)[:, None, None] * (Xf @ Xf.transpose(1, 2)) + GRAM_DIAG * torch.eye(r)
     for i in range(batch):
         assert torch.isfinite(A[i]).all(), "unwritten output element"
         assert rel_frob(A[i].numpy(), ref[i].numpy()) < 4e-3
@@ -58,17 +65,19 @@ def test_poly_matches_fp32_matmul(batch, r, c):
     gen = torch.Generator().manual_seed(r * 11 + c)
     ldr = _pitch(r)
     Xs = torch.randn(batch, r, c, generator=gen) / np.sqrt(c)
-    Asym = (Xs @ Xs.transpose(1, 2)).to(torch.bfloat16)
-    Asym = ((Asym.float() + Asym.float().transpose(1, 2)) / 2).to(torch.bfloat16)  # exactly symmetric
-    A = torch.zeros(batch, r, ldr, dtype=torch.bfloat16)
+    # C = sqrt(c) A + b / (2 sqrt(c)) I, stored in fp16 as the Gram stage writes it
+    C = GRAM_GAIN * (Xs @ Xs.transpose(1, 2)) + GRAM_DIAG * torch.eye(r)
+    Asym = ((C + C.transpose(1, 2)) / 2).to(torch.float16)  # exactly symmetric
+    A = torch.zeros(batch, r, ldr, dtype=torch.float16)
     A[:, :, :r] = Asym
     Ad = A.cuda()
     Bd = torch.full((batch, r, ldr), float("nan"), dtype=torch.bfloat16, device="cuda")
-    N.prm_ns_poly(Ad.data_ptr(), Bd.data_ptr(), A_C, B_C, C_C, batch, r, ldr, torch.cuda.current_stream().cuda_stream)
+    N.prm_ns_poly(Ad.data_ptr(), Bd.data_ptr(), POLY_GAIN, POLY_DIAG, N.PRM_FP16, batch, r, ldr,
+                  torch.cuda.current_stream().cuda_stream)
     torch.cuda.synchronize()
     B = Bd.float().cpu()[:, :, :r]
     Af = Asym.float()
-    ref = A_C * torch.eye(r) + B_C * Af + C_C * (Af @ Af)
+    ref = POLY_GAIN * (Af @ Af) + POLY_DIAG * torch.eye(r)
     for i in range(batch):
         assert torch.isfinite(B[i]).all()
         assert rel_frob(B[i].numpy(), ref[i].numpy()) < 4e-3
@@ -111,3 +120,21 @@ def test_combine_is_not_symmetric_in_disguise():
     torch.cuda.synchronize()
     ref = B.float() @ X.float()
     assert rel_frob(Od.float().cpu().numpy(), ref.numpy()) < 4e-3
+
+
+@pytest.mark.parametrize("gain", [1.0, -1.0])
+def test_poly_negative_gain(gain):
+    """sgn(c) = -1 (a quintic with c < 0) flips the square's sign."""
+    gen = torch.Generator().manual_seed(9)
+    r = 384
+    Xs = torch.randn(1, r, 512, generator=gen) / np.sqrt(512)
+    Csym = (Xs @ Xs.transpose(1, 2) - 0.5 * torch.eye(r)).to(torch.bfloat16)
+    Csym = ((Csym.float() + Csym.float().transpose(1, 2)) / 2).to(torch.bfloat16)
+    Cd = Csym.cuda()
+    Pd = torch.empty_like(Cd)
+    N.prm_ns_poly(Cd.data_ptr(), Pd.data_ptr(), gain, 0.25, N.PRM_BF16, 1, r, r,
+                  torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    Cf = Csym.float()
+    ref = gain * (Cf @ Cf) + 0.25 * torch.eye(r)
+    assert rel_frob(Pd.float().cpu().numpy(), ref.numpy()) < 4e-3
