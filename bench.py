@@ -29,6 +29,10 @@ import time
 ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
+# The end-to-end leg runs the compute stream, several copy streams (some of
+# them waiting on events) and a read-back stream at once; with the default 8
+# hardware work queues, streams that share a queue would also share its waits.
+os.environ.setdefault("CUDA_DEVICE_MAX_CONNECTIONS", "32")
 
 METRIC = "ms per K=3 PR-Muon cycle (1.3B/15B DiT shapes); NS5 TFLOP/s; RowNorm GB/s"
 UNIT = "ms/cycle"
@@ -545,8 +549,10 @@ def run_ours(args):
         d2h = out_row.numel() * 4
         d2h_stream = torch.cuda.Stream(device=dev)  # the read-back never holds up the next step
 
+        stream_pool = [torch.cuda.Stream(device=dev) for _ in range(8)]
+
         def upload_alone(nstreams):
-            css = [torch.cuda.Stream(device=dev) for _ in range(nstreams)]
+            css = stream_pool[:nstreams]
             bnd = [total * q // nstreams // 128 * 128 for q in range(nstreams)] + [total]
             best = None
             for _ in range(3):
@@ -564,12 +570,12 @@ def run_ours(args):
             return best
 
         # the host link rate behind the number, and the copy-stream count used
-        up_ms = {n: upload_alone(n) for n in (4, 8)}
+        up_ms = {n: upload_alone(n) for n in (1, 4)}
         ncopy = min(up_ms, key=up_ms.get)
-        copy_streams = [torch.cuda.Stream(device=dev) for _ in range(ncopy)]
+        copy_streams = stream_pool[:ncopy]
         bounds = [total * q // ncopy // 128 * 128 for q in range(ncopy)] + [total]
 
-        def run(first_t, nsteps, per=None):
+        def run(first_t, nsteps, per=None, up_ev=None):
             step_done = {}
             uploaded = {}
 
@@ -579,10 +585,14 @@ def run_ours(args):
                 for q, cs in enumerate(copy_streams):
                     if s - nbuf in step_done:
                         cs.wait_event(step_done[s - nbuf])
+                    if up_ev is not None:
+                        up_ev[s][q][0].record(cs)
                     with torch.cuda.stream(cs):
                         dst[bounds[q]:bounds[q + 1]].copy_(hflat[bounds[q]:bounds[q + 1]], non_blocking=True)
-                    e = torch.cuda.Event()
+                    e = torch.cuda.Event(enable_timing=up_ev is not None)
                     e.record(cs)
+                    if up_ev is not None:
+                        up_ev[s][q][1] = e
                     ev.append(e)
                 uploaded[s] = ev
 
@@ -612,9 +622,10 @@ def run_ours(args):
             dist.barrier()
         nst = args.steps * ms.K
         per = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(nst)]
+        up_ev = [[[torch.cuda.Event(enable_timing=True), None] for _ in copy_streams] for _ in range(nst)]
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        run((args.warmup + args.steps) * ms.K, nst, per)
+        run((args.warmup + args.steps) * ms.K, nst, per, up_ev)
         e1.record(stream)
         torch.cuda.synchronize()
         e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, dev)
@@ -622,12 +633,18 @@ def run_ours(args):
         # (a step waiting for its gradients)
         busy = sum(a.elapsed_time(b) for a, b in per) / args.steps
         waits = [per[s][1].elapsed_time(per[s + 1][0]) for s in range(nst - 1)]
+        # each upload from its first piece's start to its last piece's end (the
+        # uploads follow one another on the link)
+        up_busy = sum(max(up_ev[s][q][0].elapsed_time(up_ev[s][q][1]) for q in range(ncopy))
+                      for s in range(nst)) / args.steps
         e2e = {"value": round(e2e_ms, 3), "unit": UNIT, "h2d_bytes_per_step": h2d * ms.K,
                "d2h_bytes_per_step": d2h * ms.K,
                "h2d_gbs_alone": round(h2d / up_ms[ncopy] / 1e6, 1), "copy_streams": ncopy,
                "gradient_buffers": nbuf, "steps_ms_per_cycle": round(busy, 3),
                "waits_ms_per_cycle": round(sum(waits) / args.steps, 3),
                "longest_wait_ms": round(max(waits) if waits else 0.0, 3),
+               "uploads_ms_per_cycle": round(up_busy, 3),
+               "h2d_gbs_under_load": round(h2d * ms.K / up_busy / 1e6, 1) if up_busy > 0 else None,
                "note": "per optimizer step: that step's gradients copied from pinned host memory (copy streams in "
                        "parallel), the step, one parameter row read back; the gradient buffers rotate so that "
                        "the uploads of the next steps overlap the current one"}
