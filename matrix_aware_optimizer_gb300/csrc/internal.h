@@ -68,6 +68,7 @@ cudaError_t launch_apply(const View* d_views, int count, int64_t rows, int64_t c
                          const uint16_t* X, int64_t ldc, int64_t x_mat_stride, float decay,
                          float eta, cudaStream_t stream);
 
+
 // ---- tcgen05 GEMM stages of one NS5 round -------------------------------
 enum GemmKind { GEMM_GRAM = 0, GEMM_POLY = 1, GEMM_COMBINE = 2 };
 
@@ -86,25 +87,37 @@ struct SymMaps {
 int encode_x_maps(NsMaps* maps, const void* X, int batch, int64_t r, int64_t c, int64_t ldc);
 int encode_sym_maps(SymMaps* maps, const void* A, int batch, int64_t r, int64_t ldr);
 
-struct GemmLaunch {
+// One same-shape batch of a GEMM launch: `batch` matrices of r x c (GRAM
+// reads X, r x c; POLY reads C, r x r; COMBINE reads P, r x r, and X, r x c).
+// Maps: GRAM a = b = X rows128, out = C store (matrices out_z0 ..);
+// POLY a = b = C rows128, out = P store; COMBINE a = P rows128, b = X x_k64,
+// out = X' store.
+struct GemmSegSpec {
+  const CUtensorMap* a;
+  const CUtensorMap* b;
+  const CUtensorMap* out;
+  const float* scale;     // per-matrix s or nullptr (GRAM: s^2, COMBINE: s)
   int batch;
-  int64_t r, c, ldc, ldr;
-  const float* scale;     // per-matrix scale or nullptr
-  float gain, diag;       // GRAM / POLY epilogue: gain * acc + diag on the diagonal
-  bool in_fp16;           // operands fp16 (POLY reading C) instead of bf16
-  bool out_fp16;          // output packed as fp16 (GRAM writing C) instead of bf16
-  int* err;               // device error word
-  int num_sms;
+  int64_t r, c;
+  int out_z0;
 };
 
-// GRAM: C = gain * scale^2 * X X^T + diag * I into matrices
-// [out_z0, out_z0 + batch) of `cout` (an r-class array); POLY: P = gain * C C
-// + diag * I over the r-class; COMBINE: Xout = scale * P X.
-cudaError_t launch_gram(const NsMaps& xin, const SymMaps& cout, int out_z0, const GemmLaunch& g,
+// Launch-wide epilogue constants: GRAM / POLY write gain * acc + diag on the
+// diagonal (GRAM also scale^2), COMBINE scale * acc.
+struct GemmEpilogue {
+  float gain = 1.f, diag = 0.f;
+  bool in_fp16 = false;   // operands fp16 (POLY reading C) instead of bf16
+  bool out_fp16 = false;  // output packed as fp16 (GRAM writing C) instead of bf16
+  int* err = nullptr;     // device error word
+  int num_sms = 0;
+};
+
+constexpr int GEMM_MAX_SEGMENTS = 7;  // segments per launch (kernel parameter block under 4 KB)
+
+// Runs the tiles of every segment of one GEMM kind from one queue (in
+// launches of up to 7 segments; segments with the longest reduction first).
+cudaError_t launch_gemm(GemmKind kind, const GemmSegSpec* segs, int count, const GemmEpilogue& epi,
                         cudaStream_t stream);
-cudaError_t launch_poly(const SymMaps& c, const SymMaps& pout, const GemmLaunch& g, cudaStream_t stream);
-cudaError_t launch_combine(const SymMaps& b, const NsMaps& xin, const NsMaps& xout, const GemmLaunch& g,
-                           cudaStream_t stream);
 
 // Largest dynamic shared memory the GEMM kernels request (for set-up checks).
 size_t gemm_smem_bytes();

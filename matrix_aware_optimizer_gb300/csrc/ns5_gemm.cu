@@ -53,6 +53,7 @@
 #include <algorithm>
 #include <atomic>
 #include <mutex>
+#include <vector>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -91,22 +92,37 @@ constexpr size_t SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + EPI_SMEM_BYTES + BAR
 static_assert(SMEM_BYTES <= 232448, "dynamic shared memory above the 227 KB per-block limit");
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;  // 2 s per individual wait
 
-struct GemmParams {
-  int M;              // output rows (r)
-  int N;              // output cols (r for GRAM/POLY, c for COMBINE)
-  int K;              // reduction length (c for GRAM, r otherwise)
-  int tiles_m;        // COMBINE: ceil(M / 256)
-  int nb;             // GRAM/POLY: ceil(M / 256) super-blocks per side
+// One same-shape batch of a launch: an NS5 group (GRAM, COMBINE) or an
+// r-class (POLY). A launch runs the tiles of up to MAX_SEGS segments from one
+// queue, so the tail of one batch overlaps the next instead of idling SMs
+// between launches.
+constexpr int MAX_SEGS = GEMM_MAX_SEGMENTS;  // 7: keeps the parameter block under 4 KB (a segment is 512 bytes)
+struct Segment {
+  CUtensorMap mapA;    // A operand, 128-row K-major boxes
+  CUtensorMap mapB;    // B operand: K-major rows (GRAM, POLY), 64 x 64 MN-major boxes (COMBINE)
+  CUtensorMap mapOut;  // output, 32 x 32 store boxes
+  const float* scale;  // per-matrix s (GRAM applies s^2, COMBINE s), or nullptr
+  int64_t tile_begin;  // first tile of this segment in the launch's queue
+  int M;               // output rows (r)
+  int N;               // output cols (r for GRAM/POLY, c for COMBINE)
+  int K;               // reduction length (c for GRAM, r otherwise)
+  int tiles_m;         // COMBINE: ceil(M / 256)
+  int nb;              // GRAM/POLY: ceil(M / 256) super-blocks per side
   int tiles_per_mat;
+  int out_z0;          // first matrix of the output map this segment writes
+};
+
+struct GemmParams {
+  Segment seg[MAX_SEGS];
+  int nseg;
   int64_t total_tiles;
-  int out_z0;           // first matrix of the output map this launch writes
-  const float* scale;   // per-matrix s (GRAM: s^2 applied; COMBINE: s), or nullptr
   float gain, diag;     // GRAM / POLY: out = gain * (scale^2) * acc + diag * [i == j]
   int in_fp16;          // operands are fp16 (POLY reading C); else bf16
   int out_fp16;         // output is packed as fp16 (GRAM writing C); else bf16
   int* err;
   uint64_t timeout_ns;
 };
+static_assert(sizeof(GemmParams) <= 4096, "kernel parameters above the 4 KB classic limit");
 
 struct TileCoord {
   int mat;
@@ -115,9 +131,17 @@ struct TileCoord {
   bool mirror;
 };
 
-// Pair tile `tile` of the queue: (matrix, 256-row block, 256-column block).
+// Segment holding queue tile `tile` (segments are stored in queue order).
+__device__ __forceinline__ int seg_of(const GemmParams& p, int64_t tile) {
+  int s = 0;
+  while (s + 1 < p.nseg && tile >= p.seg[s + 1].tile_begin) ++s;
+  return s;
+}
+
+// Tile `tile` of segment `p` (counted from the segment's first tile):
+// (matrix, 256-row block, 256-column block).
 template <int KIND>
-__device__ __forceinline__ TileCoord tile_coord(const GemmParams& p, int64_t tile) {
+__device__ __forceinline__ TileCoord tile_coord(const Segment& p, int64_t tile) {
   TileCoord t;
   t.mat = static_cast<int>(tile / p.tiles_per_mat);
   const int local = static_cast<int>(tile - static_cast<int64_t>(t.mat) * p.tiles_per_mat);
@@ -166,23 +190,24 @@ __device__ __forceinline__ uint32_t stage_off(int row, int chunk) {
 // previous stores (two chunks back) must have read them before they are
 // rewritten.
 template <int KIND>
-__device__ __forceinline__ void epilogue_tile(const GemmParams& p, const CUtensorMap* tm_out, const TileCoord& tc,
-                                              int i, uint32_t t_row, uint8_t* stage, int lane, uint32_t& nchunk) {
+__device__ __forceinline__ void epilogue_tile(const GemmParams& p, const Segment& sg, const TileCoord& tc, int i,
+                                              uint32_t t_row, uint8_t* stage, int lane, uint32_t& nchunk) {
   const int i0 = i - lane;  // first output row of this warp
+  const CUtensorMap* tm_out = &sg.mapOut;
   float s = 1.f;
-  if (KIND == GEMM_GRAM && p.scale != nullptr) {
-    const float q = p.scale[tc.mat];
+  if (KIND == GEMM_GRAM && sg.scale != nullptr) {
+    const float q = sg.scale[tc.mat];
     s = q * q;
   }
-  if (KIND == GEMM_COMBINE && p.scale != nullptr) s = p.scale[tc.mat];
+  if (KIND == GEMM_COMBINE && sg.scale != nullptr) s = sg.scale[tc.mat];
   if (KIND != GEMM_COMBINE) s *= p.gain;
-  const int z = p.out_z0 + tc.mat;
-  const bool rows_in = i0 < p.M;  // warp-uniform
+  const int z = sg.out_z0 + tc.mat;
+  const bool rows_in = i0 < sg.M;  // warp-uniform
 
 #pragma unroll
   for (int q = 0; q < EPI_CHUNKS; ++q) {
     const int j0 = tc.n0 + q * 32;
-    if (j0 < p.N) {  // uniform over the warp: depends on the tile only
+    if (j0 < sg.N) {  // uniform over the warp: depends on the tile only
       float v[32];
       tmem_load_32cols(t_row + static_cast<uint32_t>(q * 32), v);
 #pragma unroll
@@ -230,8 +255,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const CUtenso
 
 template <int KIND>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
-    ns_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const __grid_constant__ CUtensorMap tmOut, const GemmParams p) {
+    ns_gemm_kernel(const __grid_constant__ GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
@@ -274,18 +298,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
   cluster_sync_all();
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_holder;
-  const int num_kb = (p.K + BK - 1) / BK;
 
   if (warp == 0) {
     if (lane == 0) {
-      tma_prefetch_desc(&tmA);
-      tma_prefetch_desc(&tmB);
+      for (int q = 0; q < p.nseg; ++q) {
+        tma_prefetch_desc(&p.seg[q].mapA);
+        tma_prefetch_desc(&p.seg[q].mapB);
+      }
       int stage = 0;
       uint32_t phase = 0;
       uint32_t issued = 0, issued_parity = 0;
       bool ok = true;
       for (int64_t tile = pair_id; ok && tile < p.total_tiles; tile += num_pairs) {
-        const TileCoord tc = tile_coord<KIND>(p, tile);
+        const Segment& sg = p.seg[seg_of(p, tile)];
+        const TileCoord tc = tile_coord<KIND>(sg, tile - sg.tile_begin);
+        const int num_kb = (sg.K + BK - 1) / BK;
         const int m_cta = tc.m0 + static_cast<int>(rank) * BM;
         const int n_cta = tc.n0 + static_cast<int>(rank) * BN_HALF;
         for (int kb = 0; kb < num_kb; ++kb) {
@@ -297,13 +324,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
           const uint32_t bar = mapa_shared(smem_u32(&full_bar[stage]), 0);
           uint8_t* a_dst = sA + stage * A_TILE_BYTES;
           uint8_t* b_dst = sB + stage * B_TILE_BYTES;
-          tma_load_3d_pair(a_dst, &tmA, bar, kb * BK, m_cta, tc.mat);
+          tma_load_3d_pair(a_dst, &sg.mapA, bar, kb * BK, m_cta, tc.mat);
           if (KIND == GEMM_COMBINE) {
 #pragma unroll
             for (int q = 0; q < BN_HALF / 64; ++q)
-              tma_load_3d_pair(b_dst + q * MN_CHUNK_BYTES, &tmB, bar, n_cta + q * 64, kb * BK, tc.mat);
+              tma_load_3d_pair(b_dst + q * MN_CHUNK_BYTES, &sg.mapB, bar, n_cta + q * 64, kb * BK, tc.mat);
           } else {
-            tma_load_3d_pair(b_dst, &tmB, bar, kb * BK, n_cta, tc.mat);
+            tma_load_3d_pair(b_dst, &sg.mapB, bar, kb * BK, n_cta, tc.mat);
           }
           issued |= 1u << stage;
           issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
@@ -334,6 +361,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       uint32_t acc_phase = 0;
       bool ok = true, issued_any = false;
       for (int64_t tile = pair_id; ok && tile < p.total_tiles; tile += num_pairs) {
+        const int num_kb = (p.seg[seg_of(p, tile)].K + BK - 1) / BK;
         if (!wait_bounded(&tempty_bar[acc], acc_phase ^ 1u, abort_flag, p.err, p.timeout_ns)) {
           ok = false;
           break;
@@ -380,18 +408,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     const int quarter = warp & 3;  // TMEM lanes [32 * quarter, 32 * quarter + 32) belong to this warp
     uint8_t* stage = sEpi + quarter * EPI_WARP_BYTES;
     uint32_t nchunk = 0;
-    if (lane == 0) tma_prefetch_desc(&tmOut);
+    if (lane == 0)
+      for (int q = 0; q < p.nseg; ++q) tma_prefetch_desc(&p.seg[q].mapOut);
     const uint32_t tempty_even = mapa_shared(smem_u32(&tempty_bar[0]), 0);
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int64_t tile = pair_id; tile < p.total_tiles; tile += num_pairs) {
-      const TileCoord tc = tile_coord<KIND>(p, tile);
+      const Segment& sg = p.seg[seg_of(p, tile)];
+      const TileCoord tc = tile_coord<KIND>(sg, tile - sg.tile_begin);
       const int i = tc.m0 + static_cast<int>(rank) * BM + quarter * 32 + lane;
       const bool got = wait_bounded(&tfull_bar[acc], acc_phase, abort_flag, p.err, p.timeout_ns);
       if (!__all_sync(0xffffffffu, got)) break;
       tc_fence_after_sync();
       const uint32_t t_row = tmem_base + static_cast<uint32_t>(acc * BN) + (static_cast<uint32_t>(quarter * 32) << 16);
-      epilogue_tile<KIND>(p, &tmOut, tc, i, t_row, stage, lane, nchunk);
+      epilogue_tile<KIND>(p, sg, tc, i, t_row, stage, lane, nchunk);
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive_remote(tempty_even + static_cast<uint32_t>(acc * sizeof(uint64_t)));
@@ -477,33 +507,11 @@ int max_resident_pairs(int num_sms) {
 }
 
 template <int KIND>
-cudaError_t launch_kind(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& out, const GemmParams& p,
-                        int num_sms, cudaStream_t stream) {
+cudaError_t launch_kind(const GemmParams& p, int num_sms, cudaStream_t stream) {
   if (p.total_tiles == 0) return cudaSuccess;
   const int64_t pairs = std::min<int64_t>(p.total_tiles, max_resident_pairs<KIND>(num_sms));
-  ns_gemm_kernel<KIND><<<static_cast<unsigned>(2 * pairs), NUM_THREADS, SMEM_BYTES, stream>>>(a, b, out, p);
+  ns_gemm_kernel<KIND><<<static_cast<unsigned>(2 * pairs), NUM_THREADS, SMEM_BYTES, stream>>>(p);
   return cudaGetLastError();
-}
-
-GemmParams base_params(const GemmLaunch& g) {
-  GemmParams p{};
-  p.scale = g.scale;
-  p.gain = g.gain;
-  p.diag = g.diag;
-  p.in_fp16 = g.in_fp16 ? 1 : 0;
-  p.out_fp16 = g.out_fp16 ? 1 : 0;
-  p.err = g.err;
-  p.timeout_ns = WAIT_LIMIT_NS;
-  return p;
-}
-
-void set_symmetric_tiles(GemmParams& p, int batch, int64_t r) {
-  p.M = static_cast<int>(r);
-  p.N = static_cast<int>(r);
-  p.nb = static_cast<int>((r + BN - 1) / BN);
-  p.tiles_m = 0;
-  p.tiles_per_mat = p.nb * (p.nb + 1) / 2;  // upper-triangle 256 x 256 super-blocks
-  p.total_tiles = static_cast<int64_t>(p.tiles_per_mat) * batch;
 }
 
 }  // namespace
@@ -535,37 +543,58 @@ int encode_sym_maps(SymMaps* maps, const void* A, int batch, int64_t r, int64_t 
   return encode_3d(&maps->store, A, batch, r, r, ldr, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
-cudaError_t launch_gram(const NsMaps& xin, const SymMaps& aout, int out_z0, const GemmLaunch& g,
+cudaError_t launch_gemm(GemmKind kind, const GemmSegSpec* specs, int count, const GemmEpilogue& epi,
                         cudaStream_t stream) {
-  GemmParams p = base_params(g);
-  set_symmetric_tiles(p, g.batch, g.r);
-  p.K = static_cast<int>(g.c);
-  p.out_z0 = out_z0;
-  return launch_kind<GEMM_GRAM>(xin.x_rows128, xin.x_rows128, aout.store, p, g.num_sms, stream);
-}
-
-cudaError_t launch_poly(const SymMaps& c, const SymMaps& pout, const GemmLaunch& g, cudaStream_t stream) {
-  GemmParams p = base_params(g);
-  set_symmetric_tiles(p, g.batch, g.r);
-  p.K = static_cast<int>(g.r);
-  p.out_z0 = 0;
-  p.scale = nullptr;
-  return launch_kind<GEMM_POLY>(c.rows128, c.rows128, pout.store, p, g.num_sms, stream);
-}
-
-cudaError_t launch_combine(const SymMaps& b, const NsMaps& xin, const NsMaps& xout, const GemmLaunch& g,
-                           cudaStream_t stream) {
-  GemmParams p = base_params(g);
-  p.M = static_cast<int>(g.r);
-  p.N = static_cast<int>(g.c);
-  p.K = static_cast<int>(g.r);
-  p.tiles_m = static_cast<int>((g.r + PAIR_M - 1) / PAIR_M);
-  p.nb = 0;
-  const int tiles_n = static_cast<int>((g.c + BN - 1) / BN);
-  p.tiles_per_mat = p.tiles_m * tiles_n;
-  p.total_tiles = static_cast<int64_t>(p.tiles_per_mat) * g.batch;
-  p.out_z0 = 0;
-  return launch_kind<GEMM_COMBINE>(b.rows128, xin.x_k64, xout.store, p, g.num_sms, stream);
+  // Longest tiles (largest K) first, so that the queue's last wave holds the
+  // shortest ones.
+  std::vector<int> order;
+  for (int i = 0; i < count; ++i)
+    if (specs[i].batch > 0) order.push_back(i);
+  auto reduction = [&](const GemmSegSpec& g) { return kind == GEMM_GRAM ? g.c : g.r; };
+  std::stable_sort(order.begin(), order.end(),
+                   [&](int x, int y) { return reduction(specs[x]) > reduction(specs[y]); });
+  for (size_t first = 0; first < order.size(); first += MAX_SEGS) {
+    GemmParams p{};
+    p.gain = epi.gain;
+    p.diag = epi.diag;
+    p.in_fp16 = epi.in_fp16 ? 1 : 0;
+    p.out_fp16 = epi.out_fp16 ? 1 : 0;
+    p.err = epi.err;
+    p.timeout_ns = WAIT_LIMIT_NS;
+    int64_t tiles = 0;
+    for (size_t k = first; k < order.size() && p.nseg < MAX_SEGS; ++k) {
+      const GemmSegSpec& g = specs[order[k]];
+      Segment& sg = p.seg[p.nseg++];
+      sg.mapA = *g.a;
+      sg.mapB = *g.b;
+      sg.mapOut = *g.out;
+      sg.scale = g.scale;
+      sg.tile_begin = tiles;
+      sg.out_z0 = g.out_z0;
+      if (kind == GEMM_COMBINE) {
+        sg.M = static_cast<int>(g.r);
+        sg.N = static_cast<int>(g.c);
+        sg.K = static_cast<int>(g.r);
+        sg.tiles_m = static_cast<int>((g.r + PAIR_M - 1) / PAIR_M);
+        sg.nb = 0;
+        sg.tiles_per_mat = sg.tiles_m * static_cast<int>((g.c + BN - 1) / BN);
+      } else {
+        sg.M = static_cast<int>(g.r);
+        sg.N = static_cast<int>(g.r);
+        sg.K = static_cast<int>(kind == GEMM_GRAM ? g.c : g.r);
+        sg.tiles_m = 0;
+        sg.nb = static_cast<int>((g.r + BN - 1) / BN);
+        sg.tiles_per_mat = sg.nb * (sg.nb + 1) / 2;  // upper-triangle 256 x 256 super-blocks
+      }
+      tiles += static_cast<int64_t>(sg.tiles_per_mat) * g.batch;
+    }
+    p.total_tiles = tiles;
+    cudaError_t e = kind == GEMM_GRAM   ? launch_kind<GEMM_GRAM>(p, epi.num_sms, stream)
+                    : kind == GEMM_POLY ? launch_kind<GEMM_POLY>(p, epi.num_sms, stream)
+                                        : launch_kind<GEMM_COMBINE>(p, epi.num_sms, stream);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 }  // namespace prm

@@ -449,59 +449,54 @@ int run_ns(prm_ctx* c, NsPlan& plan, void* base, bool update_momentum, float bet
   const float gram_diag = static_cast<float>(square ? sg * cb / (2.0 * root) : ca);
   const float poly_gain = static_cast<float>(sg);
   const float poly_diag = static_cast<float>(square ? ca - cb * cb / (4.0 * cc) : 0.0);
-  auto group_launch = [&](const NsGroup& g) {
-    GemmLaunch gl{};
-    gl.batch = g.count;
-    gl.r = g.r;
-    gl.c = g.c;
-    gl.ldc = g.ldc;
-    gl.ldr = g.ldr;
-    gl.err = c->d_err;
-    gl.num_sms = c->num_sms;
-    return gl;
-  };
-  // 2. five rounds in lockstep over the groups; POLY once per r-class
+  GemmEpilogue gram_epi, poly_epi, comb_epi;
+  gram_epi.gain = gram_gain;
+  gram_epi.diag = gram_diag;
+  gram_epi.out_fp16 = square;  // C (fp16) for POLY; P (bf16) for COMBINE when c = 0
+  poly_epi.gain = poly_gain;
+  poly_epi.diag = poly_diag;
+  poly_epi.in_fp16 = true;
+  for (GemmEpilogue* ep : {&gram_epi, &poly_epi, &comb_epi}) {
+    ep->err = c->d_err;
+    ep->num_sms = c->num_sms;
+  }
+  double gram_flops = 0, poly_flops = 0;
+  for (const auto& g : plan.groups) gram_flops += 2.0 * g.count * double(g.r) * g.r * g.c;
+  for (const auto& rcl : plan.rclasses) poly_flops += 2.0 * rcl.count * double(rcl.r) * rcl.r * rcl.r;
+  std::vector<GemmSegSpec> gram(plan.groups.size()), comb(plan.groups.size()), poly(plan.rclasses.size());
+  auto launches_for = [](size_t segments) { return static_cast<int>((segments + GEMM_MAX_SEGMENTS - 1) / GEMM_MAX_SEGMENTS); };
+  // 2. five rounds; each stage is one launch over every group (POLY: every
+  // r-class), so a round is three launches however many shapes there are
   for (int it = 0; it < steps; ++it) {
     const bool odd = (it & 1) != 0;  // round `it` reads X_it: x0 on even rounds, x1 on odd ones
-    for (auto& g : plan.groups) {
-      GemmLaunch gl = group_launch(g);
-      gl.scale = it == 0 ? reinterpret_cast<float*>(b + g.off_scale) : nullptr;
-      gl.gain = gram_gain;
-      gl.diag = gram_diag;
-      gl.out_fp16 = square;  // C (fp16) for POLY; P (bf16) for COMBINE when c = 0
+    for (size_t k = 0; k < plan.groups.size(); ++k) {
+      const NsGroup& g = plan.groups[k];
       const NsRClass& rcl = plan.rclasses[g.rclass];
-      const size_t ev = c->prof.begin(stream);
-      if ((e = launch_gram(odd ? g.mx1 : g.mx0, rcl.ma, g.base_slot, gl, stream)) != cudaSuccess)
-        return cuda_fail(c, e, "gram launch");
-      c->prof.end(ev, PRM_FAMILY_NS_GRAM, 1, 2.0 * g.count * double(g.r) * g.r * g.c, stream);
+      const NsMaps& cur = odd ? g.mx1 : g.mx0;
+      const NsMaps& nxt = odd ? g.mx0 : g.mx1;
+      const float* scale = it == 0 ? reinterpret_cast<const float*>(b + g.off_scale) : nullptr;
+      gram[k] = GemmSegSpec{&cur.x_rows128, &cur.x_rows128, &rcl.ma.store, scale, g.count, g.r, g.c, static_cast<int>(g.base_slot)};
+      const SymMaps& pm = square ? g.mb : g.ma;
+      comb[k] = GemmSegSpec{&pm.rows128, &cur.x_k64, &nxt.store, scale, g.count, g.r, g.c, 0};
     }
+    for (size_t k = 0; k < plan.rclasses.size(); ++k) {
+      const NsRClass& rcl = plan.rclasses[k];
+      poly[k] = GemmSegSpec{&rcl.ma.rows128, &rcl.ma.rows128, &rcl.mb.store, nullptr, rcl.count, rcl.r, rcl.r, 0};
+    }
+    size_t ev = c->prof.begin(stream);
+    if ((e = launch_gemm(GEMM_GRAM, gram.data(), static_cast<int>(gram.size()), gram_epi, stream)) != cudaSuccess)
+      return cuda_fail(c, e, "gram launch");
+    c->prof.end(ev, PRM_FAMILY_NS_GRAM, launches_for(gram.size()), gram_flops, stream);
     if (square) {
-      for (auto& rcl : plan.rclasses) {
-        GemmLaunch gl{};
-        gl.batch = rcl.count;
-        gl.r = rcl.r;
-        gl.c = rcl.r;
-        gl.ldc = rcl.ldr;
-        gl.ldr = rcl.ldr;
-        gl.gain = poly_gain;
-        gl.diag = poly_diag;
-        gl.in_fp16 = true;
-        gl.err = c->d_err;
-        gl.num_sms = c->num_sms;
-        const size_t ev = c->prof.begin(stream);
-        if ((e = launch_poly(rcl.ma, rcl.mb, gl, stream)) != cudaSuccess) return cuda_fail(c, e, "poly launch");
-        c->prof.end(ev, PRM_FAMILY_NS_POLY, 1, 2.0 * rcl.count * double(rcl.r) * rcl.r * rcl.r, stream);
-      }
+      ev = c->prof.begin(stream);
+      if ((e = launch_gemm(GEMM_POLY, poly.data(), static_cast<int>(poly.size()), poly_epi, stream)) != cudaSuccess)
+        return cuda_fail(c, e, "poly launch");
+      c->prof.end(ev, PRM_FAMILY_NS_POLY, launches_for(poly.size()), poly_flops, stream);
     }
-    for (auto& g : plan.groups) {
-      GemmLaunch gl = group_launch(g);
-      gl.scale = it == 0 ? reinterpret_cast<float*>(b + g.off_scale) : nullptr;
-      const size_t ev = c->prof.begin(stream);
-      if ((e = launch_combine(square ? g.mb : g.ma, odd ? g.mx1 : g.mx0, odd ? g.mx0 : g.mx1, gl, stream)) !=
-          cudaSuccess)
-        return cuda_fail(c, e, "combine launch");
-      c->prof.end(ev, PRM_FAMILY_NS_COMBINE, 1, 2.0 * g.count * double(g.r) * g.r * g.c, stream);
-    }
+    ev = c->prof.begin(stream);
+    if ((e = launch_gemm(GEMM_COMBINE, comb.data(), static_cast<int>(comb.size()), comb_epi, stream)) != cudaSuccess)
+      return cuda_fail(c, e, "combine launch");
+    c->prof.end(ev, PRM_FAMILY_NS_COMBINE, launches_for(comb.size()), gram_flops, stream);
   }
   // 3. W <- W (1 - lr wd) - eta s D, D = X_steps (transposed back for tall views)
   for (auto& g : plan.groups) {
@@ -964,19 +959,15 @@ int prm_ns_gram(const uint16_t* X, uint16_t* C, const float* scale, float gain, 
   SymMaps mc;
   if (encode_x_maps(&mx, X, batch, r, c, ldc) != 0 || encode_sym_maps(&mc, C, batch, r, ldr) != 0)
     return PRM_ERR_CUDA;
-  GemmLaunch g{};
-  g.batch = batch;
-  g.r = r;
-  g.c = c;
-  g.ldc = ldc;
-  g.ldr = ldr;
-  g.scale = scale;
-  g.gain = gain;
-  g.diag = diag;
-  g.out_fp16 = out_dtype == PRM_FP16;
-  g.err = ds->d_err;
-  g.num_sms = ds->num_sms;
-  return launch_gram(mx, mc, 0, g, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PRM_OK : PRM_ERR_CUDA;
+  GemmSegSpec seg{&mx.x_rows128, &mx.x_rows128, &mc.store, scale, batch, r, c, 0};
+  GemmEpilogue epi;
+  epi.gain = gain;
+  epi.diag = diag;
+  epi.out_fp16 = out_dtype == PRM_FP16;
+  epi.err = ds->d_err;
+  epi.num_sms = ds->num_sms;
+  return launch_gemm(GEMM_GRAM, &seg, 1, epi, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PRM_OK
+                                                                                              : PRM_ERR_CUDA;
 }
 
 int prm_ns_poly(const uint16_t* C, uint16_t* P, float gain, float diag, int in_dtype, int batch, int64_t r,
@@ -992,18 +983,15 @@ int prm_ns_poly(const uint16_t* C, uint16_t* P, float gain, float diag, int in_d
   SymMaps mc, mp;
   if (encode_sym_maps(&mc, C, batch, r, ldr) != 0 || encode_sym_maps(&mp, P, batch, r, ldr) != 0)
     return PRM_ERR_CUDA;
-  GemmLaunch g{};
-  g.batch = batch;
-  g.r = r;
-  g.c = r;
-  g.ldc = ldr;
-  g.ldr = ldr;
-  g.gain = gain;
-  g.diag = diag;
-  g.in_fp16 = in_dtype == PRM_FP16;
-  g.err = ds->d_err;
-  g.num_sms = ds->num_sms;
-  return launch_poly(mc, mp, g, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PRM_OK : PRM_ERR_CUDA;
+  GemmSegSpec seg{&mc.rows128, &mc.rows128, &mp.store, nullptr, batch, r, r, 0};
+  GemmEpilogue epi;
+  epi.gain = gain;
+  epi.diag = diag;
+  epi.in_fp16 = in_dtype == PRM_FP16;
+  epi.err = ds->d_err;
+  epi.num_sms = ds->num_sms;
+  return launch_gemm(GEMM_POLY, &seg, 1, epi, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PRM_OK
+                                                                                              : PRM_ERR_CUDA;
 }
 
 int prm_ns_combine(const uint16_t* X, const uint16_t* B, uint16_t* Xout, const float* scale, int batch, int64_t r,
@@ -1021,16 +1009,12 @@ int prm_ns_combine(const uint16_t* X, const uint16_t* B, uint16_t* Xout, const f
   if (encode_x_maps(&mx, X, batch, r, c, ldc) != 0 || encode_sym_maps(&mb, B, batch, r, ldr) != 0 ||
       encode_x_maps(&mo, Xout, batch, r, c, ldc) != 0)
     return PRM_ERR_CUDA;
-  GemmLaunch g{};
-  g.batch = batch;
-  g.r = r;
-  g.c = c;
-  g.ldc = ldc;
-  g.ldr = ldr;
-  g.scale = scale;
-  g.err = ds->d_err;
-  g.num_sms = ds->num_sms;
-  return launch_combine(mb, mx, mo, g, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PRM_OK : PRM_ERR_CUDA;
+  GemmSegSpec seg{&mb.rows128, &mx.x_k64, &mo.store, scale, batch, r, c, 0};
+  GemmEpilogue epi;
+  epi.err = ds->d_err;
+  epi.num_sms = ds->num_sms;
+  return launch_gemm(GEMM_COMBINE, &seg, 1, epi, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PRM_OK
+                                                                                                 : PRM_ERR_CUDA;
 }
 
 static void standalone_group(int batch, int64_t m, int64_t n, NsPlan& plan) {

@@ -141,7 +141,9 @@ def test_dit_1p3b_muonbp_sampled():
 def test_dit_15b_sampled():
     """15B-shaped set (192 matrices, 15.1 G parameters, ~151 GB of state plus
     the NS5 workspace): RowNorm steps on sampled vectors of every shape, and
-    the NS5 refresh checked on the square 5120 x 5120 matrix."""
+    the NS5 refresh checked on the square 5120 x 5120 matrix and on a tall
+    20480 x 5120 one (orthogonalised transposed; ~1.2e13 fp64 FLOPs in the
+    oracle)."""
     torch.cuda.empty_cache()
     free, _ = torch.cuda.mem_get_info()
     if free < 215e9:
@@ -150,7 +152,7 @@ def test_dit_15b_sampled():
     Ws, Ms, grads, opt = _setup(ms)
     rng = np.random.default_rng(1)
     _fill_grads(ms, grads, 0)
-    _check_ns_sampled(ms, Ws, Ms, grads, opt, 0, [1])
+    _check_ns_sampled(ms, Ws, Ms, grads, opt, 0, [1, 3])
     _fill_grads(ms, grads, 1)
     _check_rownorm_sampled(ms, Ws, Ms, grads, opt, 1, rng, k=4)
     opt.close()
