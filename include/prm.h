@@ -177,7 +177,8 @@ PRM_API int prm_sync_status(prm_ctx* ctx, void* stream);
  * Fig. 4), before the step size s * eta is applied. D is recomputed from the
  * matrix's momentum with the step's own kernels, so the momentum must still
  * hold M_t: call it before the next step and before anything else writes the
- * momentum. The NS5 directions equal the ones the step applied bit for bit;
+ * momentum. The NS5 directions are recomputed by the step's own (deterministic)
+ * kernels from the same momentum, so they are the bf16 values the step applied;
  * the RowNorm direction is the fp32 quotient M / max(||v||, eps), which the
  * step folds into one coefficient with s * eta. Synchronises the device,
  * allocates and frees its own scratch (the matrix's size twice, plus the NS5
