@@ -33,17 +33,19 @@
 // bytes read from shared memory and L2 for a given number of FLOPs, and it
 // leaves room for a 6-stage TMA ring.
 //
-// CTA layout (192 threads, one CTA per SM):
+// CTA layout (320 threads, one CTA per SM):
 //   warp 0     : TMA producer (one lane): per stage a 128x64 A tile and a
 //                128-row (N) slice of B, 128-byte swizzle; completion counted
 //                on the even CTA's barrier
 //   warp 1     : TMEM allocation for the pair (512 columns: two 128x256 fp32
 //                accumulators); in the even CTA one lane issues the MMAs
-//   warps 2..5 : epilogue -- tcgen05.ld of this CTA's 128 accumulator rows
-//                (one TMEM lane = one output row per thread), fused scaling
-//                and diagonal shift, bf16 results staged per 32 x 32 box in
-//                shared memory and written by TMA stores (plus the
-//                transposed box for the mirrored half of symmetric outputs)
+//   warps 2..9 : epilogue -- tcgen05.ld of this CTA's 128 accumulator rows
+//                (one TMEM lane = one output row per thread; warp w reads
+//                lane quarter w % 4, warps 2-5 the tile's left 128 columns,
+//                warps 6-9 the right ones), fused scaling and diagonal
+//                shift, 16-bit results staged per 32 x 32 box in shared
+//                memory and written by TMA stores (plus the transposed box
+//                for the mirrored half of symmetric outputs)
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -73,20 +75,20 @@ constexpr uint32_t B_TILE_BYTES = BN_HALF * BK * 2;  // 16 KB
 constexpr uint32_t STAGE_BYTES = A_TILE_BYTES + B_TILE_BYTES;
 constexpr uint32_t PAIR_STAGE_BYTES = 2 * STAGE_BYTES;  // what the even CTA's full barrier expects
 constexpr uint32_t MN_CHUNK_BYTES = 64 * BK * 2;        // one 64-column MN-major box of the B operand
-constexpr int NUM_THREADS = 192;
-constexpr int EPI_WARPS = 4;
+constexpr int NUM_THREADS = 320;
+constexpr int EPI_WARPS = 8;     // two per TMEM lane quarter, each taking half of a tile's columns
 constexpr uint32_t TMEM_COLS = 2 * BN;
 constexpr size_t BARRIER_BYTES = 256;
-// Epilogue staging: per epilogue warp four 32 x 32 bf16 boxes (64-byte rows;
-// two for the tile's own chunks, two for the mirrored ones, used in
-// alternation) from which TMA stores write the output. The boxes follow the
+// Epilogue staging: per epilogue warp two 32 x 32 16-bit boxes (64-byte rows;
+// one for the tile's own chunk, one for its mirror) from which TMA stores
+// write the output. The boxes follow the
 // output maps' 64-byte swizzle: the 16-byte chunk c of box row rho sits at
 // chunk c ^ ((rho >> 1) & 3) (address bits [5:4] ^= bits [8:7] of a
 // 512-byte aligned box), which also keeps the row-per-lane writes free of
 // bank conflicts.
 constexpr int STAGE_ROW_BYTES = 64;
 constexpr uint32_t EPI_BUF_BYTES = 32 * STAGE_ROW_BYTES;
-constexpr uint32_t EPI_WARP_BYTES = 4 * EPI_BUF_BYTES;
+constexpr uint32_t EPI_WARP_BYTES = 2 * EPI_BUF_BYTES;
 constexpr size_t EPI_SMEM_BYTES = EPI_WARPS * EPI_WARP_BYTES;
 constexpr size_t SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + EPI_SMEM_BYTES + BARRIER_BYTES;
 static_assert(SMEM_BYTES <= 232448, "dynamic shared memory above the 227 KB per-block limit");
@@ -185,13 +187,13 @@ __device__ __forceinline__ uint32_t stage_off(int row, int chunk) {
   return static_cast<uint32_t>(row * STAGE_ROW_BYTES + ((chunk ^ ((row >> 1) & 3)) << 4));
 }
 
-// One tile's epilogue for this warp's 32 accumulator rows. `nchunk` counts
-// the warp's chunks across tiles: its parity picks the staging boxes, whose
-// previous stores (two chunks back) must have read them before they are
-// rewritten.
+// One tile's epilogue for this warp's 32 accumulator rows and its half of
+// the columns (chunks qbase .. qbase + 3). The warp's two staging boxes
+// (direct, mirrored) are rewritten only after its previous stores have read
+// them.
 template <int KIND>
 __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const Segment& sg, const TileCoord& tc, int i,
-                                              uint32_t t_row, uint8_t* stage, int lane, uint32_t& nchunk) {
+                                              uint32_t t_row, uint8_t* stage, int lane, int qbase) {
   const int i0 = i - lane;  // first output row of this warp
   const CUtensorMap* tm_out = &sg.mapOut;
   float s = 1.f;
@@ -205,7 +207,8 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const Segment
   const bool rows_in = i0 < sg.M;  // warp-uniform
 
 #pragma unroll
-  for (int q = 0; q < EPI_CHUNKS; ++q) {
+  for (int qq = 0; qq < EPI_CHUNKS / 2; ++qq) {
+    const int q = qbase + qq;
     const int j0 = tc.n0 + q * 32;
     if (j0 < sg.N) {  // uniform over the warp: depends on the tile only
       float v[32];
@@ -222,10 +225,9 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const Segment
       for (int h = 0; h < 16; ++h)
         w[h] = p.out_fp16 ? pack_f16x2(v[2 * h], v[2 * h + 1]) : pack_bf16x2(v[2 * h], v[2 * h + 1]);
       const bool mirror = KIND != GEMM_COMBINE && tc.mirror;
-      uint8_t* bd = stage + (nchunk & 1u) * EPI_BUF_BYTES;
-      uint8_t* bm = stage + (2u + (nchunk & 1u)) * EPI_BUF_BYTES;
-      ++nchunk;
-      if (lane == 0) bulk_wait_group_read<1>();
+      uint8_t* bd = stage;
+      uint8_t* bm = stage + EPI_BUF_BYTES;
+      if (lane == 0) bulk_wait_group_read<0>();
       __syncwarp();
       // this lane's row i, columns j0 .. j0 + 31
 #pragma unroll
@@ -406,8 +408,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     }
   } else {
     const int quarter = warp & 3;  // TMEM lanes [32 * quarter, 32 * quarter + 32) belong to this warp
-    uint8_t* stage = sEpi + quarter * EPI_WARP_BYTES;
-    uint32_t nchunk = 0;
+    const int ew = warp - 2;                         // epilogue warp 0..7
+    const int qbase = (ew >> 2) * (EPI_CHUNKS / 2);  // first 32-column chunk of this warp's half
+    uint8_t* stage = sEpi + ew * EPI_WARP_BYTES;
     if (lane == 0)
       for (int q = 0; q < p.nseg; ++q) tma_prefetch_desc(&p.seg[q].mapOut);
     const uint32_t tempty_even = mapa_shared(smem_u32(&tempty_bar[0]), 0);
@@ -421,7 +424,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       if (!__all_sync(0xffffffffu, got)) break;
       tc_fence_after_sync();
       const uint32_t t_row = tmem_base + static_cast<uint32_t>(acc * BN) + (static_cast<uint32_t>(quarter * 32) << 16);
-      epilogue_tile<KIND>(p, sg, tc, i, t_row, stage, lane, nchunk);
+      epilogue_tile<KIND>(p, sg, tc, i, t_row, stage, lane, qbase);
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive_remote(tempty_even + static_cast<uint32_t>(acc * sizeof(uint64_t)));
