@@ -237,15 +237,15 @@ PRM_API int prm_adamw_step(float* param, float* exp_avg, float* exp_avg_sq, cons
  * work is accumulated: dense bf16 FLOPs for the GEMM families (2 r^2 c for
  * GRAM and COMBINE, 2 r^3 for POLY per matrix), bytes for the memory-bound
  * ones (RowNorm 18 B per parameter with bf16 gradients, 20 B with fp32;
- * prep 12 / 14 B; apply 10 B). Families: */
+ * prep 12 / 14 B). The refresh's parameter update runs in the epilogue of
+ * the last COMBINE launch and is timed with it. Families: */
 #define PRM_FAMILY_ROWNORM_WIDE 0
 #define PRM_FAMILY_ROWNORM_TALL 1
 #define PRM_FAMILY_NS_PREP      2
 #define PRM_FAMILY_NS_GRAM      3
 #define PRM_FAMILY_NS_POLY      4
 #define PRM_FAMILY_NS_COMBINE   5
-#define PRM_FAMILY_NS_APPLY     6
-#define PRM_FAMILY_COUNT        7
+#define PRM_FAMILY_COUNT        6
 
 /* enable = 1 clears the records and starts recording; 0 stops. */
 PRM_API int prm_profile(prm_ctx* ctx, int enable);

@@ -61,12 +61,6 @@ cudaError_t launch_prep(const View* d_views, int count, int64_t rows, int64_t co
 cudaError_t launch_norm_finish(const float* partials, int64_t slots, float* scale, int count, float ns_eps,
                                cudaStream_t stream);
 
-// W <- W * decay - eta * shape_scale * D, D read from X (bf16, transposed
-// back for tall views). With W == nullptr in the view, writes D (fp32) to
-// the view's M pointer instead (standalone orthogonaliser).
-cudaError_t launch_apply(const View* d_views, int count, int64_t rows, int64_t cols, bool vec_ok,
-                         const uint16_t* X, int64_t ldc, int64_t x_mat_stride, float decay,
-                         float eta, cudaStream_t stream);
 
 
 // ---- tcgen05 GEMM stages of one NS5 round -------------------------------
@@ -100,6 +94,7 @@ struct GemmSegSpec {
   int batch;
   int64_t r, c;
   int out_z0;
+  const View* views = nullptr;  // COMBINE with apply: device views indexed by batch slot
 };
 
 // Launch-wide epilogue constants: GRAM / POLY write gain * acc + diag on the
@@ -108,6 +103,11 @@ struct GemmEpilogue {
   float gain = 1.f, diag = 0.f;
   bool in_fp16 = false;   // operands fp16 (POLY reading C) instead of bf16
   bool out_fp16 = false;  // output packed as fp16 (GRAM writing C) instead of bf16
+  // COMBINE of the last round: instead of storing X' = D, apply it to the
+  // segment's views, W <- W * decay - eta * shape_scale * D (transposed back
+  // for tall views), or D into `out` for views without W
+  bool apply = false;
+  float decay = 1.f, eta = 0.f;
   int* err = nullptr;     // device error word
   int num_sms = 0;
 };

@@ -112,6 +112,7 @@ struct Segment {
   int nb;              // GRAM/POLY: ceil(M / 256) super-blocks per side
   int tiles_per_mat;
   int out_z0;          // first matrix of the output map this segment writes
+  const View* views;   // COMBINE of the last round: the segment's views by batch slot
 };
 
 struct GemmParams {
@@ -121,6 +122,8 @@ struct GemmParams {
   float gain, diag;     // GRAM / POLY: out = gain * (scale^2) * acc + diag * [i == j]
   int in_fp16;          // operands are fp16 (POLY reading C); else bf16
   int out_fp16;         // output is packed as fp16 (GRAM writing C); else bf16
+  int apply;            // COMBINE: apply D = X' to the views' W instead of storing X'
+  float decay, eta;     // apply: W <- W * decay - eta * shape_scale * D
   int* err;
   uint64_t timeout_ns;
 };
@@ -187,13 +190,129 @@ __device__ __forceinline__ uint32_t stage_off(int row, int chunk) {
   return static_cast<uint32_t>(row * STAGE_ROW_BYTES + ((chunk ^ ((row >> 1) & 3)) << 4));
 }
 
+// ---- last round: D = X5 applied to W in the COMBINE epilogue -------------
+// (the parameter update of the refresh, W <- W (1 - lr wd) - eta s D, with D
+// the bf16 X5 as the separate update pass would read it). Wide views update
+// W in X's orientation, 8 rows x 128 contiguous bytes per instruction (D
+// from the staged box); tall views store X transposed, so lane = W column
+// and every instruction covers one W row segment of 128 bytes. A warp
+// loads the W values of its next chunk before it works on the current one,
+// so their latency overlaps the current chunk's TMEM load and arithmetic.
+
+struct ApplyTarget {
+  float* dst;    // W, or the D output of a view without W (orthogonaliser only)
+  int64_t ld;
+  float step;    // eta * shape_scale
+  bool tall;
+  bool upd;      // dst is W (update) rather than D's output
+  bool vec;      // 16-byte aligned rows (wide views)
+};
+
+__device__ __forceinline__ ApplyTarget apply_target(const GemmParams& p, const View* views, int mat) {
+  const View* v = views + mat;
+  ApplyTarget t;
+  float* W = v->W;
+  t.upd = W != nullptr;
+  t.dst = t.upd ? W : v->out;
+  t.ld = v->ld;
+  t.step = p.eta * v->shape_scale;
+  t.tall = v->rows > v->cols;
+  t.vec = (t.ld % 4 == 0) && ((reinterpret_cast<uintptr_t>(t.dst) & 15u) == 0);
+  return t;
+}
+
+__device__ __forceinline__ float bf16_half(uint32_t word, int hi) {
+  return __uint_as_float(hi ? (word & 0xFFFF0000u) : (word << 16));
+}
+
+// W values of the chunk (rows i0.., columns j0.. of X): wide views in the
+// 8-rows-per-instruction layout (value 8 * it + e: row i0 + 8 it + lane / 4,
+// column j0 + 8 (lane % 4) + e), tall views as W[j0 + k][i0 + lane] (value
+// k). Out-of-range values are 0 and never stored.
+__device__ __forceinline__ void apply_load(const ApplyTarget& t, int M, int N, int i0, int j0, int lane,
+                                           float (&wv)[32]) {
+  if (!t.upd) return;
+  if (!t.tall) {
+    const int j = j0 + 8 * (lane & 3);
+#pragma unroll
+    for (int it = 0; it < 4; ++it) {
+      const int i = i0 + 8 * it + (lane >> 2);
+      const float* row = t.dst + static_cast<int64_t>(i) * t.ld + j;
+      if (i < M && t.vec && j + 8 <= N) {
+        const float4 a = *reinterpret_cast<const float4*>(row);
+        const float4 b = *reinterpret_cast<const float4*>(row + 4);
+        wv[8 * it + 0] = a.x;
+        wv[8 * it + 1] = a.y;
+        wv[8 * it + 2] = a.z;
+        wv[8 * it + 3] = a.w;
+        wv[8 * it + 4] = b.x;
+        wv[8 * it + 5] = b.y;
+        wv[8 * it + 6] = b.z;
+        wv[8 * it + 7] = b.w;
+      } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) wv[8 * it + e] = (i < M && j + e < N) ? row[e] : 0.f;
+      }
+    }
+  } else {
+    const int i = i0 + lane;
+#pragma unroll
+    for (int k = 0; k < 32; ++k)
+      wv[k] = (i < M && j0 + k < N) ? t.dst[static_cast<int64_t>(j0 + k) * t.ld + i] : 0.f;
+  }
+}
+
+__device__ __forceinline__ void apply_store(const GemmParams& p, const ApplyTarget& t, int M, int N, int i0, int j0,
+                                            int lane, const float (&wv)[32], const uint8_t* box,
+                                            const uint32_t (&w)[16]) {
+  if (!t.tall) {
+    const int c4 = lane & 3;
+    const int j = j0 + 8 * c4;
+#pragma unroll
+    for (int it = 0; it < 4; ++it) {
+      const int rho = 8 * it + (lane >> 2);
+      const int i = i0 + rho;
+      if (i >= M) continue;
+      const uint4 u = *reinterpret_cast<const uint4*>(box + stage_off(rho, c4));
+      const uint32_t uw[4] = {u.x, u.y, u.z, u.w};
+      float o[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const float d = bf16_half(uw[e >> 1], e & 1);
+        o[e] = t.upd ? fmaf(wv[8 * it + e], p.decay, -t.step * d) : d;
+      }
+      float* row = t.dst + static_cast<int64_t>(i) * t.ld + j;
+      if (t.vec && j + 8 <= N) {
+        *reinterpret_cast<float4*>(row) = make_float4(o[0], o[1], o[2], o[3]);
+        *reinterpret_cast<float4*>(row + 4) = make_float4(o[4], o[5], o[6], o[7]);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+          if (j + e < N) row[e] = o[e];
+      }
+    }
+  } else {
+    const int i = i0 + lane;
+    if (i < M) {
+#pragma unroll
+      for (int k = 0; k < 32; ++k) {
+        if (j0 + k < N) {
+          const float d = bf16_half(w[k >> 1], k & 1);
+          t.dst[static_cast<int64_t>(j0 + k) * t.ld + i] = t.upd ? fmaf(wv[k], p.decay, -t.step * d) : d;
+        }
+      }
+    }
+  }
+}
+
 // One tile's epilogue for this warp's 32 accumulator rows and its half of
 // the columns (chunks qbase .. qbase + 3). The warp's two staging boxes
 // (direct, mirrored) are rewritten only after its previous stores have read
 // them.
 template <int KIND>
 __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const Segment& sg, const TileCoord& tc, int i,
-                                              uint32_t t_row, uint8_t* stage, int lane, int qbase) {
+                                              uint32_t t_row, uint8_t* stage, int lane, int qbase,
+                                              const ApplyTarget& at, float (&weven)[32], float (&wodd)[32]) {
   const int i0 = i - lane;  // first output row of this warp
   const CUtensorMap* tm_out = &sg.mapOut;
   float s = 1.f;
@@ -241,6 +360,17 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const Segment
         for (int k = 0; k < 32; ++k)
           *reinterpret_cast<uint16_t*>(bm + stage_off(k, lane >> 3) + (lane & 7) * 2) =
               static_cast<uint16_t>(w[k >> 1] >> ((k & 1) * 16));
+      }
+      if (KIND == GEMM_COMBINE && p.apply) {
+        // this chunk's W values were loaded one chunk earlier (into the
+        // array of this chunk's parity); load the next chunk's into the other
+        float(&wcur)[32] = (qq & 1) ? wodd : weven;
+        float(&wnext)[32] = (qq & 1) ? weven : wodd;
+        if (qq + 1 < EPI_CHUNKS / 2) apply_load(at, sg.M, sg.N, i0, j0 + 32, lane, wnext);
+        __syncwarp();
+        if (rows_in) apply_store(p, at, sg.M, sg.N, i0, j0, lane, wcur, bd, w);
+        __syncwarp();
+        continue;
       }
       fence_proxy_async_smem();
       __syncwarp();
@@ -420,11 +550,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       const Segment& sg = p.seg[seg_of(p, tile)];
       const TileCoord tc = tile_coord<KIND>(sg, tile - sg.tile_begin);
       const int i = tc.m0 + static_cast<int>(rank) * BM + quarter * 32 + lane;
+      ApplyTarget at{};
+      float weven[32], wodd[32];
+      if (KIND == GEMM_COMBINE && p.apply) {
+        // the first chunk's W values load while the accumulator is computed
+        at = apply_target(p, sg.views, tc.mat);
+        apply_load(at, sg.M, sg.N, i - lane, tc.n0 + qbase * 32, lane, weven);
+      }
       const bool got = wait_bounded(&tfull_bar[acc], acc_phase, abort_flag, p.err, p.timeout_ns);
       if (!__all_sync(0xffffffffu, got)) break;
       tc_fence_after_sync();
       const uint32_t t_row = tmem_base + static_cast<uint32_t>(acc * BN) + (static_cast<uint32_t>(quarter * 32) << 16);
-      epilogue_tile<KIND>(p, sg, tc, i, t_row, stage, lane, qbase);
+      epilogue_tile<KIND>(p, sg, tc, i, t_row, stage, lane, qbase, at, weven, wodd);
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive_remote(tempty_even + static_cast<uint32_t>(acc * sizeof(uint64_t)));
@@ -562,6 +699,9 @@ cudaError_t launch_gemm(GemmKind kind, const GemmSegSpec* specs, int count, cons
     p.diag = epi.diag;
     p.in_fp16 = epi.in_fp16 ? 1 : 0;
     p.out_fp16 = epi.out_fp16 ? 1 : 0;
+    p.apply = (kind == GEMM_COMBINE && epi.apply) ? 1 : 0;
+    p.decay = epi.decay;
+    p.eta = epi.eta;
     p.err = epi.err;
     p.timeout_ns = WAIT_LIMIT_NS;
     int64_t tiles = 0;
@@ -572,6 +712,7 @@ cudaError_t launch_gemm(GemmKind kind, const GemmSegSpec* specs, int count, cons
       sg.mapB = *g.b;
       sg.mapOut = *g.out;
       sg.scale = g.scale;
+      sg.views = g.views;
       sg.tile_begin = tiles;
       sg.out_z0 = g.out_z0;
       if (kind == GEMM_COMBINE) {

@@ -61,6 +61,7 @@ struct NsGroup {
   NsMaps mx0{}, mx1{};
   SymMaps mb{};  // this group's slice of the r-class B array (P; COMBINE operand)
   SymMaps ma{};  // this group's slice of the r-class A array (P when POLY is skipped, c = 0)
+  View* d_slot_views = nullptr;  // device: the group's views by slot (the last COMBINE applies D through them)
 };
 
 // All matrices with the same short side r: their A = X X^T and
@@ -95,7 +96,11 @@ void free_sets(std::vector<LaunchSet>& sets) {
 }
 
 void free_plan(NsPlan& p) {
-  for (auto& g : p.groups) free_sets(g.sets);
+  for (auto& g : p.groups) {
+    free_sets(g.sets);
+    if (g.d_slot_views) cudaFree(g.d_slot_views);
+    g.d_slot_views = nullptr;
+  }
   p.groups.clear();
   p.bytes = 0;
 }
@@ -109,6 +114,19 @@ cudaError_t upload_sets(std::vector<LaunchSet>& sets) {
     if ((e = cudaMemcpy(s.d_views, s.views.data(), b, cudaMemcpyHostToDevice)) != cudaSuccess) return e;
   }
   return cudaSuccess;
+}
+
+// Uploads a group's launch tables: the per-shape sets (prep kernels) and the
+// slot-indexed view table through which the last COMBINE round applies D.
+cudaError_t upload_group(NsGroup& g) {
+  cudaError_t e = upload_sets(g.sets);
+  if (e != cudaSuccess) return e;
+  std::vector<View> by_slot(static_cast<size_t>(g.count));
+  for (const auto& st : g.sets)
+    for (const View& v : st.views) by_slot[static_cast<size_t>(v.slot)] = v;
+  const size_t bytes = by_slot.size() * sizeof(View);
+  if ((e = cudaMalloc(reinterpret_cast<void**>(&g.d_slot_views), bytes)) != cudaSuccess) return e;
+  return cudaMemcpy(g.d_slot_views, by_slot.data(), bytes, cudaMemcpyHostToDevice);
 }
 
 bool view_vec_ok(const View& v) {
@@ -493,22 +511,17 @@ int run_ns(prm_ctx* c, NsPlan& plan, void* base, bool update_momentum, float bet
         return cuda_fail(c, e, "poly launch");
       c->prof.end(ev, PRM_FAMILY_NS_POLY, launches_for(poly.size()), poly_flops, stream);
     }
+    // 3. the last round applies D = X_steps instead of storing it:
+    // W <- W (1 - lr wd) - eta s D, transposed back for tall views
+    const bool last = it == steps - 1;
+    comb_epi.apply = last;
+    comb_epi.decay = decay;
+    comb_epi.eta = eta;
+    for (size_t k = 0; k < plan.groups.size(); ++k) comb[k].views = last ? plan.groups[k].d_slot_views : nullptr;
     ev = c->prof.begin(stream);
     if ((e = launch_gemm(GEMM_COMBINE, comb.data(), static_cast<int>(comb.size()), comb_epi, stream)) != cudaSuccess)
       return cuda_fail(c, e, "combine launch");
     c->prof.end(ev, PRM_FAMILY_NS_COMBINE, launches_for(comb.size()), gram_flops, stream);
-  }
-  // 3. W <- W (1 - lr wd) - eta s D, D = X_steps (transposed back for tall views)
-  for (auto& g : plan.groups) {
-    const uint16_t* fin = reinterpret_cast<const uint16_t*>(b + ((steps & 1) ? g.off_x1 : g.off_x0));
-    const size_t ev = c->prof.begin(stream);
-    for (auto& s : g.sets) {
-      e = launch_apply(s.d_views, static_cast<int>(s.views.size()), s.rows, s.cols, s.vec_ok, fin, g.ldc,
-                       g.r * g.ldc, decay, eta, stream);
-      if (e != cudaSuccess) return cuda_fail(c, e, "apply launch");
-    }
-    c->prof.end(ev, PRM_FAMILY_NS_APPLY, static_cast<int>(g.sets.size()),
-                static_cast<double>(g.count) * g.r * g.c * 10.0, stream);
   }
   return PRM_OK;
 }
@@ -682,7 +695,7 @@ int prm_register_matrices(prm_ctx* c, const prm_matrix_desc* d, int count, int m
   for (auto* plans : {&c->ns_full, &c->ns_blocks})
     for (auto& p : *plans)
       for (auto& g : p.groups)
-        if (e == cudaSuccess) e = upload_sets(g.sets);
+        if (e == cudaSuccess) e = upload_group(g);
   if (e != cudaSuccess) {
     clear_registration(c);
     return cuda_fail(c, e, "uploading launch tables");
@@ -866,7 +879,7 @@ int prm_debug_last_direction(prm_ctx* c, int idx, float* host_out) {
     NsPlan plan;
     build_ns_plan(parts, plan);
     for (auto& g : plan.groups) {
-      if ((e = upload_sets(g.sets)) != cudaSuccess) {
+      if ((e = upload_group(g)) != cudaSuccess) {
         free_plan(plan);
         return finish(cuda_fail(c, e, "uploading launch tables"));
       }
@@ -1068,7 +1081,7 @@ int prm_newton_schulz(const float* in, float* out, int batch, int64_t m, int64_t
   }
   build_ns_plan(views, plan);
   if (workspace == nullptr || ws_bytes < plan.bytes) return PRM_ERR_WORKSPACE;
-  if (upload_sets(plan.groups[0].sets) != cudaSuccess) {
+  if (upload_group(plan.groups[0]) != cudaSuccess) {
     free_plan(plan);
     return PRM_ERR_CUDA;
   }

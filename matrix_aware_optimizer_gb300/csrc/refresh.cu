@@ -9,8 +9,8 @@
 //            epilogue multiplies by its square and the first COMBINE epilogue
 //            by the scale itself, which is the same NS5 round on M / ||M||.
 //   finish : per-view scale = 1 / (sqrt(sum of partials) + eps_ns).
-//   apply  : W <- W * (1 - lr wd) - eta * s * D with D = X5 (bf16), read
-//            transposed back for tall views.
+//   (the update W <- W (1 - lr wd) - eta s D, D = X5, runs in the epilogue
+//   of the last NS5 round's COMBINE launch, see ns5_gemm.cu)
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -234,119 +234,6 @@ __global__ void __launch_bounds__(256) norm_finish_kernel(const float* __restric
   if (threadIdx.x == 0) scale[blockIdx.x] = 1.f / (sqrtf(total) + ns_eps);
 }
 
-// ---------------------------------------------------------------- apply
-template <bool VEC>
-__global__ void __launch_bounds__(PREP_THREADS) apply_wide_kernel(const View* __restrict__ views, int64_t cols,
-                                                                  const uint16_t* __restrict__ X, int64_t ldc,
-                                                                  int64_t x_stride, float decay, float eta) {
-  const View v = views[blockIdx.y];
-  const int64_t row = blockIdx.x;
-  const uint16_t* Xr = X + v.slot * x_stride + row * ldc;
-  const float step = eta * v.shape_scale;
-  if (v.W == nullptr) {
-    float* Or = v.out + row * v.ld;
-    for (int64_t c = threadIdx.x; c < cols; c += PREP_THREADS) Or[c] = bf16_to_float(Xr[c]);
-    return;
-  }
-  float* Wr = v.W + row * v.ld;
-  if constexpr (VEC) {
-    for (int64_t c = threadIdx.x * 4; c < cols; c += PREP_THREADS * 4) {
-      const uint2 u = *reinterpret_cast<const uint2*>(Xr + c);
-      float4 w = *reinterpret_cast<const float4*>(Wr + c);
-      w.x = fmaf(w.x, decay, -step * bf16_to_float(u.x & 0xFFFFu));
-      w.y = fmaf(w.y, decay, -step * bf16_to_float(u.x >> 16));
-      w.z = fmaf(w.z, decay, -step * bf16_to_float(u.y & 0xFFFFu));
-      w.w = fmaf(w.w, decay, -step * bf16_to_float(u.y >> 16));
-      *reinterpret_cast<float4*>(Wr + c) = w;
-    }
-  } else {
-    for (int64_t c = threadIdx.x; c < cols; c += PREP_THREADS) Wr[c] = fmaf(Wr[c], decay, -step * bf16_to_float(Xr[c]));
-  }
-}
-
-// Tall views: W[i][j] -= step * X[j][i]. X rows arrive as 32-byte pieces
-// (four threads per row of the 64 x 64 tile), are transposed in shared
-// memory, and W is updated with all its loads issued before the stores.
-template <bool VEC>
-__global__ void __launch_bounds__(PREP_THREADS) apply_tall_kernel(const View* __restrict__ views, int64_t rows,
-                                                                  int64_t cols, const uint16_t* __restrict__ X,
-                                                                  int64_t ldc, int64_t x_stride, float decay,
-                                                                  float eta) {
-  __shared__ float tile[TILE][TILE + 1];
-  const View v = views[blockIdx.z];
-  const int tid = threadIdx.x;
-  const int64_t i0 = static_cast<int64_t>(blockIdx.y) * TILE;
-  const int64_t j0 = static_cast<int64_t>(blockIdx.x) * TILE;
-  const uint16_t* Xv = X + v.slot * x_stride;
-  {
-    const int jj = tid >> 2, ic = (tid & 3) * 16;
-    const int64_t j = j0 + jj, ib = i0 + ic;
-    if (j < cols && ib + 16 <= rows) {
-      const uint4* src = reinterpret_cast<const uint4*>(Xv + j * ldc + ib);
-      const uint4 a = src[0], b = src[1];
-      const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-#pragma unroll
-      for (int h = 0; h < 8; ++h) {
-        tile[ic + 2 * h][jj] = bf16_to_float(w[h] & 0xFFFFu);
-        tile[ic + 2 * h + 1][jj] = bf16_to_float(w[h] >> 16);
-      }
-    } else {
-#pragma unroll
-      for (int k = 0; k < 16; ++k)
-        tile[ic + k][jj] = (j < cols && ib + k < rows) ? bf16_to_float(Xv[j * ldc + ib + k]) : 0.f;
-    }
-  }
-  __syncthreads();
-  const float step = eta * v.shape_scale;
-  if constexpr (VEC) {
-    const int tx = tid & 15, ty = tid >> 4;
-    const int64_t j = j0 + tx * 4;
-    float4 w[4];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int64_t i = i0 + ty + 16 * k;
-      w[k] = (v.W != nullptr && i < rows && j < cols) ? *reinterpret_cast<const float4*>(v.W + i * v.ld + j)
-                                                       : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int64_t i = i0 + ty + 16 * k;
-      if (i < rows && j < cols) {
-        const float* d = &tile[ty + 16 * k][tx * 4];
-        if (v.W == nullptr) {
-          *reinterpret_cast<float4*>(v.out + i * v.ld + j) = make_float4(d[0], d[1], d[2], d[3]);
-        } else {
-          float4 o;
-          o.x = fmaf(w[k].x, decay, -step * d[0]);
-          o.y = fmaf(w[k].y, decay, -step * d[1]);
-          o.z = fmaf(w[k].z, decay, -step * d[2]);
-          o.w = fmaf(w[k].w, decay, -step * d[3]);
-          *reinterpret_cast<float4*>(v.W + i * v.ld + j) = o;
-        }
-      }
-    }
-  } else {
-    const int tx = tid & 63, ty = tid >> 6;
-    float w[16];
-#pragma unroll
-    for (int k = 0; k < 16; ++k) {
-      const int64_t i = i0 + ty + 4 * k, j = j0 + tx;
-      w[k] = (v.W != nullptr && i < rows && j < cols) ? v.W[i * v.ld + j] : 0.f;
-    }
-#pragma unroll
-    for (int k = 0; k < 16; ++k) {
-      const int64_t i = i0 + ty + 4 * k, j = j0 + tx;
-      if (i < rows && j < cols) {
-        const float d = tile[ty + 4 * k][tx];
-        if (v.W == nullptr)
-          v.out[i * v.ld + j] = d;
-        else
-          v.W[i * v.ld + j] = fmaf(w[k], decay, -step * d);
-      }
-    }
-  }
-}
-
 }  // namespace
 
 int64_t prep_slots(int64_t rows, int64_t cols) {
@@ -397,26 +284,6 @@ cudaError_t launch_norm_finish(const float* partials, int64_t slots, float* scal
                                cudaStream_t stream) {
   if (count == 0) return cudaSuccess;
   norm_finish_kernel<<<count, 256, 0, stream>>>(partials, slots, scale, ns_eps);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_apply(const View* d_views, int count, int64_t rows, int64_t cols, bool vec_ok, const uint16_t* X,
-                         int64_t ldc, int64_t x_mat_stride, float decay, float eta, cudaStream_t stream) {
-  if (count == 0) return cudaSuccess;
-  if (rows <= cols) {
-    const dim3 grid(static_cast<unsigned>(rows), static_cast<unsigned>(count));
-    if (vec_ok)
-      apply_wide_kernel<true><<<grid, PREP_THREADS, 0, stream>>>(d_views, cols, X, ldc, x_mat_stride, decay, eta);
-    else
-      apply_wide_kernel<false><<<grid, PREP_THREADS, 0, stream>>>(d_views, cols, X, ldc, x_mat_stride, decay, eta);
-  } else {
-    const dim3 grid(static_cast<unsigned>((cols + TILE - 1) / TILE), static_cast<unsigned>((rows + TILE - 1) / TILE),
-                    static_cast<unsigned>(count));
-    if (vec_ok)
-      apply_tall_kernel<true><<<grid, PREP_THREADS, 0, stream>>>(d_views, rows, cols, X, ldc, x_mat_stride, decay, eta);
-    else
-      apply_tall_kernel<false><<<grid, PREP_THREADS, 0, stream>>>(d_views, rows, cols, X, ldc, x_mat_stride, decay, eta);
-  }
   return cudaGetLastError();
 }
 

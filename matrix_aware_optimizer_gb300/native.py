@@ -27,8 +27,7 @@ PRM_FAMILY_NS_PREP = 2
 PRM_FAMILY_NS_GRAM = 3
 PRM_FAMILY_NS_POLY = 4
 PRM_FAMILY_NS_COMBINE = 5
-PRM_FAMILY_NS_APPLY = 6
-FAMILY_NAMES = ["rownorm_wide", "rownorm_tall", "ns_prep", "ns_gram", "ns_poly", "ns_combine", "ns_apply"]
+FAMILY_NAMES = ["rownorm_wide", "rownorm_tall", "ns_prep", "ns_gram", "ns_poly", "ns_combine"]
 
 PRM_FP32 = 0
 PRM_BF16 = 1
