@@ -1,7 +1,7 @@
-"""A whole K=3 PR-Muon cycle captured into a CUDA graph and replayed gives
-bit-for-bit the same state as running the steps directly: prm_step only
-enqueues kernels and asynchronous memsets on the caller's stream, and the
-branch of each position in the cycle is fixed by t mod K."""
+"""A whole K=3 PR-Muon (or MuonBP) cycle captured into a CUDA graph and
+replayed gives bit-for-bit the same state as running the steps directly:
+prm_step only enqueues kernels and asynchronous memsets on the caller's
+stream, and the branch of each position in the cycle is fixed by t mod K."""
 import pytest
 import torch
 
@@ -28,24 +28,25 @@ def _setup():
     return ms, Ws, Ms, grads
 
 
-def test_graph_replay_matches_direct_steps():
+@pytest.mark.parametrize("mode,blocks", [("prmuon", 0), ("muonbp", 4)])
+def test_graph_replay_matches_direct_steps(mode, blocks):
     ms, Wa, Ma, ga = _setup()
-    opt_a = PeriodicRowMuon(Wa, Ma, ga)
+    opt_a = PeriodicRowMuon(Wa, Ma, ga, muonbp_blocks=blocks)
     for t in range(9):
-        opt_a.step(t)
+        opt_a.step(t, mode=mode)
     opt_a.sync_status()
 
     ms, Wb, Mb, gb = _setup()
-    opt_b = PeriodicRowMuon(Wb, Mb, gb)
+    opt_b = PeriodicRowMuon(Wb, Mb, gb, muonbp_blocks=blocks)
     # first cycle directly (also warms up per-device set-up), then capture one cycle
     for t in range(3):
-        opt_b.step(t)
+        opt_b.step(t, mode=mode)
     torch.cuda.synchronize()
     g = torch.cuda.CUDAGraph()
     side = torch.cuda.Stream()
     with torch.cuda.graph(g, stream=side):
         for t in range(3, 6):
-            opt_b.step(t)
+            opt_b.step(t, mode=mode)
     # capture records without executing: two replays run cycles 2 and 3
     g.replay()
     g.replay()

@@ -18,7 +18,7 @@ from matrix_aware_optimizer_gb300 import native as N
 from matrix_aware_optimizer_gb300 import synth
 from matrix_aware_optimizer_gb300.optimizer import PeriodicRowMuon, newton_schulz
 
-from .gpu_helpers import direction_from_update, ensure_built, host64, rel_frob
+from .gpu_helpers import direction_from_update, ensure_built, host64, make_set, rel_frob
 
 pytestmark = pytest.mark.gpu
 
@@ -172,6 +172,16 @@ def test_edge_shapes_directions(gdtype):
                 assert rel_frob(Dg, Do) <= 1e-6, ((m, n), rel_frob(Dg, Do))
                 assert np.all(Dg[Do == 0] == 0)
         opt.close()
+
+
+def test_more_shape_groups_than_one_launch_holds():
+    """Nine distinct shapes make nine NS5 groups and nine r-classes: each GEMM
+    stage then runs as two launches (up to seven segments each), which must
+    give the same refresh as the oracle for every matrix."""
+    shapes = [(32 + 16 * k, 64 + 32 * k) for k in range(9)]
+    shapes[3] = (shapes[3][1], shapes[3][0])  # one tall matrix among them
+    ms = make_set(shapes, synth.GRAD_BF16, seed=17)
+    _run_teacher_forced(ms, steps=[0, 1])
 
 
 def test_muonbp_block_and_full_steps():
