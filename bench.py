@@ -53,7 +53,8 @@ def parse_args():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-adamw", action="store_true")
     p.add_argument("--workspace-limit-gb", type=float, default=0.0,
-                   help="cap the NS5 workspace (sequential sub-plans); 0 = no cap")
+                   help="cap the NS5 workspace (sequential sub-plans); 0 = the library's automatic policy, "
+                        "-1 = no cap")
     return p.parse_args()
 
 
@@ -385,8 +386,9 @@ def run_ours(args):
         synth.make_grad(s, ms.seed, 0, i, ms.grad_std, ms.grad_dtype, ms.row_sigma, device=dev, out=g)
         grads.append(g)
     torch.cuda.synchronize()
+    ws_limit = -1 if args.workspace_limit_gb < 0 else int(args.workspace_limit_gb * 2 ** 30)
     opt = PeriodicRowMuon(Ws, Ms, grads, muonbp_blocks=blocks,
-                          workspace_limit=int(args.workspace_limit_gb * 2 ** 30))
+                          workspace_limit=ws_limit)
     stream = torch.cuda.current_stream()
 
     def cycle(k, ev_ref=None):
@@ -543,7 +545,7 @@ def run_ours(args):
         for buf in extra:
             gl = [buf[offs[i]:offs[i] + s[0] * s[1]].view(s) for i, s in enumerate(ms.shapes)]
             opts.append(PeriodicRowMuon(Ws, Ms, gl, muonbp_blocks=blocks, workspace=opt.workspace,
-                                        workspace_limit=int(args.workspace_limit_gb * 2 ** 30)))
+                                        workspace_limit=ws_limit))
         bufs = list(zip([gflat] + extra, opts))
         out_row = torch.empty(ms.shapes[0][1], dtype=torch.float32).pin_memory()
         d2h = out_row.numel() * 4
@@ -673,7 +675,10 @@ def run_ours(args):
                    "muonbp_blocks": blocks, "grad_dtype": ms.grad_dtype,
                    "l2": "inputs larger than L2 (no flush)", "parallelism": f"replicas x{world}",
                    "step": "one K=3 cycle: refresh + 2 cheap steps",
-                   "workspace_gb": round(opt.workspace_bytes / 2 ** 30, 2)},
+                   "workspace_gb": round(opt.workspace_bytes / 2 ** 30, 2),
+                   "workspace_policy": ("automatic" if args.workspace_limit_gb == 0 else
+                                        "no cap" if args.workspace_limit_gb < 0 else
+                                        f"cap {args.workspace_limit_gb} GiB")},
         "ms_refresh_step": round(refresh_ms, 3), "ms_cheap_step": round(cheap_ms, 3),
         "ns5_tflops": round(ns_flop / (ns_ms * 1e-3) / 1e12, 1) if ns_ms else None,
         "rownorm_gbs": round(rn_bytes / (rn_ms * 1e-3) / 1e9, 1) if rn_ms else None,

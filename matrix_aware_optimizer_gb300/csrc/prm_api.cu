@@ -205,16 +205,29 @@ void build_ns_plan(const std::vector<View>& views, NsPlan& plan) {
   plan.bytes = off;
 }
 
+// Automatic workspace policy (limit 0): a plan whose buffers would exceed
+// AUTO_SPLIT_ABOVE runs as sequential sub-plans of at most AUTO_SUBPLAN_BYTES.
+// Measured on the 15B-shaped set (75 GB as one plan): 3 / 10 / 40 GB
+// sub-plans run the K = 3 cycle 10 / 8.5 / 4 % faster than one plan, the SM
+// clock under the power cap rising as the per-launch working set shrinks;
+// on the 1.3B-shaped set (6 GB) splitting gains nothing, so plans below the
+// threshold stay whole (all groups in lockstep, POLY once per r-class).
+constexpr size_t AUTO_SPLIT_ABOVE = size_t(16) << 30;
+constexpr size_t AUTO_SUBPLAN_BYTES = size_t(4) << 30;
+
 // Splits the views into sequential sub-plans whose workspace fits `limit`
-// bytes (0: one plan for everything). Views are taken in (r, c) order so that
-// same-shape matrices stay together; a sub-plan holds at least one view.
+// bytes (SIZE_MAX: one plan for everything; 0: the automatic policy above).
+// Views are taken in (r, c) order so that same-shape matrices stay together;
+// a sub-plan holds at least one view.
 void build_ns_subplans(const std::vector<View>& views, size_t limit, std::vector<NsPlan>& out) {
   out.clear();
   if (views.empty()) return;
-  if (limit == 0) {
+  if (limit == 0 || limit == SIZE_MAX) {
     out.emplace_back();
     build_ns_plan(views, out.back());
-    return;
+    if (limit == SIZE_MAX || out.back().bytes <= AUTO_SPLIT_ABOVE) return;
+    out.clear();
+    limit = AUTO_SUBPLAN_BYTES;
   }
   std::vector<View> sorted = views;
   std::stable_sort(sorted.begin(), sorted.end(), [](const View& x, const View& y) {
@@ -303,7 +316,7 @@ struct prm_ctx {
   int blocks = 0;
   RowNormPlan rn;
   std::vector<NsPlan> ns_full, ns_blocks;  // sequential sub-plans (one unless a workspace cap splits them)
-  size_t ws_limit = 0;                     // prm_set_workspace_limit; 0 = no cap
+  size_t ws_limit = 0;                     // prm_set_workspace_limit; 0 = automatic, SIZE_MAX = no cap
   std::vector<View> full;                  // registered matrices, in registration order
   struct {
     bool valid = false;

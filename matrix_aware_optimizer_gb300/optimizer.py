@@ -24,8 +24,10 @@ class PeriodicRowMuon:
     muonbp_blocks    : 0, or P > 0 to also plan MuonBP blocks.
     shape_scales     : optional per-matrix step multipliers (default
                        sqrt(max(1, rows / cols))).
-    workspace_limit  : cap in bytes on the NS5 workspace (0 = none): the
-                       refresh then runs in sequential sub-plans that fit it.
+    workspace_limit  : cap in bytes on the NS5 workspace: the refresh then runs
+                       in sequential sub-plans that fit it. 0 (default) is the
+                       library's automatic policy (whole plans up to 16 GiB,
+                       4 GiB sub-plans above), -1 no cap.
     workspace        : optional uint8 CUDA tensor to use as the scratch instead
                        of allocating one (at least workspace_bytes large).
                        Optimizers whose steps are ordered on one stream may
@@ -65,7 +67,7 @@ class PeriodicRowMuon:
         with torch.cuda.device(dev):
             self.ctx = N.prm_create(dev.index if dev.index is not None else torch.cuda.current_device())
             try:
-                N.prm_set_workspace_limit(self.ctx, int(workspace_limit))
+                N.prm_set_workspace_limit(self.ctx, int(workspace_limit) if workspace_limit >= 0 else (1 << 64) - 1)
                 N.prm_register_matrices(self.ctx, descs, muonbp_blocks)
                 nbytes = N.prm_workspace_bytes(self.ctx)
                 if workspace is None:

@@ -38,7 +38,11 @@ def _run(limit, mode, blocks):
 
 @pytest.mark.parametrize("mode,blocks", [("prmuon", 0), ("muonbp", 4)])
 def test_capped_workspace_gives_identical_results(mode, blocks):
-    full, full_bytes = _run(0, mode, blocks)
+    full, full_bytes = _run(-1, mode, blocks)  # no cap: one plan
+    auto, auto_bytes = _run(0, mode, blocks)   # automatic: a set this small stays whole
+    assert auto_bytes == full_bytes
+    for x, y in zip(full, auto):
+        assert torch.equal(x, y)
     cap = full_bytes // 5
     capped, capped_bytes = _run(cap, mode, blocks)
     assert capped_bytes < full_bytes
