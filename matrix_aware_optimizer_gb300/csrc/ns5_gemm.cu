@@ -195,9 +195,10 @@ __device__ __forceinline__ uint32_t stage_off(int row, int chunk) {
 // the bf16 X5 as the separate update pass would read it). Wide views update
 // W in X's orientation, 8 rows x 128 contiguous bytes per instruction (D
 // from the staged box); tall views store X transposed, so lane = W column
-// and every instruction covers one W row segment of 128 bytes. A warp
-// loads the W values of its next chunk before it works on the current one,
-// so their latency overlaps the current chunk's TMEM load and arithmetic.
+// and every instruction covers one W row segment of 128 bytes. A warp loads
+// the W values of its first two chunks while the accumulator is computed,
+// and those of chunk q + 2 right after using chunk q's, so each load has a
+// whole chunk of work to hide behind.
 
 struct ApplyTarget {
   float* dst;    // W, or the D output of a view without W (orthogonaliser only)
@@ -362,13 +363,13 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const Segment
               static_cast<uint16_t>(w[k >> 1] >> ((k & 1) * 16));
       }
       if (KIND == GEMM_COMBINE && p.apply) {
-        // this chunk's W values were loaded one chunk earlier (into the
-        // array of this chunk's parity); load the next chunk's into the other
+        // this chunk's W values sit in the array of its parity (loaded two
+        // chunks earlier, or before the accumulator wait for the first two);
+        // once they are used, the array takes the values two chunks ahead
         float(&wcur)[32] = (qq & 1) ? wodd : weven;
-        float(&wnext)[32] = (qq & 1) ? weven : wodd;
-        if (qq + 1 < EPI_CHUNKS / 2) apply_load(at, sg.M, sg.N, i0, j0 + 32, lane, wnext);
         __syncwarp();
         if (rows_in) apply_store(p, at, sg.M, sg.N, i0, j0, lane, wcur, bd, w);
+        if (qq + 2 < EPI_CHUNKS / 2) apply_load(at, sg.M, sg.N, i0, j0 + 64, lane, wcur);
         __syncwarp();
         continue;
       }
@@ -553,9 +554,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       ApplyTarget at{};
       float weven[32], wodd[32];
       if (KIND == GEMM_COMBINE && p.apply) {
-        // the first chunk's W values load while the accumulator is computed
+        // the first two chunks' W values load while the accumulator is computed
         at = apply_target(p, sg.views, tc.mat);
         apply_load(at, sg.M, sg.N, i - lane, tc.n0 + qbase * 32, lane, weven);
+        apply_load(at, sg.M, sg.N, i - lane, tc.n0 + qbase * 32 + 32, lane, wodd);
       }
       const bool got = wait_bounded(&tfull_bar[acc], acc_phase, abort_flag, p.err, p.timeout_ns);
       if (!__all_sync(0xffffffffu, got)) break;
