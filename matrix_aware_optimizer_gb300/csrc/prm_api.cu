@@ -495,7 +495,9 @@ int run_ns(prm_ctx* c, NsPlan& plan, void* base, bool update_momentum, float bet
   for (const auto& g : plan.groups) gram_flops += 2.0 * g.count * double(g.r) * g.r * g.c;
   for (const auto& rcl : plan.rclasses) poly_flops += 2.0 * rcl.count * double(rcl.r) * rcl.r * rcl.r;
   std::vector<GemmSegSpec> gram(plan.groups.size()), comb(plan.groups.size()), poly(plan.rclasses.size());
-  auto launches_for = [](size_t segments) { return static_cast<int>((segments + GEMM_MAX_SEGMENTS - 1) / GEMM_MAX_SEGMENTS); };
+  auto launches_for = [](size_t segments) {
+    return static_cast<int>((segments + GEMM_MAX_SEGMENTS - 1) / GEMM_MAX_SEGMENTS);
+  };
   // 2. five rounds; each stage is one launch over every group (POLY: every
   // r-class), so a round is three launches however many shapes there are
   for (int it = 0; it < steps; ++it) {
@@ -506,7 +508,8 @@ int run_ns(prm_ctx* c, NsPlan& plan, void* base, bool update_momentum, float bet
       const NsMaps& cur = odd ? g.mx1 : g.mx0;
       const NsMaps& nxt = odd ? g.mx0 : g.mx1;
       const float* scale = it == 0 ? reinterpret_cast<const float*>(b + g.off_scale) : nullptr;
-      gram[k] = GemmSegSpec{&cur.x_rows128, &cur.x_rows128, &rcl.ma.store, scale, g.count, g.r, g.c, static_cast<int>(g.base_slot)};
+      gram[k] = GemmSegSpec{&cur.x_rows128, &cur.x_rows128, &rcl.ma.store, scale, g.count, g.r, g.c,
+                            static_cast<int>(g.base_slot)};
       const SymMaps& pm = square ? g.mb : g.ma;
       comb[k] = GemmSegSpec{&pm.rows128, &cur.x_k64, &nxt.store, scale, g.count, g.r, g.c, 0};
     }
