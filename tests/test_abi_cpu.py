@@ -80,7 +80,7 @@ def test_standalone_argument_checks(lib):
     assert lib.prm_newton_schulz_workspace(0, 4, 4, ctypes.byref(n)) == N.PRM_OK and n.value == 0
     assert lib.prm_newton_schulz_workspace(2, 0, 4, ctypes.byref(n)) == N.PRM_ERR_INVALID_ARG
     assert lib.prm_newton_schulz_workspace(3, 100, 40, ctypes.byref(n)) == N.PRM_OK
-    # wide orientation 40 x 100: two bf16 X buffers (pitch 104), two 40 x 40 (pitch 40) ...
+    # wide orientation 40 x 100: two bf16 X buffers (pitch >= 104), two 40 x 40 (pitch >= 40) ...
     assert n.value >= 3 * 40 * 104 * 2 * 2 + 3 * 40 * 40 * 2 * 2
 
 
