@@ -124,29 +124,35 @@ class ClockSampler:
             self.proc.kill()
         if self._t:
             self._t.join(timeout=2)
-        sm, mx, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        lines = self.lines
-        if self.window is not None:
-            inside = [x for x in lines if self.window[0] <= x[0] <= self.window[1] + 0.06]
-            if len(inside) >= 3:
-                lines = inside
-        for _, ln in lines:
-            parts = [x.strip() for x in ln.split(",")]
-            if len(parts) < 9:
-                continue
-            try:
-                sm.append(float(parts[1]))
-                mx.append(float(parts[2]))
-            except ValueError:
-                continue
-            for nm, v in zip(names, parts[5:9]):
-                if v.lower().startswith("active"):
-                    reasons.add(nm)
-        if not sm:
-            return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm)}
+        return summarize_clocks(self.lines, self.window)
+
+
+def summarize_clocks(lines, window=None):
+    """Median SM clock, max clock and the throttle reasons seen, from
+    (arrival time, nvidia-smi csv line) samples; only samples inside the
+    timed window count when at least three arrived in it."""
+    sm, mx, reasons = [], [], set()
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    if window is not None:
+        inside = [x for x in lines if window[0] <= x[0] <= window[1] + 0.06]
+        if len(inside) >= 3:
+            lines = inside
+    for _, ln in lines:
+        parts = [x.strip() for x in ln.split(",")]
+        if len(parts) < 9:
+            continue
+        try:
+            sm.append(float(parts[1]))
+            mx.append(float(parts[2]))
+        except ValueError:
+            continue
+        for nm, v in zip(names, parts[5:9]):
+            if v.lower().startswith("active"):
+                reasons.add(nm)
+    if not sm:
+        return None
+    return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+            "samples": len(sm)}
 
 
 # ------------------------------------------------------------------ oracle timing
