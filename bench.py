@@ -55,6 +55,8 @@ def parse_args():
     p.add_argument("--workspace-limit-gb", type=float, default=0.0,
                    help="cap the NS5 workspace (sequential sub-plans); 0 = the library's automatic policy, "
                         "-1 = no cap")
+    p.add_argument("--ns-form", choices=["auto", "direct"], default="auto",
+                   help="NS5 evaluation: auto = Gram route for groups with c >= 2 r, direct = rounds on X")
     return p.parse_args()
 
 
@@ -394,7 +396,7 @@ def run_ours(args):
     torch.cuda.synchronize()
     ws_limit = -1 if args.workspace_limit_gb < 0 else int(args.workspace_limit_gb * 2 ** 30)
     opt = PeriodicRowMuon(Ws, Ms, grads, muonbp_blocks=blocks,
-                          workspace_limit=ws_limit)
+                          workspace_limit=ws_limit, ns_form=args.ns_form)
     stream = torch.cuda.current_stream()
 
     def cycle(k, ev_ref=None):
@@ -551,7 +553,7 @@ def run_ours(args):
         for buf in extra:
             gl = [buf[offs[i]:offs[i] + s[0] * s[1]].view(s) for i, s in enumerate(ms.shapes)]
             opts.append(PeriodicRowMuon(Ws, Ms, gl, muonbp_blocks=blocks, workspace=opt.workspace,
-                                        workspace_limit=ws_limit))
+                                        workspace_limit=ws_limit, ns_form=args.ns_form))
         bufs = list(zip([gflat] + extra, opts))
         out_row = torch.empty(ms.shapes[0][1], dtype=torch.float32).pin_memory()
         d2h = out_row.numel() * 4
@@ -684,7 +686,8 @@ def run_ours(args):
                    "workspace_gb": round(opt.workspace_bytes / 2 ** 30, 2),
                    "workspace_policy": ("automatic" if args.workspace_limit_gb == 0 else
                                         "no cap" if args.workspace_limit_gb < 0 else
-                                        f"cap {args.workspace_limit_gb} GiB")},
+                                        f"cap {args.workspace_limit_gb} GiB"),
+                   "ns_form": args.ns_form},
         "ms_refresh_step": round(refresh_ms, 3), "ms_cheap_step": round(cheap_ms, 3),
         "ns5_tflops": round(ns_flop / (ns_ms * 1e-3) / 1e12, 1) if ns_ms else None,
         "rownorm_gbs": round(rn_bytes / (rn_ms * 1e-3) / 1e9, 1) if rn_ms else None,

@@ -126,6 +126,24 @@ PRM_API int prm_register_matrices(prm_ctx* ctx, const prm_matrix_desc* descs, in
  * bounded number of matrices materialised at a time). Errors: INVALID_ARG. */
 PRM_API int prm_set_workspace_limit(prm_ctx* ctx, size_t max_bytes);
 
+/* How the NS5 rounds of the next prm_register_matrices are evaluated. Both
+ * forms compute the same five rounds X <- a X + (b A + c A A) X, A = X X^T,
+ * of [SMDiT] section "Periodic Row-wise Muon"; they differ in rounding only.
+ *   PRM_NS_FORM_AUTO (the default): NS5 groups whose wide shape has
+ *     c >= 2 r take the Gram route -- the rounds run in legs of at most
+ *     three; a leg starts from an explicit X_s, iterates only r x r matrices
+ *     (Q_j = P_j ... P_1 and T_j = Q_j X_s X_s^T, fp16 with fp32
+ *     accumulation) and ends with X_e = Q_L X_s. Per matrix a leg of L
+ *     rounds costs 4 r^2 c + O(L r^3) flops instead of L (4 r^2 c + 2 r^3):
+ *     for the five default rounds on c = 4 r about 30 % fewer flops. The
+ *     other groups, and every group when c = 0 in ns_coeffs, take the direct
+ *     route.
+ *   PRM_NS_FORM_DIRECT: every group evaluates the five rounds on X itself.
+ * Errors: INVALID_ARG (unknown form). */
+#define PRM_NS_FORM_AUTO   0
+#define PRM_NS_FORM_DIRECT 1
+PRM_API int prm_set_ns_form(prm_ctx* ctx, int form);
+
 /* Bytes of device scratch the registered plan needs (NS5 operands in bf16,
  * Gram / polynomial matrices, norm and column partial sums). *bytes (host)
  * receives the size; 0 when nothing is registered. */

@@ -81,11 +81,10 @@ struct SymMaps {
 int encode_x_maps(NsMaps* maps, const void* X, int batch, int64_t r, int64_t c, int64_t ldc);
 int encode_sym_maps(SymMaps* maps, const void* A, int batch, int64_t r, int64_t ldr);
 
-// One same-shape batch of a GEMM launch: `batch` matrices of r x c (GRAM
-// reads X, r x c; POLY reads C, r x r; COMBINE reads P, r x r, and X, r x c).
-// Maps: GRAM a = b = X rows128, out = C store (matrices out_z0 ..);
-// POLY a = b = C rows128, out = P store; COMBINE a = P rows128, b = X x_k64,
-// out = X' store.
+// One same-shape batch of a GEMM launch: `batch` matrices. GRAM: out =
+// A B^T over K = c (r x r, symmetric: upper super-blocks computed, the rest
+// mirrored; a = b = X rows128 for X X^T); POLY: C C (r x r, K = r); COMBINE:
+// out = A B, A r x r rows128, B r x c x_k64 (K = r), out r x c.
 struct GemmSegSpec {
   const CUtensorMap* a;
   const CUtensorMap* b;
@@ -94,28 +93,32 @@ struct GemmSegSpec {
   int batch;
   int64_t r, c;
   int out_z0;
-  const View* views = nullptr;  // COMBINE with apply: device views indexed by batch slot
+  const View* views = nullptr;  // COMBINE: apply D to these device views (by batch slot) instead of storing it
+  bool in_fp16 = false;         // operands fp16 (else bf16); A and B always share the type
+  bool out_fp16 = false;        // output packed as fp16 (else bf16)
+  float gmul = 1.f;             // GRAM / POLY: multiplies the launch's gain
+  // GRAM / POLY: a second output, fp16(gain2 * scale^2 * acc) with no
+  // diagonal shift, written through this map (nullptr: none)
+  const CUtensorMap* out2 = nullptr;
+  float gain2 = 0.f;
 };
 
-// Launch-wide epilogue constants: GRAM / POLY write gain * acc + diag on the
-// diagonal (GRAM also scale^2), COMBINE scale * acc.
+// Launch-wide epilogue constants: GRAM / POLY write gain * gmul * acc + diag
+// on the diagonal (GRAM also scale^2), COMBINE scale * acc. A COMBINE segment
+// with views applies D = X' to them, W <- W * decay - eta * shape_scale * D
+// (transposed back for tall views), or writes D into `out` for views
+// without W.
 struct GemmEpilogue {
   float gain = 1.f, diag = 0.f;
-  bool in_fp16 = false;   // operands fp16 (POLY reading C) instead of bf16
-  bool out_fp16 = false;  // output packed as fp16 (GRAM writing C) instead of bf16
-  // COMBINE of the last round: instead of storing X' = D, apply it to the
-  // segment's views, W <- W * decay - eta * shape_scale * D (transposed back
-  // for tall views), or D into `out` for views without W
-  bool apply = false;
   float decay = 1.f, eta = 0.f;
   int* err = nullptr;     // device error word
   int num_sms = 0;
 };
 
-constexpr int GEMM_MAX_SEGMENTS = 7;  // segments per launch (kernel parameter block under 4 KB)
+constexpr int GEMM_MAX_SEGMENTS = 6;  // segments per launch (kernel parameter block within 4 KB)
 
 // Runs the tiles of every segment of one GEMM kind from one queue (in
-// launches of up to 7 segments; segments with the longest reduction first).
+// launches of up to 6 segments; segments with the longest reduction first).
 cudaError_t launch_gemm(GemmKind kind, const GemmSegSpec* segs, int count, const GemmEpilogue& epi,
                         cudaStream_t stream);
 

@@ -98,31 +98,35 @@ constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;  // 2 s per individual wait
 // r-class (POLY). A launch runs the tiles of up to MAX_SEGS segments from one
 // queue, so the tail of one batch overlaps the next instead of idling SMs
 // between launches.
-constexpr int MAX_SEGS = GEMM_MAX_SEGMENTS;  // 7: keeps the parameter block under 4 KB (a segment is 512 bytes)
+constexpr int MAX_SEGS = GEMM_MAX_SEGMENTS;  // 6: keeps the parameter block within 4 KB (a segment is 640 bytes)
+constexpr int SEG_IN_FP16 = 1;   // operands are fp16 (else bf16)
+constexpr int SEG_OUT_FP16 = 2;  // output packed as fp16 (else bf16)
+constexpr int SEG_DUAL = 4;      // GRAM / POLY: also write gain2 * scale^2 * acc through mapOut2
 struct Segment {
-  CUtensorMap mapA;    // A operand, 128-row K-major boxes
-  CUtensorMap mapB;    // B operand: K-major rows (GRAM, POLY), 64 x 64 MN-major boxes (COMBINE)
-  CUtensorMap mapOut;  // output, 32 x 32 store boxes
-  const float* scale;  // per-matrix s (GRAM applies s^2, COMBINE s), or nullptr
-  int64_t tile_begin;  // first tile of this segment in the launch's queue
-  int M;               // output rows (r)
-  int N;               // output cols (r for GRAM/POLY, c for COMBINE)
-  int K;               // reduction length (c for GRAM, r otherwise)
-  int tiles_m;         // COMBINE: ceil(M / 256)
-  int nb;              // GRAM/POLY: ceil(M / 256) super-blocks per side
+  CUtensorMap mapA;     // A operand, 128-row K-major boxes
+  CUtensorMap mapB;     // B operand: K-major rows (GRAM, POLY), 64 x 64 MN-major boxes (COMBINE)
+  CUtensorMap mapOut;   // output, 32 x 32 store boxes
+  CUtensorMap mapOut2;  // second output of a SEG_DUAL segment (no diagonal shift)
+  const float* scale;   // per-matrix s (GRAM applies s^2, COMBINE s), or nullptr
+  int64_t tile_begin;   // first tile of this segment in the launch's queue
+  int M;                // output rows (r)
+  int N;                // output cols (r for GRAM/POLY, c for COMBINE)
+  int K;                // reduction length (c for GRAM, r otherwise)
+  int tiles_m;          // COMBINE: ceil(M / 256)
+  int nb;               // GRAM/POLY: ceil(M / 256) super-blocks per side
   int tiles_per_mat;
-  int out_z0;          // first matrix of the output map this segment writes
-  const View* views;   // COMBINE of the last round: the segment's views by batch slot
+  int out_z0;           // first matrix of the output map this segment writes
+  int flags;            // SEG_*
+  float gmul;           // GRAM / POLY: multiplies the launch's gain
+  float gain2;          // SEG_DUAL: gain of the second output
+  const View* views;    // COMBINE: apply D to these views (by batch slot) instead of storing it
 };
 
 struct GemmParams {
   Segment seg[MAX_SEGS];
   int nseg;
   int64_t total_tiles;
-  float gain, diag;     // GRAM / POLY: out = gain * (scale^2) * acc + diag * [i == j]
-  int in_fp16;          // operands are fp16 (POLY reading C); else bf16
-  int out_fp16;         // output is packed as fp16 (GRAM writing C); else bf16
-  int apply;            // COMBINE: apply D = X' to the views' W instead of storing X'
+  float gain, diag;     // GRAM / POLY: out = gain * gmul * (scale^2) * acc + diag * [i == j]
   float decay, eta;     // apply: W <- W * decay - eta * shape_scale * D
   int* err;
   uint64_t timeout_ns;
@@ -306,25 +310,58 @@ __device__ __forceinline__ void apply_store(const GemmParams& p, const ApplyTarg
   }
 }
 
+// Stages one lane's 32 packed values (row `lane` of the box) and, for a
+// mirrored tile, the transposed box, then issues their TMA stores. The
+// warp's boxes are rewritten only after its previous stores have read them.
+__device__ __forceinline__ void stage_and_store(const CUtensorMap* tm, uint8_t* stage, int lane, const uint32_t (&w)[16],
+                                                bool mirror, bool rows_in, int i0, int j0, int z) {
+  uint8_t* bd = stage;
+  uint8_t* bm = stage + EPI_BUF_BYTES;
+  if (lane == 0) bulk_wait_group_read<0>();
+  __syncwarp();
+#pragma unroll
+  for (int c = 0; c < 4; ++c)
+    *reinterpret_cast<uint4*>(bd + stage_off(lane, c)) = make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+  if (mirror) {
+    // Lower super-block (J, I): out[j][i] for this chunk's 32 columns j and
+    // the warp's 32 rows i, staged transposed (box row = j).
+#pragma unroll
+    for (int k = 0; k < 32; ++k)
+      *reinterpret_cast<uint16_t*>(bm + stage_off(k, lane >> 3) + (lane & 7) * 2) =
+          static_cast<uint16_t>(w[k >> 1] >> ((k & 1) * 16));
+  }
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0) {
+    if (rows_in) {
+      tma_store_3d(tm, bd, j0, i0, z);
+      if (mirror) tma_store_3d(tm, bm, i0, j0, z);
+    }
+    bulk_commit_group();
+  }
+}
+
 // One tile's epilogue for this warp's 32 accumulator rows and its half of
-// the columns (chunks qbase .. qbase + 3). The warp's two staging boxes
-// (direct, mirrored) are rewritten only after its previous stores have read
-// them.
+// the columns (chunks qbase .. qbase + 3).
 template <int KIND>
 __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const Segment& sg, const TileCoord& tc, int i,
                                               uint32_t t_row, uint8_t* stage, int lane, int qbase,
                                               const ApplyTarget& at, float (&weven)[32], float (&wodd)[32]) {
   const int i0 = i - lane;  // first output row of this warp
-  const CUtensorMap* tm_out = &sg.mapOut;
   float s = 1.f;
   if (KIND == GEMM_GRAM && sg.scale != nullptr) {
     const float q = sg.scale[tc.mat];
     s = q * q;
   }
   if (KIND == GEMM_COMBINE && sg.scale != nullptr) s = sg.scale[tc.mat];
-  if (KIND != GEMM_COMBINE) s *= p.gain;
+  const float s2 = s * sg.gain2;  // SEG_DUAL
+  if (KIND != GEMM_COMBINE) s *= p.gain * sg.gmul;
   const int z = sg.out_z0 + tc.mat;
   const bool rows_in = i0 < sg.M;  // warp-uniform
+  const bool out16 = (sg.flags & SEG_OUT_FP16) != 0;
+  const bool dual = KIND != GEMM_COMBINE && (sg.flags & SEG_DUAL) != 0;
+  const bool apply = KIND == GEMM_COMBINE && sg.views != nullptr;
+  const bool mirror = KIND != GEMM_COMBINE && tc.mirror;
 
 #pragma unroll
   for (int qq = 0; qq < EPI_CHUNKS / 2; ++qq) {
@@ -333,6 +370,11 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const Segment
     if (j0 < sg.N) {  // uniform over the warp: depends on the tile only
       float v[32];
       tmem_load_32cols(t_row + static_cast<uint32_t>(q * 32), v);
+      uint32_t w2[16];
+      if (dual) {
+#pragma unroll
+        for (int h = 0; h < 16; ++h) w2[h] = pack_f16x2(v[2 * h] * s2, v[2 * h + 1] * s2);
+      }
 #pragma unroll
       for (int k = 0; k < 32; ++k) v[k] *= s;
       if (KIND != GEMM_COMBINE && j0 == i0) {  // the warp's 32 diagonal elements (warp-uniform)
@@ -343,29 +385,19 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const Segment
       uint32_t w[16];
 #pragma unroll
       for (int h = 0; h < 16; ++h)
-        w[h] = p.out_fp16 ? pack_f16x2(v[2 * h], v[2 * h + 1]) : pack_bf16x2(v[2 * h], v[2 * h + 1]);
-      const bool mirror = KIND != GEMM_COMBINE && tc.mirror;
-      uint8_t* bd = stage;
-      uint8_t* bm = stage + EPI_BUF_BYTES;
-      if (lane == 0) bulk_wait_group_read<0>();
-      __syncwarp();
-      // this lane's row i, columns j0 .. j0 + 31
+        w[h] = out16 ? pack_f16x2(v[2 * h], v[2 * h + 1]) : pack_bf16x2(v[2 * h], v[2 * h + 1]);
+      if (apply) {
+        // D = X' from the staged box; this chunk's W values sit in the array
+        // of its parity (loaded two chunks earlier, or before the
+        // accumulator wait for the first two); once they are used, the array
+        // takes the values two chunks ahead
+        uint8_t* bd = stage;
+        if (lane == 0) bulk_wait_group_read<0>();
+        __syncwarp();
 #pragma unroll
-      for (int c = 0; c < 4; ++c)
-        *reinterpret_cast<uint4*>(bd + stage_off(lane, c)) =
-            make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
-      if (mirror) {
-        // Lower super-block (J, I): out[j][i] for this chunk's 32 columns j
-        // and the warp's 32 rows i, staged transposed (box row = j).
-#pragma unroll
-        for (int k = 0; k < 32; ++k)
-          *reinterpret_cast<uint16_t*>(bm + stage_off(k, lane >> 3) + (lane & 7) * 2) =
-              static_cast<uint16_t>(w[k >> 1] >> ((k & 1) * 16));
-      }
-      if (KIND == GEMM_COMBINE && p.apply) {
-        // this chunk's W values sit in the array of its parity (loaded two
-        // chunks earlier, or before the accumulator wait for the first two);
-        // once they are used, the array takes the values two chunks ahead
+        for (int c = 0; c < 4; ++c)
+          *reinterpret_cast<uint4*>(bd + stage_off(lane, c)) =
+              make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
         float(&wcur)[32] = (qq & 1) ? wodd : weven;
         __syncwarp();
         if (rows_in) apply_store(p, at, sg.M, sg.N, i0, j0, lane, wcur, bd, w);
@@ -373,15 +405,8 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const Segment
         __syncwarp();
         continue;
       }
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) {
-        if (rows_in) {
-          tma_store_3d(tm_out, bd, j0, i0, z);
-          if (mirror) tma_store_3d(tm_out, bm, i0, j0, z);
-        }
-        bulk_commit_group();
-      }
+      stage_and_store(&sg.mapOut, stage, lane, w, mirror, rows_in, i0, j0, z);
+      if (dual) stage_and_store(&sg.mapOut2, stage, lane, w2, mirror, rows_in, i0, j0, z);
     }
   }
 }
@@ -487,14 +512,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     }
   } else if (warp == 1) {
     if (lane == 0 && rank == 0) {
-      const uint32_t idesc = idesc_f16kind_f32(PAIR_M, BN, false, KIND == GEMM_COMBINE, p.in_fp16 != 0);
+      const uint32_t idesc_bf16 = idesc_f16kind_f32(PAIR_M, BN, false, KIND == GEMM_COMBINE, false);
+      const uint32_t idesc_fp16 = idesc_f16kind_f32(PAIR_M, BN, false, KIND == GEMM_COMBINE, true);
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true, issued_any = false;
       for (int64_t tile = pair_id; ok && tile < p.total_tiles; tile += num_pairs) {
-        const int num_kb = (p.seg[seg_of(p, tile)].K + BK - 1) / BK;
+        const Segment& sg = p.seg[seg_of(p, tile)];
+        const int num_kb = (sg.K + BK - 1) / BK;
+        const uint32_t idesc = (sg.flags & SEG_IN_FP16) ? idesc_fp16 : idesc_bf16;
         if (!wait_bounded(&tempty_bar[acc], acc_phase ^ 1u, abort_flag, p.err, p.timeout_ns)) {
           ok = false;
           break;
@@ -543,7 +571,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     const int qbase = (ew >> 2) * (EPI_CHUNKS / 2);  // first 32-column chunk of this warp's half
     uint8_t* stage = sEpi + ew * EPI_WARP_BYTES;
     if (lane == 0)
-      for (int q = 0; q < p.nseg; ++q) tma_prefetch_desc(&p.seg[q].mapOut);
+      for (int q = 0; q < p.nseg; ++q) {
+        tma_prefetch_desc(&p.seg[q].mapOut);
+        if (p.seg[q].flags & SEG_DUAL) tma_prefetch_desc(&p.seg[q].mapOut2);
+      }
     const uint32_t tempty_even = mapa_shared(smem_u32(&tempty_bar[0]), 0);
     int acc = 0;
     uint32_t acc_phase = 0;
@@ -553,7 +584,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       const int i = tc.m0 + static_cast<int>(rank) * BM + quarter * 32 + lane;
       ApplyTarget at{};
       float weven[32], wodd[32];
-      if (KIND == GEMM_COMBINE && p.apply) {
+      if (KIND == GEMM_COMBINE && sg.views != nullptr) {
         // the first two chunks' W values load while the accumulator is computed
         at = apply_target(p, sg.views, tc.mat);
         apply_load(at, sg.M, sg.N, i - lane, tc.n0 + qbase * 32, lane, weven);
@@ -699,9 +730,6 @@ cudaError_t launch_gemm(GemmKind kind, const GemmSegSpec* specs, int count, cons
     GemmParams p{};
     p.gain = epi.gain;
     p.diag = epi.diag;
-    p.in_fp16 = epi.in_fp16 ? 1 : 0;
-    p.out_fp16 = epi.out_fp16 ? 1 : 0;
-    p.apply = (kind == GEMM_COMBINE && epi.apply) ? 1 : 0;
     p.decay = epi.decay;
     p.eta = epi.eta;
     p.err = epi.err;
@@ -713,8 +741,13 @@ cudaError_t launch_gemm(GemmKind kind, const GemmSegSpec* specs, int count, cons
       sg.mapA = *g.a;
       sg.mapB = *g.b;
       sg.mapOut = *g.out;
+      if (g.out2 != nullptr) sg.mapOut2 = *g.out2;
       sg.scale = g.scale;
-      sg.views = g.views;
+      sg.views = kind == GEMM_COMBINE ? g.views : nullptr;
+      sg.flags = (g.in_fp16 ? SEG_IN_FP16 : 0) | (g.out_fp16 ? SEG_OUT_FP16 : 0) |
+                 (kind != GEMM_COMBINE && g.out2 != nullptr ? SEG_DUAL : 0);
+      sg.gmul = g.gmul;
+      sg.gain2 = g.gain2;
       sg.tile_begin = tiles;
       sg.out_z0 = g.out_z0;
       if (kind == GEMM_COMBINE) {

@@ -46,21 +46,34 @@ struct LaunchSet {
   size_t off_partials = 0, off_inv = 0;  // tall RowNorm scratch (relative to workspace base)
 };
 
+// Maps of one Gram-route Y buffer: per matrix an r x (ldr + r) fp16 array
+// [Q | T] (pitch 2 ldr), T starting at column ldr; `full` spans both halves
+// (the padding columns between them are computed and never read).
+struct YMaps {
+  NsMaps q, t, full;
+};
+
 // Same wide-orientation shape r x c: one batch for the GRAM and COMBINE
-// GEMMs. Its r x r Gram / polynomial matrices live in the r-class arrays.
+// GEMMs. Direct route: its r x r Gram / polynomial matrices live in the
+// r-class arrays. Gram route (c >= 2 r): its own C and P arrays and two Y
+// buffers.
 struct NsGroup {
   int64_t r = 0, c = 0, ldc = 0, ldr = 0;
   int count = 0;
-  int rclass = 0;
+  int rclass = -1;        // direct route: index of its r-class
+  bool gram = false;      // Gram route
   int64_t base_slot = 0;  // first slot of this group inside its r-class arrays
   int64_t slots = 0;      // Frobenius partial slots per matrix
   std::vector<LaunchSet> sets;
   size_t off_x0 = 0, off_x1 = 0, off_scale = 0, off_partials = 0;
+  size_t off_c = 0, off_p = 0, off_ya = 0, off_yb = 0;  // Gram route
   // tensor maps for the bound workspace
   const void* maps_base = nullptr;
   NsMaps mx0{}, mx1{};
-  SymMaps mb{};  // this group's slice of the r-class B array (P; COMBINE operand)
-  SymMaps ma{};  // this group's slice of the r-class A array (P when POLY is skipped, c = 0)
+  SymMaps mb{};  // direct: this group's slice of the r-class B array (P; COMBINE operand)
+  SymMaps ma{};  // direct: this group's slice of the r-class A array (P when POLY is skipped, c = 0)
+  SymMaps mc{}, mp{};  // Gram route: C and P
+  YMaps ya{}, yb{};    // Gram route
   View* d_slot_views = nullptr;  // device: the group's views by slot (the last COMBINE applies D through them)
 };
 
@@ -137,7 +150,8 @@ bool view_vec_ok(const View& v) {
 }
 
 // Groups views for the NS5 branch and lays out the shared group workspace.
-void build_ns_plan(const std::vector<View>& views, NsPlan& plan) {
+// `form` PRM_NS_FORM_AUTO puts the groups with c >= 2 r on the Gram route.
+void build_ns_plan(const std::vector<View>& views, NsPlan& plan, int form) {
   std::map<std::pair<int64_t, int64_t>, size_t> index;
   for (const View& v0 : views) {
     const bool tall = v0.rows > v0.cols;
@@ -183,6 +197,20 @@ void build_ns_plan(const std::vector<View>& views, NsPlan& plan) {
     off += align_up(static_cast<size_t>(g.count) * 4, 256);
     g.off_partials = off;
     off += align_up(static_cast<size_t>(g.count) * g.slots * 4, 256);
+    g.gram = form == PRM_NS_FORM_AUTO && g.c >= 2 * g.r;
+    if (g.gram) {
+      const size_t cb = align_up(static_cast<size_t>(g.count) * g.r * g.ldr * 2, 256);
+      const size_t yb = align_up(static_cast<size_t>(g.count) * g.r * 2 * g.ldr * 2, 256);
+      g.off_c = off;
+      off += cb;
+      g.off_p = off;
+      off += cb;
+      g.off_ya = off;
+      off += yb;
+      g.off_yb = off;
+      off += yb;
+      continue;
+    }
     auto it = rindex.find(g.r);
     if (it == rindex.end()) {
       NsRClass rc;
@@ -219,12 +247,12 @@ constexpr size_t AUTO_SUBPLAN_BYTES = size_t(4) << 30;
 // bytes (SIZE_MAX: one plan for everything; 0: the automatic policy above).
 // Views are taken in (r, c) order so that same-shape matrices stay together;
 // a sub-plan holds at least one view.
-void build_ns_subplans(const std::vector<View>& views, size_t limit, std::vector<NsPlan>& out) {
+void build_ns_subplans(const std::vector<View>& views, size_t limit, int form, std::vector<NsPlan>& out) {
   out.clear();
   if (views.empty()) return;
   if (limit == 0 || limit == SIZE_MAX) {
     out.emplace_back();
-    build_ns_plan(views, out.back());
+    build_ns_plan(views, out.back(), form);
     if (limit == SIZE_MAX || out.back().bytes <= AUTO_SPLIT_ABOVE) return;
     out.clear();
     limit = AUTO_SUBPLAN_BYTES;
@@ -239,16 +267,16 @@ void build_ns_subplans(const std::vector<View>& views, size_t limit, std::vector
   for (const View& v : sorted) {
     cur.push_back(v);
     NsPlan trial;
-    build_ns_plan(cur, trial);
+    build_ns_plan(cur, trial, form);
     if (trial.bytes > limit && cur.size() > 1) {
       cur.pop_back();
       out.emplace_back();
-      build_ns_plan(cur, out.back());
+      build_ns_plan(cur, out.back(), form);
       cur.assign(1, v);
     }
   }
   out.emplace_back();
-  build_ns_plan(cur, out.back());
+  build_ns_plan(cur, out.back(), form);
 }
 
 size_t plans_bytes(const std::vector<NsPlan>& plans) {
@@ -317,6 +345,7 @@ struct prm_ctx {
   RowNormPlan rn;
   std::vector<NsPlan> ns_full, ns_blocks;  // sequential sub-plans (one unless a workspace cap splits them)
   size_t ws_limit = 0;                     // prm_set_workspace_limit; 0 = automatic, SIZE_MAX = no cap
+  int ns_form = PRM_NS_FORM_AUTO;          // prm_set_ns_form
   std::vector<View> full;                  // registered matrices, in registration order
   struct {
     bool valid = false;
@@ -426,12 +455,24 @@ int bind_maps(prm_ctx* c, NsPlan& plan, void* base) {
   }
   for (auto& g : plan.groups) {
     if (g.maps_base == base) continue;
-    const NsRClass& rc = plan.rclasses[g.rclass];
-    const size_t slice = static_cast<size_t>(g.base_slot) * g.r * g.ldr * 2;
     int e = encode_x_maps(&g.mx0, b + g.off_x0, g.count, g.r, g.c, g.ldc);
     if (e == 0) e = encode_x_maps(&g.mx1, b + g.off_x1, g.count, g.r, g.c, g.ldc);
-    if (e == 0) e = encode_sym_maps(&g.mb, b + rc.off_b + slice, g.count, g.r, g.ldr);
-    if (e == 0) e = encode_sym_maps(&g.ma, b + rc.off_a + slice, g.count, g.r, g.ldr);
+    if (g.gram) {
+      if (e == 0) e = encode_sym_maps(&g.mc, b + g.off_c, g.count, g.r, g.ldr);
+      if (e == 0) e = encode_sym_maps(&g.mp, b + g.off_p, g.count, g.r, g.ldr);
+      for (auto yy : {std::make_pair(&g.ya, g.off_ya), std::make_pair(&g.yb, g.off_yb)}) {
+        char* y = b + yy.second;
+        const int64_t ld = 2 * g.ldr;
+        if (e == 0) e = encode_x_maps(&yy.first->q, y, g.count, g.r, g.r, ld);
+        if (e == 0) e = encode_x_maps(&yy.first->t, y + g.ldr * 2, g.count, g.r, g.r, ld);
+        if (e == 0) e = encode_x_maps(&yy.first->full, y, g.count, g.r, g.ldr + g.r, ld);
+      }
+    } else {
+      const NsRClass& rc = plan.rclasses[g.rclass];
+      const size_t slice = static_cast<size_t>(g.base_slot) * g.r * g.ldr * 2;
+      if (e == 0) e = encode_sym_maps(&g.mb, b + rc.off_b + slice, g.count, g.r, g.ldr);
+      if (e == 0) e = encode_sym_maps(&g.ma, b + rc.off_a + slice, g.count, g.r, g.ldr);
+    }
     if (e != 0) return fail(c, PRM_ERR_CUDA, "cuTensorMapEncodeTiled failed (code " + std::to_string(e) + ")");
     g.maps_base = base;
   }
@@ -476,68 +517,160 @@ int run_ns(prm_ctx* c, NsPlan& plan, void* base, bool update_momentum, float bet
   const double ca = coeffs[0], cb = coeffs[1], cc = coeffs[2];
   const bool square = cc != 0.0;
   const double root = square ? std::sqrt(std::fabs(cc)) : 0.0, sg = cc > 0.0 ? 1.0 : -1.0;
-  const float gram_gain = static_cast<float>(square ? root : cb);
-  const float gram_diag = static_cast<float>(square ? sg * cb / (2.0 * root) : ca);
-  const float poly_gain = static_cast<float>(sg);
-  const float poly_diag = static_cast<float>(square ? ca - cb * cb / (4.0 * cc) : 0.0);
   GemmEpilogue gram_epi, poly_epi, comb_epi;
-  gram_epi.gain = gram_gain;
-  gram_epi.diag = gram_diag;
-  gram_epi.out_fp16 = square;  // C (fp16) for POLY; P (bf16) for COMBINE when c = 0
-  poly_epi.gain = poly_gain;
-  poly_epi.diag = poly_diag;
-  poly_epi.in_fp16 = true;
+  gram_epi.gain = static_cast<float>(square ? root : cb);
+  gram_epi.diag = static_cast<float>(square ? sg * cb / (2.0 * root) : ca);
+  poly_epi.gain = static_cast<float>(sg);
+  poly_epi.diag = static_cast<float>(square ? ca - cb * cb / (4.0 * cc) : 0.0);
+  comb_epi.decay = decay;
+  comb_epi.eta = eta;
   for (GemmEpilogue* ep : {&gram_epi, &poly_epi, &comb_epi}) {
     ep->err = c->d_err;
     ep->num_sms = c->num_sms;
   }
-  double gram_flops = 0, poly_flops = 0;
-  for (const auto& g : plan.groups) gram_flops += 2.0 * g.count * double(g.r) * g.r * g.c;
-  for (const auto& rcl : plan.rclasses) poly_flops += 2.0 * rcl.count * double(rcl.r) * rcl.r * rcl.r;
-  std::vector<GemmSegSpec> gram(plan.groups.size()), comb(plan.groups.size()), poly(plan.rclasses.size());
   auto launches_for = [](size_t segments) {
     return static_cast<int>((segments + GEMM_MAX_SEGMENTS - 1) / GEMM_MAX_SEGMENTS);
   };
-  // 2. five rounds; each stage is one launch over every group (POLY: every
-  // r-class), so a round is three launches however many shapes there are
+  auto run = [&](GemmKind kind, const std::vector<GemmSegSpec>& specs, const GemmEpilogue& epi, int family,
+                 double flops, const char* what) -> int {
+    if (specs.empty()) return PRM_OK;
+    const size_t ev = c->prof.begin(stream);
+    const cudaError_t err = launch_gemm(kind, specs.data(), static_cast<int>(specs.size()), epi, stream);
+    if (err != cudaSuccess) return cuda_fail(c, err, what);
+    c->prof.end(ev, family, launches_for(specs.size()), flops, stream);
+    return PRM_OK;
+  };
+  // Gram route: the rounds run in legs of at most three. A leg starts from an
+  // explicit X_s (X_0, or the previous leg's result) and iterates r x r
+  // matrices only: with A_0 = X_s X_s^T and Q_j = P_j ... P_1 (so that
+  // X_j = Q_j X_s and A_j = Q_{j-1} A_0 Q_{j-1}^T), round j computes
+  //   C_j = sqrt|c| T_{j-1} Q_{j-1}^T / S + sgn(c) b / (2 sqrt|c|) I
+  //         (T = Q A_0 S, symmetric; round 1: C_1 from X_s X_s^T directly),
+  //   P_j = sgn(c) C_j C_j + (a - b^2 / (4c)) I,
+  //   [Q_j | T_j] = P_j [Q_{j-1} | T_{j-1}]   ([Q_0 | T_0] = [I | S A_0]),
+  // and the leg ends with X_e = Q_L X_s. Round 1's GRAM also writes S A_0
+  // (its second output) and its POLY writes P_1 = Q_1 in place; the last
+  // round forms Q_L alone, in bf16 for the product with X_s. Per matrix and
+  // leg of L rounds that is 2 r^2 c (GRAM) + 2 r^2 c (X_e) + (4L - 2) r^3
+  // (symmetric, half computed) + (4L - 4) r^3 flops, against L (4 r^2 c +
+  // 2 r^3) for the direct rounds.
+  std::vector<int> leg_first, leg_len;  // per round: first round and length of its leg
+  for (int r0 = 0; r0 < steps; r0 += 3)
+    for (int k = r0; k < std::min(steps, r0 + 3); ++k) {
+      leg_first.push_back(r0);
+      leg_len.push_back(std::min(3, steps - r0));
+    }
+  auto gram_scale = [](int64_t r) {  // S: a power of two near r, so S A_0 and T stay well inside fp16
+    double S = 1.0;
+    while (S * 2.0 <= static_cast<double>(r) && S < 8192.0) S *= 2.0;
+    return S;
+  };
+  // 2. the rounds: each stage is one launch over every group (POLY: every
+  // direct r-class and Gram group); a Gram leg's end is one more COMBINE
   for (int it = 0; it < steps; ++it) {
-    const bool odd = (it & 1) != 0;  // round `it` reads X_it: x0 on even rounds, x1 on odd ones
-    for (size_t k = 0; k < plan.groups.size(); ++k) {
-      const NsGroup& g = plan.groups[k];
-      const NsRClass& rcl = plan.rclasses[g.rclass];
+    const bool last = it == steps - 1;
+    const int leg = leg_first[it] / 3, j = it - leg_first[it] + 1, L = leg_len[it];
+    std::vector<GemmSegSpec> gram, poly, comb, ends;
+    double f_gram = 0, f_poly = 0, f_comb = 0, f_end = 0;
+    for (const NsGroup& g : plan.groups) {
+      const double n = g.count, r = static_cast<double>(g.r), cw = static_cast<double>(g.c);
+      const float* scale0 = reinterpret_cast<const float*>(b + g.off_scale);
+      if (g.gram && square) {
+        const NsMaps& xs = (leg & 1) ? g.mx1 : g.mx0;
+        const NsMaps& xe = (leg & 1) ? g.mx0 : g.mx1;
+        const float* sc = leg == 0 ? scale0 : nullptr;
+        const YMaps& yprev = ((j - 1) & 1) ? g.yb : g.ya;  // holds [Q_{j-1} | T_{j-1}] for j >= 2
+        const YMaps& ycur = (j & 1) ? g.yb : g.ya;
+        const double S = gram_scale(g.r);
+        if (j == 1) {
+          GemmSegSpec gs{&xs.x_rows128, &xs.x_rows128, &g.mc.store, sc, g.count, g.r, g.c, 0};
+          gs.out_fp16 = true;
+          if (L > 1) {
+            gs.out2 = &g.ya.t.store;
+            gs.gain2 = static_cast<float>(S);
+          }
+          gram.push_back(gs);
+          f_gram += 2 * n * r * r * cw;
+          GemmSegSpec ps{&g.mc.rows128, &g.mc.rows128, L > 1 ? &g.yb.q.store : &g.mp.store, nullptr,
+                         g.count, g.r, g.r, 0};
+          ps.in_fp16 = true;
+          ps.out_fp16 = L > 1;
+          poly.push_back(ps);
+          f_poly += 2 * n * r * r * r;
+          if (L > 1) {
+            GemmSegSpec cs{&g.yb.q.x_rows128, &g.ya.t.x_k64, &g.yb.t.store, nullptr, g.count, g.r, g.r, 0};
+            cs.in_fp16 = cs.out_fp16 = true;
+            comb.push_back(cs);
+            f_comb += 2 * n * r * r * r;
+          } else {
+            GemmSegSpec cs{&g.mp.rows128, &xs.x_k64, &xe.store, sc, g.count, g.r, g.c, 0};
+            if (last) cs.views = g.d_slot_views;
+            comb.push_back(cs);
+            f_comb += 2 * n * r * r * cw;
+          }
+        } else {
+          GemmSegSpec gs{&yprev.t.x_rows128, &yprev.q.x_rows128, &g.mc.store, nullptr, g.count, g.r, g.r, 0};
+          gs.in_fp16 = gs.out_fp16 = true;
+          gs.gmul = static_cast<float>(1.0 / S);
+          gram.push_back(gs);
+          f_gram += 2 * n * r * r * r;
+          GemmSegSpec ps{&g.mc.rows128, &g.mc.rows128, &g.mp.store, nullptr, g.count, g.r, g.r, 0};
+          ps.in_fp16 = ps.out_fp16 = true;
+          poly.push_back(ps);
+          f_poly += 2 * n * r * r * r;
+          if (j < L) {
+            GemmSegSpec cs{&g.mp.rows128, &yprev.full.x_k64, &ycur.full.store, nullptr, g.count, g.r,
+                           g.ldr + g.r, 0};
+            cs.in_fp16 = cs.out_fp16 = true;
+            comb.push_back(cs);
+            f_comb += 4 * n * r * r * r;
+          } else {
+            GemmSegSpec cs{&g.mp.rows128, &yprev.q.x_k64, &ycur.q.store, nullptr, g.count, g.r, g.r, 0};
+            cs.in_fp16 = true;  // Q_L in bf16, the type of X_s
+            comb.push_back(cs);
+            f_comb += 2 * n * r * r * r;
+            GemmSegSpec es{&ycur.q.x_rows128, &xs.x_k64, &xe.store, sc, g.count, g.r, g.c, 0};
+            if (last) es.views = g.d_slot_views;
+            ends.push_back(es);
+            f_end += 2 * n * r * r * cw;
+          }
+        }
+        continue;
+      }
+      // direct rounds: X_it in x0 on even rounds, x1 on odd ones
+      const bool odd = (it & 1) != 0;
       const NsMaps& cur = odd ? g.mx1 : g.mx0;
       const NsMaps& nxt = odd ? g.mx0 : g.mx1;
-      const float* scale = it == 0 ? reinterpret_cast<const float*>(b + g.off_scale) : nullptr;
-      gram[k] = GemmSegSpec{&cur.x_rows128, &cur.x_rows128, &rcl.ma.store, scale, g.count, g.r, g.c,
-                            static_cast<int>(g.base_slot)};
-      const SymMaps& pm = square ? g.mb : g.ma;
-      comb[k] = GemmSegSpec{&pm.rows128, &cur.x_k64, &nxt.store, scale, g.count, g.r, g.c, 0};
+      const float* sc = it == 0 ? scale0 : nullptr;
+      const CUtensorMap* c_out = g.gram ? &g.mc.store : &plan.rclasses[g.rclass].ma.store;
+      GemmSegSpec gs{&cur.x_rows128, &cur.x_rows128, c_out, sc, g.count, g.r, g.c,
+                     g.gram ? 0 : static_cast<int>(g.base_slot)};
+      gs.out_fp16 = square;  // C (fp16) for POLY; P (bf16) for COMBINE when c = 0
+      gram.push_back(gs);
+      f_gram += 2 * n * r * r * cw;
+      const SymMaps& pm = g.gram ? g.mc : (square ? g.mb : g.ma);
+      GemmSegSpec cs{&pm.rows128, &cur.x_k64, &nxt.store, sc, g.count, g.r, g.c, 0};
+      if (last) cs.views = g.d_slot_views;
+      comb.push_back(cs);
+      f_comb += 2 * n * r * r * cw;
     }
-    for (size_t k = 0; k < plan.rclasses.size(); ++k) {
-      const NsRClass& rcl = plan.rclasses[k];
-      poly[k] = GemmSegSpec{&rcl.ma.rows128, &rcl.ma.rows128, &rcl.mb.store, nullptr, rcl.count, rcl.r, rcl.r, 0};
-    }
-    size_t ev = c->prof.begin(stream);
-    if ((e = launch_gemm(GEMM_GRAM, gram.data(), static_cast<int>(gram.size()), gram_epi, stream)) != cudaSuccess)
-      return cuda_fail(c, e, "gram launch");
-    c->prof.end(ev, PRM_FAMILY_NS_GRAM, launches_for(gram.size()), gram_flops, stream);
-    if (square) {
-      ev = c->prof.begin(stream);
-      if ((e = launch_gemm(GEMM_POLY, poly.data(), static_cast<int>(poly.size()), poly_epi, stream)) != cudaSuccess)
-        return cuda_fail(c, e, "poly launch");
-      c->prof.end(ev, PRM_FAMILY_NS_POLY, launches_for(poly.size()), poly_flops, stream);
-    }
+    if (square)
+      for (const NsRClass& rcl : plan.rclasses) {
+        GemmSegSpec ps{&rcl.ma.rows128, &rcl.ma.rows128, &rcl.mb.store, nullptr, rcl.count, rcl.r, rcl.r, 0};
+        ps.in_fp16 = true;
+        poly.push_back(ps);
+        f_poly += 2.0 * rcl.count * double(rcl.r) * rcl.r * rcl.r;
+      }
     // 3. the last round applies D = X_steps instead of storing it:
     // W <- W (1 - lr wd) - eta s D, transposed back for tall views
-    const bool last = it == steps - 1;
-    comb_epi.apply = last;
-    comb_epi.decay = decay;
-    comb_epi.eta = eta;
-    for (size_t k = 0; k < plan.groups.size(); ++k) comb[k].views = last ? plan.groups[k].d_slot_views : nullptr;
-    ev = c->prof.begin(stream);
-    if ((e = launch_gemm(GEMM_COMBINE, comb.data(), static_cast<int>(comb.size()), comb_epi, stream)) != cudaSuccess)
-      return cuda_fail(c, e, "combine launch");
-    c->prof.end(ev, PRM_FAMILY_NS_COMBINE, launches_for(comb.size()), gram_flops, stream);
+    int rc2;
+    if ((rc2 = run(GEMM_GRAM, gram, gram_epi, PRM_FAMILY_NS_GRAM, f_gram, "gram launch")) != PRM_OK) return rc2;
+    if (square && (rc2 = run(GEMM_POLY, poly, poly_epi, PRM_FAMILY_NS_POLY, f_poly, "poly launch")) != PRM_OK)
+      return rc2;
+    if ((rc2 = run(GEMM_COMBINE, comb, comb_epi, PRM_FAMILY_NS_COMBINE, f_comb, "combine launch")) != PRM_OK)
+      return rc2;
+    if ((rc2 = run(GEMM_COMBINE, ends, comb_epi, PRM_FAMILY_NS_COMBINE, f_end, "combine launch")) != PRM_OK)
+      return rc2;
   }
   return PRM_OK;
 }
@@ -704,8 +837,8 @@ int prm_register_matrices(prm_ctx* c, const prm_matrix_desc* d, int count, int m
     off += align_up(s.views.size() * s.cols * 4, 256);
   }
   c->rn.bytes = off;
-  build_ns_subplans(full, c->ws_limit, c->ns_full);
-  if (muonbp_blocks > 0) build_ns_subplans(blocks, c->ws_limit, c->ns_blocks);
+  build_ns_subplans(full, c->ws_limit, c->ns_form, c->ns_full);
+  if (muonbp_blocks > 0) build_ns_subplans(blocks, c->ws_limit, c->ns_form, c->ns_blocks);
   cudaError_t e = upload_sets(c->rn.wide);
   if (e == cudaSuccess) e = upload_sets(c->rn.tall);
   for (auto* plans : {&c->ns_full, &c->ns_blocks})
@@ -726,6 +859,13 @@ int prm_register_matrices(prm_ctx* c, const prm_matrix_desc* d, int count, int m
 int prm_set_workspace_limit(prm_ctx* c, size_t max_bytes) {
   if (c == nullptr) return fail(nullptr, PRM_ERR_INVALID_ARG, "ctx is NULL");
   c->ws_limit = max_bytes;
+  return PRM_OK;
+}
+
+int prm_set_ns_form(prm_ctx* c, int form) {
+  if (c == nullptr) return fail(nullptr, PRM_ERR_INVALID_ARG, "ctx is NULL");
+  if (form != PRM_NS_FORM_AUTO && form != PRM_NS_FORM_DIRECT) return fail(c, PRM_ERR_INVALID_ARG, "unknown NS5 form");
+  c->ns_form = form;
   return PRM_OK;
 }
 
@@ -893,7 +1033,7 @@ int prm_debug_last_direction(prm_ctx* c, int idx, float* host_out) {
       p.W = nullptr;
     }
     NsPlan plan;
-    build_ns_plan(parts, plan);
+    build_ns_plan(parts, plan, c->ns_form);
     for (auto& g : plan.groups) {
       if ((e = upload_group(g)) != cudaSuccess) {
         free_plan(plan);
@@ -989,10 +1129,10 @@ int prm_ns_gram(const uint16_t* X, uint16_t* C, const float* scale, float gain, 
   if (encode_x_maps(&mx, X, batch, r, c, ldc) != 0 || encode_sym_maps(&mc, C, batch, r, ldr) != 0)
     return PRM_ERR_CUDA;
   GemmSegSpec seg{&mx.x_rows128, &mx.x_rows128, &mc.store, scale, batch, r, c, 0};
+  seg.out_fp16 = out_dtype == PRM_FP16;
   GemmEpilogue epi;
   epi.gain = gain;
   epi.diag = diag;
-  epi.out_fp16 = out_dtype == PRM_FP16;
   epi.err = ds->d_err;
   epi.num_sms = ds->num_sms;
   return launch_gemm(GEMM_GRAM, &seg, 1, epi, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PRM_OK
@@ -1013,10 +1153,10 @@ int prm_ns_poly(const uint16_t* C, uint16_t* P, float gain, float diag, int in_d
   if (encode_sym_maps(&mc, C, batch, r, ldr) != 0 || encode_sym_maps(&mp, P, batch, r, ldr) != 0)
     return PRM_ERR_CUDA;
   GemmSegSpec seg{&mc.rows128, &mc.rows128, &mp.store, nullptr, batch, r, r, 0};
+  seg.in_fp16 = in_dtype == PRM_FP16;
   GemmEpilogue epi;
   epi.gain = gain;
   epi.diag = diag;
-  epi.in_fp16 = in_dtype == PRM_FP16;
   epi.err = ds->d_err;
   epi.num_sms = ds->num_sms;
   return launch_gemm(GEMM_POLY, &seg, 1, epi, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PRM_OK
@@ -1054,7 +1194,7 @@ static void standalone_group(int batch, int64_t m, int64_t n, NsPlan& plan) {
     views[i].cols = n;
     views[i].ld = n;
   }
-  build_ns_plan(views, plan);
+  build_ns_plan(views, plan, PRM_NS_FORM_AUTO);
 }
 
 int prm_newton_schulz_workspace(int batch, int64_t m, int64_t n, size_t* bytes) {
@@ -1095,7 +1235,7 @@ int prm_newton_schulz(const float* in, float* out, int batch, int64_t m, int64_t
     v.shape_scale = 1.f;
     views[i] = v;
   }
-  build_ns_plan(views, plan);
+  build_ns_plan(views, plan, PRM_NS_FORM_AUTO);
   if (workspace == nullptr || ws_bytes < plan.bytes) return PRM_ERR_WORKSPACE;
   if (upload_group(plan.groups[0]) != cudaSuccess) {
     free_plan(plan);

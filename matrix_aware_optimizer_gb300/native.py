@@ -34,6 +34,8 @@ PRM_BF16 = 1
 PRM_FP16 = 2
 PRM_MODE_PRMUON = 0
 PRM_MODE_MUONBP = 1
+PRM_NS_FORM_AUTO = 0
+PRM_NS_FORM_DIRECT = 1
 
 ERROR_NAMES = {
     PRM_OK: "OK", PRM_ERR_INVALID_ARG: "INVALID_ARG", PRM_ERR_SHAPE: "SHAPE",
@@ -64,6 +66,7 @@ SIGNATURES = {
     "prm_register_matrices": (c_int, [c_void_p, POINTER(prm_matrix_desc), c_int, c_int]),
     "prm_workspace_bytes": (c_int, [c_void_p, POINTER(c_size_t)]),
     "prm_set_workspace_limit": (c_int, [c_void_p, c_size_t]),
+    "prm_set_ns_form": (c_int, [c_void_p, c_int]),
     "prm_set_workspace": (c_int, [c_void_p, c_void_p, c_size_t]),
     "prm_step": (c_int, [c_void_p, c_int64, c_int, c_float, c_float, c_float, c_float, c_float,
                          POINTER(c_float), c_int, c_void_p]),
@@ -144,6 +147,10 @@ def prm_register_matrices(ctx, descs, muonbp_blocks: int = 0) -> None:
 
 def prm_set_workspace_limit(ctx, max_bytes: int) -> None:
     check(load().prm_set_workspace_limit(ctx, max_bytes), "prm_set_workspace_limit", ctx)
+
+
+def prm_set_ns_form(ctx, form: int) -> None:
+    check(load().prm_set_ns_form(ctx, form), "prm_set_ns_form", ctx)
 
 
 def prm_workspace_bytes(ctx) -> int:

@@ -51,12 +51,12 @@ def _hp(ms):
     return dict(K=ms.K, gamma=ms.gamma, lr=ms.lr, wd=ms.wd, beta=ms.beta, eps=ms.eps)
 
 
-def _run_teacher_forced(ms, steps, check_idx=None, mode="prmuon", blocks=0):
+def _run_teacher_forced(ms, steps, check_idx=None, mode="prmuon", blocks=0, ns_form="auto"):
     shapes = ms.shapes
     Ws, Ms = synth.make_state(ms, device="cuda")
     gdt = torch.bfloat16 if ms.grad_dtype == synth.GRAD_BF16 else torch.float32
     grads = [torch.empty(s, device="cuda", dtype=gdt) for s in shapes]
-    opt = PeriodicRowMuon(Ws, Ms, grads, muonbp_blocks=blocks)
+    opt = PeriodicRowMuon(Ws, Ms, grads, muonbp_blocks=blocks, ns_form=ns_form)
     opt.workspace.fill_(0xFF)  # NaN bit patterns: any read of unwritten scratch shows up
     hp = _hp(ms)
     idx = range(len(shapes)) if check_idx is None else check_idx
@@ -93,17 +93,21 @@ def _run_teacher_forced(ms, steps, check_idx=None, mode="prmuon", blocks=0):
     return report
 
 
-def test_tiny_set_six_steps():
+@pytest.mark.parametrize("ns_form", ["auto", "direct"])
+def test_tiny_set_six_steps(ns_form):
     """4 fp32 matrices (one tall, one ragged 128x96), K=3, 6 steps: two
-    refresh cycles."""
-    rep = _run_teacher_forced(synth.MATRIX_SETS["tiny"], range(6))
+    refresh cycles. Two of the shapes have c >= 2 r: "auto" runs their NS5
+    on the Gram route, "direct" on X itself."""
+    rep = _run_teacher_forced(synth.MATRIX_SETS["tiny"], range(6), ns_form=ns_form)
     assert [r[2] for r in rep[::4]] == [1, 0, 0, 1, 0, 0]
 
 
-def test_dit_block_d2048_full_size():
+@pytest.mark.parametrize("ns_form", ["auto", "direct"])
+def test_dit_block_d2048_full_size(ns_form):
     """The one-DiT-block set at full size (bf16 grads): a refresh step and two
-    RowNorm steps on every matrix, including the tall 8192x2048."""
-    _run_teacher_forced(synth.MATRIX_SETS["dit_block_d2048"], range(3))
+    RowNorm steps on every matrix, including the tall 8192x2048 (c = 3 r and
+    c = 4 r shapes take the Gram route under "auto")."""
+    _run_teacher_forced(synth.MATRIX_SETS["dit_block_d2048"], range(3), ns_form=ns_form)
 
 
 def test_free_running_tiny_matches_oracle():
@@ -174,14 +178,16 @@ def test_edge_shapes_directions(gdtype):
         opt.close()
 
 
-def test_more_shape_groups_than_one_launch_holds():
-    """Nine distinct shapes make nine NS5 groups and nine r-classes: each GEMM
-    stage then runs as two launches (up to seven segments each), which must
-    give the same refresh as the oracle for every matrix."""
+@pytest.mark.parametrize("ns_form", ["auto", "direct"])
+def test_more_shape_groups_than_one_launch_holds(ns_form):
+    """Nine distinct shapes make nine NS5 groups (c = 2 r: all on the Gram
+    route under "auto"; nine r-classes under "direct"): each GEMM stage then
+    runs as two launches (up to six segments each), which must give the same
+    refresh as the oracle for every matrix."""
     shapes = [(32 + 16 * k, 64 + 32 * k) for k in range(9)]
     shapes[3] = (shapes[3][1], shapes[3][0])  # one tall matrix among them
     ms = make_set(shapes, synth.GRAD_BF16, seed=17)
-    _run_teacher_forced(ms, steps=[0, 1])
+    _run_teacher_forced(ms, steps=[0, 1], ns_form=ns_form)
 
 
 def test_muonbp_block_and_full_steps():
@@ -248,13 +254,16 @@ def test_standalone_newton_schulz():
     (1.5, -0.5, 0.0),            # cubic: c = 0, the polynomial stage is skipped
     (1.875, -0.6, -0.275),       # c < 0: the square enters with a minus sign
 ])
-def test_newton_schulz_coefficient_signs(coeffs):
+@pytest.mark.parametrize("shape", [(2, 320, 600), (2, 256, 600)])
+def test_newton_schulz_coefficient_signs(coeffs, shape):
     """The library forms a I + b A + c A A as a completed square whose form
-    depends on the sign of c; every branch must match the plain iteration."""
+    depends on the sign of c; every branch must match the plain iteration,
+    on the direct route (320 x 600) and on the Gram route (256 x 600, which
+    falls back to the direct rounds for c = 0)."""
     gen = torch.Generator().manual_seed(5)
-    X = torch.randn(2, 320, 600, generator=gen)
+    X = torch.randn(*shape, generator=gen)
     D = newton_schulz(X.cuda(), ns_coeffs=coeffs).cpu().double().numpy()
-    for i in range(2):
+    for i in range(shape[0]):
         ref = O.newton_schulz(X[i].double().numpy(), coeffs=coeffs)
         assert rel_frob(D[i], ref) <= TOL_D_NS5, (coeffs, i)
 
