@@ -512,7 +512,7 @@ def run_ours(args):
         d = fam[name]
         if d["records"] == 0 or d["ms"] <= 0:
             return None
-        tensor = name in ("ns_gram", "ns_poly", "ns_combine")
+        tensor = name in ("ns_gram", "ns_poly", "ns_combine", "ns_sym")
         if tensor:
             ach = d["work"] / (d["ms"] * 1e-3) / 1e12
             peak, unit = tf_sus, "TFLOP/s"
@@ -528,8 +528,8 @@ def run_ours(args):
                 "timed_in": "the profiled pass (same K cycles as the headline, library event timer on)"}
 
     top = max(fam, key=lambda k: fam[k]["ms"])
-    ns_ms = sum(fam[k]["ms"] for k in ("ns_gram", "ns_poly", "ns_combine"))
-    ns_flop = sum(fam[k]["work"] for k in ("ns_gram", "ns_poly", "ns_combine"))
+    ns_ms = sum(fam[k]["ms"] for k in ("ns_gram", "ns_poly", "ns_combine", "ns_sym"))
+    ns_flop = sum(fam[k]["work"] for k in ("ns_gram", "ns_poly", "ns_combine", "ns_sym"))
     rn_ms = fam["rownorm_wide"]["ms"] + fam["rownorm_tall"]["ms"]
     rn_bytes = fam["rownorm_wide"]["work"] + fam["rownorm_tall"]["work"]
 

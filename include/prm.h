@@ -132,12 +132,12 @@ PRM_API int prm_set_workspace_limit(prm_ctx* ctx, size_t max_bytes);
  *   PRM_NS_FORM_AUTO (the default): NS5 groups whose wide shape has
  *     c >= 2 r take the Gram route -- the rounds run in legs of at most
  *     three; a leg starts from an explicit X_s, iterates only r x r matrices
- *     (Q_j = P_j ... P_1 and T_j = Q_j X_s X_s^T, fp16 with fp32
- *     accumulation) and ends with X_e = Q_L X_s. Per matrix a leg of L
+ *     (Q_j = P_j ... P_1 and T_j = Q_j X_s X_s^T, all symmetric, fp16 with
+ *     fp32 accumulation) and ends with X_e = Q_L X_s. Per matrix a leg of L
  *     rounds costs 4 r^2 c + O(L r^3) flops instead of L (4 r^2 c + 2 r^3):
- *     for the five default rounds on c = 4 r about 30 % fewer flops. The
- *     other groups, and every group when c = 0 in ns_coeffs, take the direct
- *     route.
+ *     for the five default rounds at r = 2048 about 40 % fewer executed
+ *     flops on c = 4 r, 23 % on c = 2 r. The other groups, and every group
+ *     when c = 0 in ns_coeffs, take the direct route.
  *   PRM_NS_FORM_DIRECT: every group evaluates the five rounds on X itself.
  * Errors: INVALID_ARG (unknown form). */
 #define PRM_NS_FORM_AUTO   0
@@ -258,8 +258,10 @@ PRM_API int prm_adamw_step(float* param, float* exp_avg, float* exp_avg_sq, cons
 /* ---- kernel timing (benchmarks) --------------------------------------
  * When enabled, every kernel family launched by prm_step is bracketed by a
  * pair of CUDA events recorded on the launching stream, and its algorithmic
- * work is accumulated: dense bf16 FLOPs for the GEMM families (2 r^2 c for
- * GRAM and COMBINE, 2 r^3 for POLY per matrix), bytes for the memory-bound
+ * work is accumulated: for the GEMM families the dense FLOPs of the products
+ * they form, 2 M N K per matrix (symmetric outputs -- GRAM, POLY and the Gram
+ * route's updates -- counted dense although only their upper 256 x 256
+ * super-blocks are computed), bytes for the memory-bound
  * ones (RowNorm 18 B per parameter with bf16 gradients, 20 B with fp32;
  * prep 12 / 14 B). The refresh's parameter update runs in the epilogue of
  * the last COMBINE launch and is timed with it. Families: */
@@ -269,7 +271,8 @@ PRM_API int prm_adamw_step(float* param, float* exp_avg, float* exp_avg_sq, cons
 #define PRM_FAMILY_NS_GRAM      3
 #define PRM_FAMILY_NS_POLY      4
 #define PRM_FAMILY_NS_COMBINE   5
-#define PRM_FAMILY_COUNT        6
+#define PRM_FAMILY_NS_SYM       6  /* Gram route: Q <- P Q, T <- P T */
+#define PRM_FAMILY_COUNT        7
 
 /* enable = 1 clears the records and starts recording; 0 stops. */
 PRM_API int prm_profile(prm_ctx* ctx, int enable);

@@ -96,20 +96,17 @@ struct GemmSegSpec {
   const View* views = nullptr;  // COMBINE: apply D to these device views (by batch slot) instead of storing it
   bool in_fp16 = false;         // operands fp16 (else bf16); A and B always share the type
   bool out_fp16 = false;        // output packed as fp16 (else bf16)
-  float gmul = 1.f;             // GRAM / POLY: multiplies the launch's gain
+  float gain = 1.f, diag = 0.f;  // GRAM / POLY: out = gain * (scale^2) * acc + diag * [i == j]
   // GRAM / POLY: a second output, fp16(gain2 * scale^2 * acc) with no
   // diagonal shift, written through this map (nullptr: none)
   const CUtensorMap* out2 = nullptr;
   float gain2 = 0.f;
 };
 
-// Launch-wide epilogue constants: GRAM / POLY write gain * gmul * acc + diag
-// on the diagonal (GRAM also scale^2), COMBINE scale * acc. A COMBINE segment
-// with views applies D = X' to them, W <- W * decay - eta * shape_scale * D
-// (transposed back for tall views), or writes D into `out` for views
-// without W.
+// Launch-wide epilogue constants. A COMBINE segment with views applies
+// D = X' to them, W <- W * decay - eta * shape_scale * D (transposed back for
+// tall views), or writes D into `out` for views without W.
 struct GemmEpilogue {
-  float gain = 1.f, diag = 0.f;
   float decay = 1.f, eta = 0.f;
   int* err = nullptr;     // device error word
   int num_sms = 0;

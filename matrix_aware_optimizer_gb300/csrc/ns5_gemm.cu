@@ -117,7 +117,7 @@ struct Segment {
   int tiles_per_mat;
   int out_z0;           // first matrix of the output map this segment writes
   int flags;            // SEG_*
-  float gmul;           // GRAM / POLY: multiplies the launch's gain
+  float gain, diag;     // GRAM / POLY: out = gain * (scale^2) * acc + diag * [i == j]
   float gain2;          // SEG_DUAL: gain of the second output
   const View* views;    // COMBINE: apply D to these views (by batch slot) instead of storing it
 };
@@ -126,7 +126,6 @@ struct GemmParams {
   Segment seg[MAX_SEGS];
   int nseg;
   int64_t total_tiles;
-  float gain, diag;     // GRAM / POLY: out = gain * gmul * (scale^2) * acc + diag * [i == j]
   float decay, eta;     // apply: W <- W * decay - eta * shape_scale * D
   int* err;
   uint64_t timeout_ns;
@@ -355,7 +354,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const Segment
   }
   if (KIND == GEMM_COMBINE && sg.scale != nullptr) s = sg.scale[tc.mat];
   const float s2 = s * sg.gain2;  // SEG_DUAL
-  if (KIND != GEMM_COMBINE) s *= p.gain * sg.gmul;
+  if (KIND != GEMM_COMBINE) s *= sg.gain;
   const int z = sg.out_z0 + tc.mat;
   const bool rows_in = i0 < sg.M;  // warp-uniform
   const bool out16 = (sg.flags & SEG_OUT_FP16) != 0;
@@ -380,7 +379,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const Segment
       if (KIND != GEMM_COMBINE && j0 == i0) {  // the warp's 32 diagonal elements (warp-uniform)
 #pragma unroll
         for (int k = 0; k < 32; ++k)
-          if (k == lane) v[k] += p.diag;
+          if (k == lane) v[k] += sg.diag;
       }
       uint32_t w[16];
 #pragma unroll
@@ -728,8 +727,6 @@ cudaError_t launch_gemm(GemmKind kind, const GemmSegSpec* specs, int count, cons
                    [&](int x, int y) { return reduction(specs[x]) > reduction(specs[y]); });
   for (size_t first = 0; first < order.size(); first += MAX_SEGS) {
     GemmParams p{};
-    p.gain = epi.gain;
-    p.diag = epi.diag;
     p.decay = epi.decay;
     p.eta = epi.eta;
     p.err = epi.err;
@@ -746,7 +743,8 @@ cudaError_t launch_gemm(GemmKind kind, const GemmSegSpec* specs, int count, cons
       sg.views = kind == GEMM_COMBINE ? g.views : nullptr;
       sg.flags = (g.in_fp16 ? SEG_IN_FP16 : 0) | (g.out_fp16 ? SEG_OUT_FP16 : 0) |
                  (kind != GEMM_COMBINE && g.out2 != nullptr ? SEG_DUAL : 0);
-      sg.gmul = g.gmul;
+      sg.gain = g.gain;
+      sg.diag = g.diag;
       sg.gain2 = g.gain2;
       sg.tile_begin = tiles;
       sg.out_z0 = g.out_z0;

@@ -517,22 +517,20 @@ int run_ns(prm_ctx* c, NsPlan& plan, void* base, bool update_momentum, float bet
   const double ca = coeffs[0], cb = coeffs[1], cc = coeffs[2];
   const bool square = cc != 0.0;
   const double root = square ? std::sqrt(std::fabs(cc)) : 0.0, sg = cc > 0.0 ? 1.0 : -1.0;
-  GemmEpilogue gram_epi, poly_epi, comb_epi;
-  gram_epi.gain = static_cast<float>(square ? root : cb);
-  gram_epi.diag = static_cast<float>(square ? sg * cb / (2.0 * root) : ca);
-  poly_epi.gain = static_cast<float>(sg);
-  poly_epi.diag = static_cast<float>(square ? ca - cb * cb / (4.0 * cc) : 0.0);
-  comb_epi.decay = decay;
-  comb_epi.eta = eta;
-  for (GemmEpilogue* ep : {&gram_epi, &poly_epi, &comb_epi}) {
-    ep->err = c->d_err;
-    ep->num_sms = c->num_sms;
-  }
+  const float gram_gain = static_cast<float>(square ? root : cb);
+  const float gram_diag = static_cast<float>(square ? sg * cb / (2.0 * root) : ca);
+  const float poly_gain = static_cast<float>(sg);
+  const float poly_diag = static_cast<float>(square ? ca - cb * cb / (4.0 * cc) : 0.0);
+  GemmEpilogue epi;
+  epi.decay = decay;
+  epi.eta = eta;
+  epi.err = c->d_err;
+  epi.num_sms = c->num_sms;
   auto launches_for = [](size_t segments) {
     return static_cast<int>((segments + GEMM_MAX_SEGMENTS - 1) / GEMM_MAX_SEGMENTS);
   };
-  auto run = [&](GemmKind kind, const std::vector<GemmSegSpec>& specs, const GemmEpilogue& epi, int family,
-                 double flops, const char* what) -> int {
+  auto run = [&](GemmKind kind, const std::vector<GemmSegSpec>& specs, int family, double flops,
+                 const char* what) -> int {
     if (specs.empty()) return PRM_OK;
     const size_t ev = c->prof.begin(stream);
     const cudaError_t err = launch_gemm(kind, specs.data(), static_cast<int>(specs.size()), epi, stream);
@@ -545,14 +543,17 @@ int run_ns(prm_ctx* c, NsPlan& plan, void* base, bool update_momentum, float bet
   // matrices only: with A_0 = X_s X_s^T and Q_j = P_j ... P_1 (so that
   // X_j = Q_j X_s and A_j = Q_{j-1} A_0 Q_{j-1}^T), round j computes
   //   C_j = sqrt|c| T_{j-1} Q_{j-1}^T / S + sgn(c) b / (2 sqrt|c|) I
-  //         (T = Q A_0 S, symmetric; round 1: C_1 from X_s X_s^T directly),
+  //         (T = S Q A_0; round 1: C_1 from X_s X_s^T directly),
   //   P_j = sgn(c) C_j C_j + (a - b^2 / (4c)) I,
-  //   [Q_j | T_j] = P_j [Q_{j-1} | T_{j-1}]   ([Q_0 | T_0] = [I | S A_0]),
-  // and the leg ends with X_e = Q_L X_s. Round 1's GRAM also writes S A_0
-  // (its second output) and its POLY writes P_1 = Q_1 in place; the last
-  // round forms Q_L alone, in bf16 for the product with X_s. Per matrix and
-  // leg of L rounds that is 2 r^2 c (GRAM) + 2 r^2 c (X_e) + (4L - 2) r^3
-  // (symmetric, half computed) + (4L - 4) r^3 flops, against L (4 r^2 c +
+  //   Q_j = P_j Q_{j-1},  T_j = P_j T_{j-1}   (Q_0 = I, T_0 = S A_0),
+  // and the leg ends with X_e = Q_L X_s. Every P, Q and T is a polynomial in
+  // A_0, so all of them are symmetric and commute: P Q = P Q^T, and the
+  // updates run on the symmetric-output kernel (upper super-blocks, the rest
+  // mirrored), like C. Round 1's GRAM also writes S A_0 (its second output)
+  // and its POLY writes P_1 = Q_1 in place; the last round forms Q_L alone,
+  // in bf16 for the product with X_s. Per matrix a leg of L > 1 rounds costs
+  // 2 r^2 c (GRAM) + 2 r^2 c (X_e) + (8L - 6) r^3 dense-equivalent flops on
+  // the symmetric kernel (about half of it computed), against L (4 r^2 c +
   // 2 r^3) for the direct rounds.
   std::vector<int> leg_first, leg_len;  // per round: first round and length of its leg
   for (int r0 = 0; r0 < steps; r0 += 3)
@@ -565,76 +566,75 @@ int run_ns(prm_ctx* c, NsPlan& plan, void* base, bool update_momentum, float bet
     while (S * 2.0 <= static_cast<double>(r) && S < 8192.0) S *= 2.0;
     return S;
   };
-  // 2. the rounds: each stage is one launch over every group (POLY: every
-  // direct r-class and Gram group); a Gram leg's end is one more COMBINE
+  // 2. the rounds. Each stage is one launch over every group: GRAM, POLY
+  // (every direct r-class and Gram group), the Gram route's symmetric
+  // updates, and COMBINE (direct rounds and the Gram legs' ends).
   for (int it = 0; it < steps; ++it) {
     const bool last = it == steps - 1;
     const int leg = leg_first[it] / 3, j = it - leg_first[it] + 1, L = leg_len[it];
-    std::vector<GemmSegSpec> gram, poly, comb, ends;
-    double f_gram = 0, f_poly = 0, f_comb = 0, f_end = 0;
+    std::vector<GemmSegSpec> gram, poly, sym, comb;
+    double f_gram = 0, f_poly = 0, f_sym = 0, f_comb = 0;
     for (const NsGroup& g : plan.groups) {
       const double n = g.count, r = static_cast<double>(g.r), cw = static_cast<double>(g.c);
+      const double r3 = 2 * n * r * r * r, r2c = 2 * n * r * r * cw;
       const float* scale0 = reinterpret_cast<const float*>(b + g.off_scale);
       if (g.gram && square) {
         const NsMaps& xs = (leg & 1) ? g.mx1 : g.mx0;
         const NsMaps& xe = (leg & 1) ? g.mx0 : g.mx1;
         const float* sc = leg == 0 ? scale0 : nullptr;
-        const YMaps& yprev = ((j - 1) & 1) ? g.yb : g.ya;  // holds [Q_{j-1} | T_{j-1}] for j >= 2
+        const YMaps& yprev = ((j - 1) & 1) ? g.yb : g.ya;  // holds Q_{j-1}, T_{j-1} for j >= 2
         const YMaps& ycur = (j & 1) ? g.yb : g.ya;
         const double S = gram_scale(g.r);
+        GemmSegSpec gs, ps{&g.mc.rows128, &g.mc.rows128, &g.mp.store, nullptr, g.count, g.r, g.r, 0};
+        ps.in_fp16 = ps.out_fp16 = true;
+        ps.gain = poly_gain;
+        ps.diag = poly_diag;
         if (j == 1) {
-          GemmSegSpec gs{&xs.x_rows128, &xs.x_rows128, &g.mc.store, sc, g.count, g.r, g.c, 0};
-          gs.out_fp16 = true;
+          gs = GemmSegSpec{&xs.x_rows128, &xs.x_rows128, &g.mc.store, sc, g.count, g.r, g.c, 0};
           if (L > 1) {
             gs.out2 = &g.ya.t.store;
             gs.gain2 = static_cast<float>(S);
-          }
-          gram.push_back(gs);
-          f_gram += 2 * n * r * r * cw;
-          GemmSegSpec ps{&g.mc.rows128, &g.mc.rows128, L > 1 ? &g.yb.q.store : &g.mp.store, nullptr,
-                         g.count, g.r, g.r, 0};
-          ps.in_fp16 = true;
-          ps.out_fp16 = L > 1;
-          poly.push_back(ps);
-          f_poly += 2 * n * r * r * r;
-          if (L > 1) {
-            GemmSegSpec cs{&g.yb.q.x_rows128, &g.ya.t.x_k64, &g.yb.t.store, nullptr, g.count, g.r, g.r, 0};
-            cs.in_fp16 = cs.out_fp16 = true;
-            comb.push_back(cs);
-            f_comb += 2 * n * r * r * r;
+            ps.out = &g.yb.q.store;  // P_1 = Q_1
+            GemmSegSpec ts{&g.yb.q.x_rows128, &g.ya.t.x_rows128, &g.yb.t.store, nullptr, g.count, g.r, g.r, 0};
+            ts.in_fp16 = ts.out_fp16 = true;
+            sym.push_back(ts);
+            f_sym += r3;
           } else {
+            ps.out_fp16 = false;  // P in bf16, the type of X_s
             GemmSegSpec cs{&g.mp.rows128, &xs.x_k64, &xe.store, sc, g.count, g.r, g.c, 0};
             if (last) cs.views = g.d_slot_views;
             comb.push_back(cs);
-            f_comb += 2 * n * r * r * cw;
+            f_comb += r2c;
           }
+          gs.gain = gram_gain;
+          f_gram += r2c;
         } else {
-          GemmSegSpec gs{&yprev.t.x_rows128, &yprev.q.x_rows128, &g.mc.store, nullptr, g.count, g.r, g.r, 0};
-          gs.in_fp16 = gs.out_fp16 = true;
-          gs.gmul = static_cast<float>(1.0 / S);
-          gram.push_back(gs);
-          f_gram += 2 * n * r * r * r;
-          GemmSegSpec ps{&g.mc.rows128, &g.mc.rows128, &g.mp.store, nullptr, g.count, g.r, g.r, 0};
-          ps.in_fp16 = ps.out_fp16 = true;
-          poly.push_back(ps);
-          f_poly += 2 * n * r * r * r;
+          gs = GemmSegSpec{&yprev.t.x_rows128, &yprev.q.x_rows128, &g.mc.store, nullptr, g.count, g.r, g.r, 0};
+          gs.in_fp16 = true;
+          gs.gain = static_cast<float>(root / S);
+          f_gram += r3;
+          GemmSegSpec qs{&g.mp.rows128, &yprev.q.x_rows128, &ycur.q.store, nullptr, g.count, g.r, g.r, 0};
+          qs.in_fp16 = true;
+          qs.out_fp16 = j < L;  // Q_L in bf16, the type of X_s
+          sym.push_back(qs);
+          f_sym += r3;
           if (j < L) {
-            GemmSegSpec cs{&g.mp.rows128, &yprev.full.x_k64, &ycur.full.store, nullptr, g.count, g.r,
-                           g.ldr + g.r, 0};
-            cs.in_fp16 = cs.out_fp16 = true;
-            comb.push_back(cs);
-            f_comb += 4 * n * r * r * r;
+            GemmSegSpec ts{&g.mp.rows128, &yprev.t.x_rows128, &ycur.t.store, nullptr, g.count, g.r, g.r, 0};
+            ts.in_fp16 = ts.out_fp16 = true;
+            sym.push_back(ts);
+            f_sym += r3;
           } else {
-            GemmSegSpec cs{&g.mp.rows128, &yprev.q.x_k64, &ycur.q.store, nullptr, g.count, g.r, g.r, 0};
-            cs.in_fp16 = true;  // Q_L in bf16, the type of X_s
-            comb.push_back(cs);
-            f_comb += 2 * n * r * r * r;
             GemmSegSpec es{&ycur.q.x_rows128, &xs.x_k64, &xe.store, sc, g.count, g.r, g.c, 0};
             if (last) es.views = g.d_slot_views;
-            ends.push_back(es);
-            f_end += 2 * n * r * r * cw;
+            comb.push_back(es);
+            f_comb += r2c;
           }
         }
+        gs.out_fp16 = true;
+        gs.diag = gram_diag;
+        gram.push_back(gs);
+        poly.push_back(ps);
+        f_poly += r3;
         continue;
       }
       // direct rounds: X_it in x0 on even rounds, x1 on odd ones
@@ -646,31 +646,32 @@ int run_ns(prm_ctx* c, NsPlan& plan, void* base, bool update_momentum, float bet
       GemmSegSpec gs{&cur.x_rows128, &cur.x_rows128, c_out, sc, g.count, g.r, g.c,
                      g.gram ? 0 : static_cast<int>(g.base_slot)};
       gs.out_fp16 = square;  // C (fp16) for POLY; P (bf16) for COMBINE when c = 0
+      gs.gain = gram_gain;
+      gs.diag = gram_diag;
       gram.push_back(gs);
-      f_gram += 2 * n * r * r * cw;
+      f_gram += r2c;
       const SymMaps& pm = g.gram ? g.mc : (square ? g.mb : g.ma);
       GemmSegSpec cs{&pm.rows128, &cur.x_k64, &nxt.store, sc, g.count, g.r, g.c, 0};
       if (last) cs.views = g.d_slot_views;
       comb.push_back(cs);
-      f_comb += 2 * n * r * r * cw;
+      f_comb += r2c;
     }
     if (square)
       for (const NsRClass& rcl : plan.rclasses) {
         GemmSegSpec ps{&rcl.ma.rows128, &rcl.ma.rows128, &rcl.mb.store, nullptr, rcl.count, rcl.r, rcl.r, 0};
         ps.in_fp16 = true;
+        ps.gain = poly_gain;
+        ps.diag = poly_diag;
         poly.push_back(ps);
         f_poly += 2.0 * rcl.count * double(rcl.r) * rcl.r * rcl.r;
       }
     // 3. the last round applies D = X_steps instead of storing it:
     // W <- W (1 - lr wd) - eta s D, transposed back for tall views
     int rc2;
-    if ((rc2 = run(GEMM_GRAM, gram, gram_epi, PRM_FAMILY_NS_GRAM, f_gram, "gram launch")) != PRM_OK) return rc2;
-    if (square && (rc2 = run(GEMM_POLY, poly, poly_epi, PRM_FAMILY_NS_POLY, f_poly, "poly launch")) != PRM_OK)
-      return rc2;
-    if ((rc2 = run(GEMM_COMBINE, comb, comb_epi, PRM_FAMILY_NS_COMBINE, f_comb, "combine launch")) != PRM_OK)
-      return rc2;
-    if ((rc2 = run(GEMM_COMBINE, ends, comb_epi, PRM_FAMILY_NS_COMBINE, f_end, "combine launch")) != PRM_OK)
-      return rc2;
+    if ((rc2 = run(GEMM_GRAM, gram, PRM_FAMILY_NS_GRAM, f_gram, "gram launch")) != PRM_OK) return rc2;
+    if (square && (rc2 = run(GEMM_POLY, poly, PRM_FAMILY_NS_POLY, f_poly, "poly launch")) != PRM_OK) return rc2;
+    if ((rc2 = run(GEMM_GRAM, sym, PRM_FAMILY_NS_SYM, f_sym, "symmetric update launch")) != PRM_OK) return rc2;
+    if ((rc2 = run(GEMM_COMBINE, comb, PRM_FAMILY_NS_COMBINE, f_comb, "combine launch")) != PRM_OK) return rc2;
   }
   return PRM_OK;
 }
@@ -1130,9 +1131,9 @@ int prm_ns_gram(const uint16_t* X, uint16_t* C, const float* scale, float gain, 
     return PRM_ERR_CUDA;
   GemmSegSpec seg{&mx.x_rows128, &mx.x_rows128, &mc.store, scale, batch, r, c, 0};
   seg.out_fp16 = out_dtype == PRM_FP16;
+  seg.gain = gain;
+  seg.diag = diag;
   GemmEpilogue epi;
-  epi.gain = gain;
-  epi.diag = diag;
   epi.err = ds->d_err;
   epi.num_sms = ds->num_sms;
   return launch_gemm(GEMM_GRAM, &seg, 1, epi, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PRM_OK
@@ -1154,9 +1155,9 @@ int prm_ns_poly(const uint16_t* C, uint16_t* P, float gain, float diag, int in_d
     return PRM_ERR_CUDA;
   GemmSegSpec seg{&mc.rows128, &mc.rows128, &mp.store, nullptr, batch, r, r, 0};
   seg.in_fp16 = in_dtype == PRM_FP16;
+  seg.gain = gain;
+  seg.diag = diag;
   GemmEpilogue epi;
-  epi.gain = gain;
-  epi.diag = diag;
   epi.err = ds->d_err;
   epi.num_sms = ds->num_sms;
   return launch_gemm(GEMM_POLY, &seg, 1, epi, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PRM_OK
