@@ -129,8 +129,10 @@ PRM_API int prm_set_workspace_limit(prm_ctx* ctx, size_t max_bytes);
 /* How the NS5 rounds of the next prm_register_matrices are evaluated. Both
  * forms compute the same five rounds X <- a X + (b A + c A A) X, A = X X^T,
  * of [SMDiT] section "Periodic Row-wise Muon"; they differ in rounding only.
- *   PRM_NS_FORM_AUTO (the default): NS5 groups whose wide shape has
- *     c >= 2 r take the Gram route -- the rounds run in legs of at most
+ *   PRM_NS_FORM_AUTO (the default): NS5 groups whose wide shape r x c is
+ *     wide enough for it to save at least 10 % of the executed flops
+ *     (c >= 1.37 r at r = 2048, c >= 1.9 r for r <= 256; square matrices
+ *     never) take the Gram route -- the rounds run in legs of at most
  *     three; a leg starts from an explicit X_s, iterates only r x r matrices
  *     (Q_j = P_j ... P_1 and T_j = Q_j X_s X_s^T, all symmetric, fp16 with
  *     fp32 accumulation) and ends with X_e = Q_L X_s. Per matrix a leg of L

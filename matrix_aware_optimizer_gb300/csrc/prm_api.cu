@@ -149,8 +149,24 @@ bool view_vec_ok(const View& v) {
   return base && ptrs && g;
 }
 
+// Whether the Gram route (see run_ns) pays for an r x c group: its executed
+// work for the five default rounds (legs of three and two) against the
+// direct rounds', in units of r^3 with rho = c / r and f the executed share
+// of a symmetric product (upper 256 x 256 super-blocks of nb x nb):
+//   Gram   4 rho f + 4 rho + 28 f     direct  10 rho f + 10 f + 10 rho
+// It is taken when at least 10 % cheaper: from c = 1.37 r at r = 2048 (for
+// square matrices it would cost 4 % more), from c = 1.9 r at r <= 256.
+bool gram_route_pays(int64_t r, int64_t c) {
+  const double nb = static_cast<double>((r + 255) / 256);
+  const double f = (nb + 1.0) / (2.0 * nb), rho = static_cast<double>(c) / static_cast<double>(r);
+  const double gram = 4.0 * rho * f + 4.0 * rho + 28.0 * f;
+  const double direct = 10.0 * rho * f + 10.0 * f + 10.0 * rho;
+  return gram <= 0.9 * direct;
+}
+
 // Groups views for the NS5 branch and lays out the shared group workspace.
-// `form` PRM_NS_FORM_AUTO puts the groups with c >= 2 r on the Gram route.
+// `form` PRM_NS_FORM_AUTO puts the groups for which gram_route_pays on the
+// Gram route.
 void build_ns_plan(const std::vector<View>& views, NsPlan& plan, int form) {
   std::map<std::pair<int64_t, int64_t>, size_t> index;
   for (const View& v0 : views) {
@@ -197,7 +213,7 @@ void build_ns_plan(const std::vector<View>& views, NsPlan& plan, int form) {
     off += align_up(static_cast<size_t>(g.count) * 4, 256);
     g.off_partials = off;
     off += align_up(static_cast<size_t>(g.count) * g.slots * 4, 256);
-    g.gram = form == PRM_NS_FORM_AUTO && g.c >= 2 * g.r;
+    g.gram = form == PRM_NS_FORM_AUTO && gram_route_pays(g.r, g.c);
     if (g.gram) {
       const size_t cb = align_up(static_cast<size_t>(g.count) * g.r * g.ldr * 2, 256);
       const size_t yb = align_up(static_cast<size_t>(g.count) * g.r * 2 * g.ldr * 2, 256);

@@ -28,11 +28,12 @@ class PeriodicRowMuon:
                        in sequential sub-plans that fit it. 0 (default) is the
                        library's automatic policy (whole plans up to 16 GiB,
                        4 GiB sub-plans above), -1 no cap.
-    ns_form          : "auto" (default): NS5 groups with c >= 2 r (wide
-                       orientation r x c) iterate r x r matrices in legs of
-                       at most three rounds (the Gram route, ~30 % fewer
-                       flops at c = 4 r); "direct": every group runs the
-                       rounds on X itself. Same rounds, different rounding.
+    ns_form          : "auto" (default): NS5 groups wide enough to gain
+                       (wide orientation r x c, c >= 1.37 r at r = 2048)
+                       iterate r x r matrices in legs of at most three rounds
+                       (the Gram route, ~40 % fewer flops at c = 4 r);
+                       "direct": every group runs the rounds on X itself.
+                       Same rounds, different rounding.
     workspace        : optional uint8 CUDA tensor to use as the scratch instead
                        of allocating one (at least workspace_bytes large).
                        Optimizers whose steps are ordered on one stream may

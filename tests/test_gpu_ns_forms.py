@@ -4,8 +4,8 @@ prescribed singular spectra.
 Both forms compute the same five rounds X <- a X + (b A + c A A) X of
 "Scaling Muon for Diffusion Transformers" (section "Periodic Row-wise Muon");
 they differ in rounding only. The direct form rounds X to bf16 after every
-round; the Gram route (c >= 2 r) iterates r x r matrices in fp16 and rounds X
-twice. Either way the quintic's slope (3.44 near 0) amplifies rounding noise
+round; the Gram route (wide groups) iterates r x r matrices in fp16 and
+rounds X twice. Either way the quintic's slope (3.44 near 0) amplifies rounding noise
 along the input's smallest singular directions, so ill-conditioned inputs
 land far from the fp64 polar factor for both forms; the requirement here is
 that the Gram route is never worse than the direct form (a 25 % + 2e-3 margin
