@@ -48,6 +48,19 @@ cudaError_t launch_rownorm_tall(const View* d_views, int count, int64_t rows, in
                                 bool grad_bf16, StepScalars s, float* partials, float* inv,
                                 cudaStream_t stream);
 
+// Tall step in one launch (16-byte aligned views with cols % 4 == 0): a
+// queue of column-stripe tiles, each stripe's update following its momentum
+// pass closely enough to read M back from L2 (see rownorm.cu). Scratch:
+// partials, inverse norms and a flag block (zeroed by the launch itself).
+// A timed-out wait sets *err to the timeout code.
+struct TallFusedScratch {
+  size_t partials_bytes = 0, inv_bytes = 0, flag_bytes = 0;
+};
+TallFusedScratch tall_fused_scratch(int count, int64_t rows, int64_t cols);
+cudaError_t launch_rownorm_tall_fused(const View* d_views, int count, int64_t rows, int64_t cols, bool grad_bf16,
+                                      StepScalars s, float* partials, float* inv, void* flags, int* err,
+                                      int num_sms, cudaStream_t stream);
+
 // ---- refresh (NS5) branch ---------------------------------------------
 // Momentum update + bf16 pack into X (wide: same orientation; tall:
 // transposed) + per-view Frobenius partial sums (partials: count * slots).

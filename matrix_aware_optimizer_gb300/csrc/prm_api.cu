@@ -43,7 +43,9 @@ struct LaunchSet {
   bool vec_ok = true;
   std::vector<View> views;
   View* d_views = nullptr;
-  size_t off_partials = 0, off_inv = 0;  // tall RowNorm scratch (relative to workspace base)
+  // tall RowNorm scratch (relative to workspace base); off_flags only for
+  // the one-launch (vec_ok) form
+  size_t off_partials = 0, off_inv = 0, off_flags = 0;
 };
 
 // Maps of one Gram-route Y buffer: per matrix an r x (ldr + r) fp16 array
@@ -706,11 +708,16 @@ int run_rownorm(prm_ctx* c, void* base, StepScalars sc, cudaStream_t stream) {
   for (auto& s : c->rn.tall) {
     const double bytes = static_cast<double>(s.views.size()) * s.rows * s.cols * (s.bf16 ? 18.0 : 20.0);
     const size_t ev = c->prof.begin(stream);
-    e = launch_rownorm_tall(s.d_views, static_cast<int>(s.views.size()), s.rows, s.cols, s.vec_ok, s.bf16, sc,
-                            reinterpret_cast<float*>(b + s.off_partials), reinterpret_cast<float*>(b + s.off_inv),
-                            stream);
+    float* partials = reinterpret_cast<float*>(b + s.off_partials);
+    float* inv = reinterpret_cast<float*>(b + s.off_inv);
+    const int n = static_cast<int>(s.views.size());
+    if (s.vec_ok)
+      e = launch_rownorm_tall_fused(s.d_views, n, s.rows, s.cols, s.bf16, sc, partials, inv, b + s.off_flags,
+                                    c->d_err, c->num_sms, stream);
+    else
+      e = launch_rownorm_tall(s.d_views, n, s.rows, s.cols, false, s.bf16, sc, partials, inv, stream);
     if (e != cudaSuccess) return cuda_fail(c, e, "rownorm tall launch");
-    c->prof.end(ev, PRM_FAMILY_ROWNORM_TALL, 3, bytes, stream);
+    c->prof.end(ev, PRM_FAMILY_ROWNORM_TALL, s.vec_ok ? 1 : 3, bytes, stream);
   }
   return PRM_OK;
 }
@@ -848,6 +855,16 @@ int prm_register_matrices(prm_ctx* c, const prm_matrix_desc* d, int count, int m
   for (const View& v : full) add_to_sets(v.rows <= v.cols ? c->rn.wide : c->rn.tall, v);
   size_t off = 0;
   for (auto& s : c->rn.tall) {
+    if (s.vec_ok) {
+      const TallFusedScratch t = tall_fused_scratch(static_cast<int>(s.views.size()), s.rows, s.cols);
+      s.off_partials = off;
+      off += align_up(t.partials_bytes, 256);
+      s.off_inv = off;
+      off += align_up(t.inv_bytes, 256);
+      s.off_flags = off;
+      off += align_up(t.flag_bytes, 256);
+      continue;
+    }
     s.off_partials = off;
     off += align_up(s.views.size() * tall_row_blocks(s.rows) * s.cols * 4, 256);
     s.off_inv = off;
@@ -1025,6 +1042,18 @@ int prm_debug_last_direction(prm_ctx* c, int idx, float* host_out) {
     const LaunchSet& s = sets.front();
     if (v.rows <= v.cols) {
       e = launch_rownorm_wide(s.d_views, 1, v.rows, v.cols, s.vec_ok, false, sc, st);
+    } else if (s.vec_ok) {
+      // the step's own one-launch kernel, so that D matches what it applied
+      const TallFusedScratch t = tall_fused_scratch(1, v.rows, v.cols);
+      float* d_part = static_cast<float*>(dev_alloc(t.partials_bytes));
+      float* d_inv = static_cast<float*>(dev_alloc(t.inv_bytes));
+      void* d_flags = dev_alloc(t.flag_bytes);
+      if (d_part == nullptr || d_inv == nullptr || d_flags == nullptr) {
+        free_sets(sets);
+        return finish(fail(c, PRM_ERR_OOM, "no device memory for scratch"));
+      }
+      e = launch_rownorm_tall_fused(s.d_views, 1, v.rows, v.cols, false, sc, d_part, d_inv, d_flags, c->d_err,
+                                    c->num_sms, st);
     } else {
       const size_t pb = static_cast<size_t>(tall_row_blocks(v.rows)) * v.cols * sizeof(float);
       float* d_part = static_cast<float*>(dev_alloc(pb));
@@ -1033,7 +1062,7 @@ int prm_debug_last_direction(prm_ctx* c, int idx, float* host_out) {
         free_sets(sets);
         return finish(fail(c, PRM_ERR_OOM, "no device memory for scratch"));
       }
-      e = launch_rownorm_tall(s.d_views, 1, v.rows, v.cols, s.vec_ok, false, sc, d_part, d_inv, st);
+      e = launch_rownorm_tall(s.d_views, 1, v.rows, v.cols, false, false, sc, d_part, d_inv, st);
     }
     if (e == cudaSuccess) e = cudaStreamSynchronize(st);
     free_sets(sets);

@@ -305,3 +305,42 @@ def test_argument_errors_on_device():
         assert N.prm_sync_status(ctx, 0) == N.PRM_OK
     finally:
         N.prm_destroy(ctx)
+
+
+@pytest.mark.parametrize("gdtype", [torch.float32, torch.bfloat16])
+def test_tall_rownorm_one_launch_ragged(gdtype):
+    """The one-launch tall RowNorm: stripes of 128 columns with a ragged last
+    stripe (388 = 3 x 128 + 4, 132 = 128 + 4), row tiles of 64 with ragged
+    last tiles (1000, 4100, 130 rows), several views in one launch; checked
+    against the oracle, and bit for bit against a second run (the column
+    sums are reduced in a fixed order whichever tile finishes a stripe)."""
+    shapes = [(1000, 388), (1000, 388), (4100, 132), (130, 64), (130, 64)]
+    gen = torch.Generator().manual_seed(13)
+    Gh = [torch.randn(s, generator=gen).to(gdtype) for s in shapes]
+    M0 = [torch.randn(s, generator=gen) * 0.5 for s in shapes]
+    W0 = [torch.randn(s, generator=gen) * 0.02 for s in shapes]
+    kw = dict(K=3, gamma=0.15, lr=0.02, wd=0.01, beta=0.95, eps=1e-8)
+
+    def run():
+        Ws = [w.cuda() for w in W0]
+        Ms = [m.cuda() for m in M0]
+        Gs = [g.cuda() for g in Gh]
+        opt = PeriodicRowMuon(Ws, Ms, Gs)
+        opt.workspace.fill_(0xFF)
+        assert opt.step(1, **kw) == 0
+        opt.sync_status()
+        opt.close()
+        return [w.cpu() for w in Ws], [m.cpu() for m in Ms]
+
+    Wa, Ma = run()
+    Wb, Mb = run()
+    for i, (m, n) in enumerate(shapes):
+        assert torch.equal(Wa[i], Wb[i]) and torch.equal(Ma[i], Mb[i])
+        W1, M1, D1, rho = O.prmuon_step(W0[i].double().numpy(), M0[i].double().numpy(),
+                                        Gh[i].double().numpy(), 1, **kw)
+        assert rho == 0
+        assert rel_frob(Ma[i].double().numpy(), M1) <= TOL_M, i
+        assert rel_frob(Wa[i].double().numpy(), W1) <= TOL_W_ROWNORM, i
+        Dg = direction_from_update(W0[i].double().numpy(), Wa[i].double().numpy(), kw["lr"], kw["wd"],
+                                   kw["lr"] * kw["gamma"], O.lr_shape_scale(m, n))
+        assert rel_frob(Dg, D1) <= TOL_D_ROWNORM, i
