@@ -56,6 +56,7 @@ cudaError_t launch_rownorm_tall(const View* d_views, int count, int64_t rows, in
 struct TallFusedScratch {
   size_t partials_bytes = 0, inv_bytes = 0, flag_bytes = 0;
 };
+bool tall_fused_fits(int count, int64_t rows, int64_t cols);  // queue and offsets within 32-bit limits
 TallFusedScratch tall_fused_scratch(int count, int64_t rows, int64_t cols);
 cudaError_t launch_rownorm_tall_fused(const View* d_views, int count, int64_t rows, int64_t cols, bool grad_bf16,
                                       StepScalars s, float* partials, float* inv, void* flags, int* err,

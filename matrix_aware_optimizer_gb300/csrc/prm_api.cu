@@ -43,8 +43,9 @@ struct LaunchSet {
   bool vec_ok = true;
   std::vector<View> views;
   View* d_views = nullptr;
-  // tall RowNorm scratch (relative to workspace base); off_flags only for
-  // the one-launch (vec_ok) form
+  // tall RowNorm: the one-launch form (aligned views within its size limits)
+  // or three launches; scratch offsets relative to the workspace base
+  bool fused = false;
   size_t off_partials = 0, off_inv = 0, off_flags = 0;
 };
 
@@ -711,13 +712,13 @@ int run_rownorm(prm_ctx* c, void* base, StepScalars sc, cudaStream_t stream) {
     float* partials = reinterpret_cast<float*>(b + s.off_partials);
     float* inv = reinterpret_cast<float*>(b + s.off_inv);
     const int n = static_cast<int>(s.views.size());
-    if (s.vec_ok)
+    if (s.fused)
       e = launch_rownorm_tall_fused(s.d_views, n, s.rows, s.cols, s.bf16, sc, partials, inv, b + s.off_flags,
                                     c->d_err, c->num_sms, stream);
     else
-      e = launch_rownorm_tall(s.d_views, n, s.rows, s.cols, false, s.bf16, sc, partials, inv, stream);
+      e = launch_rownorm_tall(s.d_views, n, s.rows, s.cols, s.vec_ok, s.bf16, sc, partials, inv, stream);
     if (e != cudaSuccess) return cuda_fail(c, e, "rownorm tall launch");
-    c->prof.end(ev, PRM_FAMILY_ROWNORM_TALL, s.vec_ok ? 1 : 3, bytes, stream);
+    c->prof.end(ev, PRM_FAMILY_ROWNORM_TALL, s.fused ? 1 : 3, bytes, stream);
   }
   return PRM_OK;
 }
@@ -855,7 +856,8 @@ int prm_register_matrices(prm_ctx* c, const prm_matrix_desc* d, int count, int m
   for (const View& v : full) add_to_sets(v.rows <= v.cols ? c->rn.wide : c->rn.tall, v);
   size_t off = 0;
   for (auto& s : c->rn.tall) {
-    if (s.vec_ok) {
+    s.fused = s.vec_ok && tall_fused_fits(static_cast<int>(s.views.size()), s.rows, s.cols);
+    if (s.fused) {
       const TallFusedScratch t = tall_fused_scratch(static_cast<int>(s.views.size()), s.rows, s.cols);
       s.off_partials = off;
       off += align_up(t.partials_bytes, 256);
@@ -981,6 +983,14 @@ int prm_step(prm_ctx* c, int64_t t, int K, float gamma, float lr, float wd, floa
   return PRM_OK;
 }
 
+// Whether the RowNorm step ran the one-launch tall kernel for this view's
+// launch set.
+static bool step_used_fused(const prm_ctx* c, const View& v) {
+  for (const auto& s : c->rn.tall)
+    if (s.rows == v.rows && s.cols == v.cols && s.bf16 == (v.grad_bf16 != 0)) return s.fused;
+  return false;
+}
+
 // Recomputes the direction D of the last step for one matrix from its
 // momentum (which, after the step, is the M_t the direction was taken from)
 // with the step's own kernels, on scratch buffers: the NS5 branch runs the
@@ -1042,7 +1052,7 @@ int prm_debug_last_direction(prm_ctx* c, int idx, float* host_out) {
     const LaunchSet& s = sets.front();
     if (v.rows <= v.cols) {
       e = launch_rownorm_wide(s.d_views, 1, v.rows, v.cols, s.vec_ok, false, sc, st);
-    } else if (s.vec_ok) {
+    } else if (step_used_fused(c, v) && tall_fused_fits(1, v.rows, v.cols)) {
       // the step's own one-launch kernel, so that D matches what it applied
       const TallFusedScratch t = tall_fused_scratch(1, v.rows, v.cols);
       float* d_part = static_cast<float*>(dev_alloc(t.partials_bytes));
@@ -1062,7 +1072,7 @@ int prm_debug_last_direction(prm_ctx* c, int idx, float* host_out) {
         free_sets(sets);
         return finish(fail(c, PRM_ERR_OOM, "no device memory for scratch"));
       }
-      e = launch_rownorm_tall(s.d_views, 1, v.rows, v.cols, false, false, sc, d_part, d_inv, st);
+      e = launch_rownorm_tall(s.d_views, 1, v.rows, v.cols, s.vec_ok, false, sc, d_part, d_inv, st);
     }
     if (e == cudaSuccess) e = cudaStreamSynchronize(st);
     free_sets(sets);

@@ -597,6 +597,12 @@ cudaError_t launch_rownorm_wide(const View* d_views, int count, int64_t rows, in
 
 int64_t tall_row_blocks(int64_t rows) { return (rows + TALL_RB - 1) / TALL_RB; }
 
+bool tall_fused_fits(int count, int64_t rows, int64_t cols) {
+  const int64_t S = static_cast<int64_t>(count) * ((cols + FT_COLS - 1) / FT_COLS);
+  const int64_t R = (rows + FT_TILE_ROWS - 1) / FT_TILE_ROWS;
+  return 2 * S * R < (int64_t(1) << 31) - 1 && static_cast<int64_t>(FT_TILE_ROWS) * cols < (int64_t(1) << 31);
+}
+
 TallFusedScratch tall_fused_scratch(int count, int64_t rows, int64_t cols) {
   TallFusedScratch t;
   const int64_t S = static_cast<int64_t>(count) * ((cols + FT_COLS - 1) / FT_COLS);
@@ -619,9 +625,8 @@ cudaError_t launch_rownorm_tall_fused(const View* d_views, int count, int64_t ro
   a.spv = static_cast<int>((cols + FT_COLS - 1) / FT_COLS);
   a.S = count * a.spv;
   a.R = static_cast<int>((rows + FT_TILE_ROWS - 1) / FT_TILE_ROWS);
+  if (!tall_fused_fits(count, rows, cols)) return cudaErrorInvalidValue;
   const int64_t total = 2 * static_cast<int64_t>(a.S) * a.R;
-  if (total >= (int64_t(1) << 31) - 1) return cudaErrorInvalidValue;
-  if (static_cast<int64_t>(FT_TILE_ROWS) * cols >= (int64_t(1) << 31)) return cudaErrorInvalidValue;
   a.total = static_cast<int>(total);
   const int64_t grid = std::min<int64_t>(total, static_cast<int64_t>(std::max(1, num_sms)) * FT_CTAS_PER_SM);
   // the lag covers the CTAs' window on the queue, so updates rarely wait
