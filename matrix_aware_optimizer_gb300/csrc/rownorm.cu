@@ -71,10 +71,6 @@ __device__ __forceinline__ float load_grad1(const void* G, int64_t off) {
 
 // ------------------------------------------------------------ wide rows
 // Bulk prefetch of `bytes` (multiple of 16, 16-byte aligned) into L2.
-__device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(p)), "r"(bytes)
-               : "memory");
-}
 
 // One CTA per row; each thread keeps NV float4 (or 4*NV floats) of the
 // updated momentum in registers across the block reduction. Short rows also
