@@ -1,5 +1,6 @@
 """Host-side logic of the benchmark that needs no GPU: the clock summary
-taken from nvidia-smi samples during the timed region."""
+taken from nvidia-smi samples during the timed region, and the metric's
+NS5 FLOP count."""
 import bench
 
 
@@ -28,3 +29,19 @@ def test_malformed_lines_are_skipped():
     assert bench.summarize_clocks([(0.0, "[N/A]"), (0.1, "garbage")]) is None
     lines = [(0.0, "0, [N/A], 2070, 1.0, 0x0, Not Active, Not Active, Not Active, Not Active"), (0.1, _line(1650))]
     assert bench.summarize_clocks(lines)["samples"] == 1
+
+
+def test_ns5_algorithmic_flop_counts():
+    """The metric's NS5 count, 5 (4 r^2 c + 2 r^3) per matrix, over the DiT
+    sets: 5.884e13 per 1.3B refresh, 1.804e15 per 15B refresh, 2.774e13 per
+    MuonBP block step (blocks of the 1.3B set along the long side)."""
+    from matrix_aware_optimizer_gb300 import synth
+    one = sum(bench._ns_flops(*s) for s in synth.MATRIX_SETS["dit_1p3b"].shapes)
+    big = sum(bench._ns_flops(*s) for s in synth.MATRIX_SETS["dit_15b"].shapes)
+    ms = synth.MATRIX_SETS["dit_1p3b_muonbp"]
+    blk = sum(bench._ns_flops(*b) for s in ms.shapes for b in bench._block_shapes(s[0], s[1], ms.blocks))
+    assert one == 58841051955200
+    assert abs(big / 1.804e15 - 1) < 1e-3
+    assert abs(blk / 2.774e13 - 1) < 1e-3
+    # a square matrix: 5 (4 + 2) r^3
+    assert bench._ns_flops(64, 64) == 30 * 64 ** 3
