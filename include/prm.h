@@ -333,8 +333,10 @@ PRM_API int prm_newton_schulz_workspace(int batch, int64_t m, int64_t n, size_t*
 
 /* out[i] = NS_steps(in[i]) for `batch` fp32 matrices of m x n (row-major,
  * contiguous, device), tall inputs orthogonalised transposed; the result is
- * fp32. steps >= 1, ns_coeffs NULL for the default quintic. The call
- * synchronises `stream` before returning (its launch tables are freed). */
+ * fp32. steps >= 1, ns_coeffs NULL for the default quintic. Evaluated in the
+ * PRM_NS_FORM_AUTO form (prm_set_ns_form): shapes wide enough take the Gram
+ * route, in legs of at most three rounds. The call synchronises `stream`
+ * before returning (its launch tables are freed). */
 PRM_API int prm_newton_schulz(const float* in, float* out, int batch, int64_t m, int64_t n,
                       const float* ns_coeffs, int steps, void* workspace, size_t ws_bytes,
                       void* stream);
