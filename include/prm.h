@@ -213,6 +213,18 @@ PRM_API int prm_sync_status(prm_ctx* ctx, void* stream);
  * range, no step since registration), NOT_REGISTERED, OOM, CUDA, TIMEOUT. */
 PRM_API int prm_debug_last_direction(prm_ctx* ctx, int idx, float* host_out);
 
+/* Test aid for the bounded waits: in the next RowNorm step, the one-launch
+ * tall-matrix kernel does not publish the inverse column norms of column
+ * stripe `stripe` (stripes of 128 columns, numbered across the tall matrices
+ * of one shape in registration order; a stripe beyond them withholds
+ * nothing), so that stripe's update tiles wait wait_limit_s seconds (in
+ * (0, 2]) for a flag that nothing sets, give up and leave that stripe of W
+ * unchanged; prm_sync_status then reports PRM_ERR_TIMEOUT and the context
+ * stays usable. The momentum update of the step completes. No effect on
+ * refresh steps (it stays armed for the next RowNorm step) or on views that
+ * take the three-launch form. Errors: INVALID_ARG. */
+PRM_API int prm_debug_withhold_tall_norms(prm_ctx* ctx, int stripe, double wait_limit_s);
+
 /* ---- allocation-free RowNorm step for one tall matrix -------------------
  * The pages have no counterpart to this call; it exists for callers that
  * cannot allocate device memory when the update runs (a host process whose

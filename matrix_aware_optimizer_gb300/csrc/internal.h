@@ -52,7 +52,9 @@ cudaError_t launch_rownorm_tall(const View* d_views, int count, int64_t rows, in
 // queue of column-stripe tiles, each stripe's update following its momentum
 // pass closely enough to read M back from L2 (see rownorm.cu). Scratch:
 // partials, inverse norms and a flag block (zeroed by the launch itself).
-// A timed-out wait sets *err to the timeout code.
+// A timed-out wait sets *err to the timeout code. Test aid: withhold_stripe
+// >= 0 keeps that stripe's inverse norms unpublished, so its update tiles
+// give up after wait_ns (0: the default 2 s limit) and leave W unchanged.
 struct TallFusedScratch {
   size_t partials_bytes = 0, inv_bytes = 0, flag_bytes = 0;
 };
@@ -60,7 +62,8 @@ bool tall_fused_fits(int count, int64_t rows, int64_t cols);  // queue and offse
 TallFusedScratch tall_fused_scratch(int count, int64_t rows, int64_t cols);
 cudaError_t launch_rownorm_tall_fused(const View* d_views, int count, int64_t rows, int64_t cols, bool grad_bf16,
                                       StepScalars s, float* partials, float* inv, void* flags, int* err,
-                                      int num_sms, cudaStream_t stream);
+                                      int num_sms, cudaStream_t stream, int withhold_stripe = -1,
+                                      uint64_t wait_ns = 0);
 
 // ---- refresh (NS5) branch ---------------------------------------------
 // Momentum update + bf16 pack into X (wide: same orientation; tall:

@@ -365,6 +365,10 @@ struct prm_ctx {
   std::vector<NsPlan> ns_full, ns_blocks;  // sequential sub-plans (one unless a workspace cap splits them)
   size_t ws_limit = 0;                     // prm_set_workspace_limit; 0 = automatic, SIZE_MAX = no cap
   int ns_form = PRM_NS_FORM_AUTO;          // prm_set_ns_form
+  struct {
+    int stripe = -1;                       // prm_debug_withhold_tall_norms: for the next RowNorm step only
+    uint64_t wait_ns = 0;
+  } withhold;
   std::vector<View> full;                  // registered matrices, in registration order
   struct {
     bool valid = false;
@@ -714,12 +718,14 @@ int run_rownorm(prm_ctx* c, void* base, StepScalars sc, cudaStream_t stream) {
     const int n = static_cast<int>(s.views.size());
     if (s.fused)
       e = launch_rownorm_tall_fused(s.d_views, n, s.rows, s.cols, s.bf16, sc, partials, inv, b + s.off_flags,
-                                    c->d_err, c->num_sms, stream);
+                                    c->d_err, c->num_sms, stream, c->withhold.stripe, c->withhold.wait_ns);
     else
       e = launch_rownorm_tall(s.d_views, n, s.rows, s.cols, s.vec_ok, s.bf16, sc, partials, inv, stream);
     if (e != cudaSuccess) return cuda_fail(c, e, "rownorm tall launch");
     c->prof.end(ev, PRM_FAMILY_ROWNORM_TALL, s.fused ? 1 : 3, bytes, stream);
   }
+  c->withhold.stripe = -1;  // the test aid covers one step
+  c->withhold.wait_ns = 0;
   return PRM_OK;
 }
 
@@ -902,6 +908,15 @@ int prm_set_ns_form(prm_ctx* c, int form) {
   if (c == nullptr) return fail(nullptr, PRM_ERR_INVALID_ARG, "ctx is NULL");
   if (form != PRM_NS_FORM_AUTO && form != PRM_NS_FORM_DIRECT) return fail(c, PRM_ERR_INVALID_ARG, "unknown NS5 form");
   c->ns_form = form;
+  return PRM_OK;
+}
+
+int prm_debug_withhold_tall_norms(prm_ctx* c, int stripe, double wait_limit_s) {
+  if (c == nullptr) return fail(nullptr, PRM_ERR_INVALID_ARG, "ctx is NULL");
+  if (stripe < 0 || !(wait_limit_s > 0.0) || wait_limit_s > 2.0)
+    return fail(c, PRM_ERR_INVALID_ARG, "stripe must be >= 0 and wait_limit_s in (0, 2]");
+  c->withhold.stripe = stripe;
+  c->withhold.wait_ns = static_cast<uint64_t>(wait_limit_s * 1e9);
   return PRM_OK;
 }
 

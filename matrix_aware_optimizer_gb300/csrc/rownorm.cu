@@ -331,6 +331,8 @@ struct FusedTall {
   int* counters;     // [S] phase-1 tiles done
   int* ready;        // [S] inverse norms published
   int* err;
+  int withhold;      // test aid: stripe whose norms are not published (-1: none)
+  uint64_t wait_ns;  // limit of one update tile's wait
 };
 
 // Queue position -> (phase 3?, stripe, row block); the queue holds fewer
@@ -440,7 +442,7 @@ __global__ void __launch_bounds__(FT_THREADS, FT_CTAS_PER_SM) tall_fused_kernel(
         if (!ok) {
           const uint64_t t0 = global_timer_ns();
           while (!(ok = ld_acquire_gpu(a.ready + s) != 0)) {
-            if (global_timer_ns() - t0 > FT_WAIT_LIMIT_NS) {
+            if (global_timer_ns() - t0 > a.wait_ns) {
               atomicExch(a.err, DEV_ERR_TIMEOUT);
               break;
             }
@@ -546,7 +548,7 @@ __global__ void __launch_bounds__(FT_THREADS, FT_CTAS_PER_SM) tall_fused_kernel(
           a.inv[static_cast<int64_t>(s) * FT_COLS + threadIdx.x] = 1.f / fmaxf(sqrtf(tot), a.eps);
         }
         __syncthreads();
-        if (threadIdx.x == 0) st_release_gpu(a.ready + s, 1);
+        if (threadIdx.x == 0 && s != a.withhold) st_release_gpu(a.ready + s, 1);
       }
     }
     __syncthreads();  // tile_sh, flag_sh and red are rewritten by the next tile
@@ -611,7 +613,7 @@ TallFusedScratch tall_fused_scratch(int count, int64_t rows, int64_t cols) {
 
 cudaError_t launch_rownorm_tall_fused(const View* d_views, int count, int64_t rows, int64_t cols, bool grad_bf16,
                                       StepScalars s, float* partials, float* inv, void* flags, int* err,
-                                      int num_sms, cudaStream_t stream) {
+                                      int num_sms, cudaStream_t stream, int withhold_stripe, uint64_t wait_ns) {
   if (count == 0 || rows == 0) return cudaSuccess;
   const TallFusedScratch t = tall_fused_scratch(count, rows, cols);
   FusedTall a{};
@@ -637,6 +639,8 @@ cudaError_t launch_rownorm_tall_fused(const View* d_views, int count, int64_t ro
   a.counters = reinterpret_cast<int*>(static_cast<char*>(flags) + sizeof(unsigned long long));
   a.ready = a.counters + a.S;
   a.err = err;
+  a.withhold = withhold_stripe;
+  a.wait_ns = (wait_ns == 0 || wait_ns > FT_WAIT_LIMIT_NS) ? FT_WAIT_LIMIT_NS : wait_ns;
   cudaError_t e = cudaMemsetAsync(flags, 0, t.flag_bytes, stream);
   if (e != cudaSuccess) return e;
   if (grad_bf16)

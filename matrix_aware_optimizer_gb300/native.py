@@ -67,6 +67,7 @@ SIGNATURES = {
     "prm_workspace_bytes": (c_int, [c_void_p, POINTER(c_size_t)]),
     "prm_set_workspace_limit": (c_int, [c_void_p, c_size_t]),
     "prm_set_ns_form": (c_int, [c_void_p, c_int]),
+    "prm_debug_withhold_tall_norms": (c_int, [c_void_p, c_int, ctypes.c_double]),
     "prm_set_workspace": (c_int, [c_void_p, c_void_p, c_size_t]),
     "prm_step": (c_int, [c_void_p, c_int64, c_int, c_float, c_float, c_float, c_float, c_float,
                          POINTER(c_float), c_int, c_void_p]),
@@ -186,6 +187,10 @@ def prm_sync_status(ctx, stream: int = 0) -> int:
 def prm_debug_last_direction(ctx, idx: int, host_out: int) -> None:
     """host_out: address of rows * cols writable host floats."""
     check(load().prm_debug_last_direction(ctx, idx, c_void_p(host_out)), "prm_debug_last_direction", ctx)
+
+
+def prm_debug_withhold_tall_norms(ctx, stripe: int, wait_limit_s: float) -> None:
+    check(load().prm_debug_withhold_tall_norms(ctx, stripe, wait_limit_s), "prm_debug_withhold_tall_norms", ctx)
 
 
 def prm_profile(ctx, enable: bool) -> None:
