@@ -48,7 +48,7 @@ def parse_args():
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default="dit_1p3b",
                    choices=["dit_1p3b", "dit_15b", "dit_1p3b_muonbp", "dit_block_d2048", "dit_1p3b_4blk",
-                            "dit_1p3b_4blk_muonbp"])
+                            "dit_1p3b_4blk_muonbp", "dit_1p3b_mlp_up"])
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-adamw", action="store_true")

@@ -98,6 +98,12 @@ MATRIX_SETS: Dict[str, MatrixSet] = {
         mode="muonbp", blocks=8, lr=0.02 * 0.8, gamma=1.25,
         description="MuonBP on 4 blocks of the 1.3B-shaped set: a profiling case with the full "
                     "set's block shapes (768, 256 and 1024 x 2048 NS5 groups) on a few GB"),
+    "dit_1p3b_mlp_up": MatrixSet(
+        name="dit_1p3b_mlp_up",
+        shapes=((8192, 2048),) * 24,
+        grad_dtype=GRAD_BF16, grad_std=1e-3, steps=30,
+        description="the 24 tall mlp-up matrices of the 1.3B-shaped set (402.7 M params): a profiling "
+                    "case for the tall RowNorm kernel"),
     "dit_15b": MatrixSet(
         name="dit_15b",
         shapes=_dit_set(5120, 48, None),
