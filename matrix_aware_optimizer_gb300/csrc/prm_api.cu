@@ -49,11 +49,10 @@ struct LaunchSet {
   size_t off_partials = 0, off_inv = 0, off_flags = 0;
 };
 
-// Maps of one Gram-route Y buffer: per matrix an r x (ldr + r) fp16 array
-// [Q | T] (pitch 2 ldr), T starting at column ldr; `full` spans both halves
-// (the padding columns between them are computed and never read).
+// Maps of one Gram-route Y buffer: per matrix Q and T side by side (r rows,
+// pitch 2 ldr fp16 elements, T starting at column ldr).
 struct YMaps {
-  NsMaps q, t, full;
+  NsMaps q, t;
 };
 
 // Same wide-orientation shape r x c: one batch for the GRAM and COMBINE
@@ -488,7 +487,6 @@ int bind_maps(prm_ctx* c, NsPlan& plan, void* base) {
         const int64_t ld = 2 * g.ldr;
         if (e == 0) e = encode_x_maps(&yy.first->q, y, g.count, g.r, g.r, ld);
         if (e == 0) e = encode_x_maps(&yy.first->t, y + g.ldr * 2, g.count, g.r, g.r, ld);
-        if (e == 0) e = encode_x_maps(&yy.first->full, y, g.count, g.r, g.ldr + g.r, ld);
       }
     } else {
       const NsRClass& rc = plan.rclasses[g.rclass];
