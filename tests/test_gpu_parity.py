@@ -344,3 +344,18 @@ def test_tall_rownorm_one_launch_ragged(gdtype):
         Dg = direction_from_update(W0[i].double().numpy(), Wa[i].double().numpy(), kw["lr"], kw["wd"],
                                    kw["lr"] * kw["gamma"], O.lr_shape_scale(m, n))
         assert rel_frob(Dg, D1) <= TOL_D_ROWNORM, i
+
+
+@pytest.mark.parametrize("steps", [1, 2, 3, 4, 6, 7])
+def test_newton_schulz_round_counts(steps):
+    """Other round counts than five: the Gram route splits them into legs of
+    at most three (1: one direct-style round; 4: three + one; 7: three +
+    three + one, the third leg back in the first X buffer); a 320 x 400
+    batch member runs the direct rounds."""
+    gen = torch.Generator().manual_seed(100 + steps)
+    for shape in [(2, 192, 640), (1, 320, 400)]:
+        X = torch.randn(*shape, generator=gen)
+        D = newton_schulz(X.cuda(), steps=steps).cpu().double().numpy()
+        for i in range(shape[0]):
+            ref = O.newton_schulz(X[i].double().numpy(), steps=steps)
+            assert rel_frob(D[i], ref) <= TOL_D_NS5, (shape, steps, i, rel_frob(D[i], ref))
