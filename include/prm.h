@@ -146,6 +146,12 @@ PRM_API int prm_set_workspace_limit(prm_ctx* ctx, size_t max_bytes);
 #define PRM_NS_FORM_DIRECT 1
 PRM_API int prm_set_ns_form(prm_ctx* ctx, int form);
 
+/* Pure helper: 1 if the planner puts an m x n matrix's NS5 on the Gram route
+ * under `form`, 0 for the direct rounds; -PRM_ERR_INVALID_ARG for m or n < 1
+ * or an unknown form. (The route also needs c != 0 in ns_coeffs at step
+ * time.) */
+PRM_API int prm_ns_route(int64_t m, int64_t n, int form);
+
 /* Bytes of device scratch the registered plan needs (NS5 operands in bf16,
  * Gram / polynomial matrices, norm and column partial sums). *bytes (host)
  * receives the size; 0 when nothing is registered. */

@@ -939,6 +939,11 @@ int prm_set_workspace(prm_ctx* c, void* dev_ptr, size_t bytes) {
   return PRM_OK;
 }
 
+int prm_ns_route(int64_t m, int64_t n, int form) {
+  if (m < 1 || n < 1 || (form != PRM_NS_FORM_AUTO && form != PRM_NS_FORM_DIRECT)) return -PRM_ERR_INVALID_ARG;
+  return (form == PRM_NS_FORM_AUTO && gram_route_pays(std::min(m, n), std::max(m, n))) ? 1 : 0;
+}
+
 int prm_branch(int64_t t, int K, int mode) {
   if (t < 0 || K < 1 || (mode != PRM_MODE_PRMUON && mode != PRM_MODE_MUONBP)) return -PRM_ERR_INVALID_ARG;
   return (t % K == 0) ? 1 : 0;

@@ -67,6 +67,7 @@ SIGNATURES = {
     "prm_workspace_bytes": (c_int, [c_void_p, POINTER(c_size_t)]),
     "prm_set_workspace_limit": (c_int, [c_void_p, c_size_t]),
     "prm_set_ns_form": (c_int, [c_void_p, c_int]),
+    "prm_ns_route": (c_int, [c_int64, c_int64, c_int]),
     "prm_debug_withhold_tall_norms": (c_int, [c_void_p, c_int, ctypes.c_double]),
     "prm_set_workspace": (c_int, [c_void_p, c_void_p, c_size_t]),
     "prm_step": (c_int, [c_void_p, c_int64, c_int, c_float, c_float, c_float, c_float, c_float,
@@ -152,6 +153,10 @@ def prm_set_workspace_limit(ctx, max_bytes: int) -> None:
 
 def prm_set_ns_form(ctx, form: int) -> None:
     check(load().prm_set_ns_form(ctx, form), "prm_set_ns_form", ctx)
+
+
+def prm_ns_route(m: int, n: int, form: int = PRM_NS_FORM_AUTO) -> int:
+    return load().prm_ns_route(m, n, form)
 
 
 def prm_workspace_bytes(ctx) -> int:
