@@ -12,12 +12,19 @@ optimizer step (rotating gradient buffers: the uploads of the next steps
 overlap the current one) and a small result read back. Inputs (22 GB per optimizer
 step on the 1.3B set) are far larger than L2, so no flush is needed.
 
+After the headline workload the same invocation times short legs on the
+other matrix sets of the metric (by default, after the 1.3B set: MuonBP on
+the 1.3B set, then the 15B set), each with its own clock summary; they sit at
+the end of the JSON line under "legs".
+
   python bench.py [--steps K] [--warmup W] [--workload dit_1p3b|dit_15b|dit_1p3b_muonbp]
+                  [--legs dit_1p3b_muonbp,dit_15b | none] [--leg-steps N]
   python bench.py --impl reference   # the fp64 CPU oracle on a bounded sample
 """
 from __future__ import annotations
 
 import argparse
+import gc
 import json
 import os
 import statistics
@@ -38,17 +45,23 @@ METRIC = "ms per K=3 PR-Muon cycle (1.3B/15B DiT shapes); NS5 TFLOP/s; RowNorm G
 UNIT = "ms/cycle"
 BASELINE_VALUE = None  # the pages publish no single-GPU number for this metric
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+GEMM_FAMILIES = ("ns_gram", "ns_poly", "ns_combine", "ns_sym")
+WORKLOADS = ["dit_1p3b", "dit_15b", "dit_1p3b_muonbp", "dit_block_d2048", "dit_1p3b_4blk",
+             "dit_1p3b_4blk_muonbp", "dit_1p3b_mlp_up"]
+DEFAULT_LEGS = {"dit_1p3b": "dit_1p3b_muonbp,dit_15b"}
 
 
-def parse_args():
+def parse_args(argv=None):
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
     p.add_argument("--steps", type=int, default=10, help="timed K=3 cycles")
     p.add_argument("--warmup", type=int, default=3, help="untimed K=3 cycles")
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--workload", default="dit_1p3b",
-                   choices=["dit_1p3b", "dit_15b", "dit_1p3b_muonbp", "dit_block_d2048", "dit_1p3b_4blk",
-                            "dit_1p3b_4blk_muonbp", "dit_1p3b_mlp_up"])
+    p.add_argument("--workload", default="dit_1p3b", choices=WORKLOADS)
+    p.add_argument("--legs", default=None,
+                   help="comma-separated matrix sets timed briefly after the headline workload "
+                        "(default after dit_1p3b: dit_1p3b_muonbp,dit_15b; 'none' for no legs)")
+    p.add_argument("--leg-steps", type=int, default=3, help="timed cycles per leg (after one warm-up cycle)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-adamw", action="store_true")
@@ -56,8 +69,19 @@ def parse_args():
                    help="cap the NS5 workspace (sequential sub-plans); 0 = the library's automatic policy, "
                         "-1 = no cap")
     p.add_argument("--ns-form", choices=["auto", "direct"], default="auto",
-                   help="NS5 evaluation: auto = Gram route for groups with c >= 2 r, direct = rounds on X")
-    return p.parse_args()
+                   help="NS5 evaluation: auto = Gram route for groups wide enough, direct = rounds on X")
+    return p.parse_args(argv)
+
+
+def leg_names(args):
+    spec = args.legs if args.legs is not None else DEFAULT_LEGS.get(args.workload, "none")
+    if spec in ("", "none"):
+        return []
+    names = [x.strip() for x in spec.split(",") if x.strip()]
+    for n in names:
+        if n not in WORKLOADS:
+            raise SystemExit(f"unknown leg {n!r}")
+    return [n for n in names if n != args.workload]
 
 
 # ------------------------------------------------------------------ helpers
@@ -157,8 +181,9 @@ def summarize_clocks(lines, window=None):
             "samples": len(sm)}
 
 
-# ------------------------------------------------------------------ oracle timing
+# ------------------------------------------------------------------ flop counts
 def _ns_flops(m, n):
+    """The metric's NS5 count for one m x n matrix: 5 (4 r^2 c + 2 r^3)."""
     r, c = min(m, n), max(m, n)
     return 5 * (4 * r * r * c + 2 * r ** 3)
 
@@ -171,97 +196,69 @@ def _block_shapes(m, n, P):
     return [(m, k) if m <= n else (k, n) for k in sizes]
 
 
-def oracle_cycle_estimate(ms, size: str):
-    """Times the fp64 oracle on a bounded sample of one K=3 cycle and scales
-    it to the whole matrix set. Returns (ms_per_cycle, sample_text, seconds).
-    PR-Muon cycles are one NS5 refresh + (K-1) RowNorm steps; MuonBP cycles
-    one full NS5 + (K-1) block-NS5 steps."""
+def ns_alg_flops_per_cycle(ms):
+    """The metric's NS5 count of one K=3 cycle: one refresh (PR-Muon), or one
+    full NS5 plus K-1 block-NS5 steps (MuonBP)."""
     if ms.mode == "muonbp":
-        return _oracle_cycle_muonbp(ms)
+        bsh = {sh: _block_shapes(sh[0], sh[1], ms.blocks) for sh in set(ms.shapes)}
+        return sum(_ns_flops(*sh) + (ms.K - 1) * sum(_ns_flops(*b) for b in bsh[sh]) for sh in ms.shapes)
+    return sum(_ns_flops(*sh) for sh in ms.shapes)
+
+
+# ------------------------------------------------------------------ oracle timing
+def oracle_cycle_sample(ms):
+    """Times the fp64 oracle on a bounded sample of one K=3 cycle of matrix
+    set `ms` and scales it to the whole set. Both the reference arm and the
+    cpu_baseline of our arm use this one sampling. Returns (ms_per_cycle,
+    sample_text, measured_seconds).
+
+    PR-Muon: NS5 is timed on one r0 x r0 matrix (r0 the smallest short side,
+    at most 2048) and scaled by the metric's FLOP count to every refresh;
+    RowNorm is timed on 256 short-side vectors of every shape and scaled by
+    parameter count. MuonBP: NS5 on one r0 x r0 matrix (r0 a typical block
+    short side, at most 1024), every full and block NS5 of the cycle scaled by
+    FLOP count."""
     import numpy as np
-    import torch
 
     import oracle as O
-    from matrix_aware_optimizer_gb300 import synth
-
-    counts = {}
-    for s in ms.shapes:
-        counts[s] = counts.get(s, 0) + 1
-    shapes = list(counts)
     t_start = time.perf_counter()
-    total_ms = 0.0
-    if size == "large":
-        # NS5 on one full matrix of every shape (extrapolated by FLOPs only for
-        # shapes whose fp64 cost would exceed the budget), RowNorm on the
-        # full matrix of every shape.
-        ns_ref = None
-        for s in shapes:
-            m, n = s
-            r, c = min(m, n), max(m, n)
-            W = synth.make_param(s, 0, 0).double().numpy()
-            G = synth.make_grad(s, 0, 0, 0, ms.grad_std, ms.grad_dtype).double().numpy()
-            M = np.zeros(s)
-            flops = 5 * (4 * r * r * c + 2 * r ** 3)
-            t0 = time.perf_counter()
-            O.prmuon_step(W, M, G, 1, ms.K, ms.gamma, ms.lr, ms.wd, ms.beta, ms.eps)
-            t_rn = time.perf_counter() - t0
-            if flops <= 1.2e12 or ns_ref is None:
-                t0 = time.perf_counter()
-                O.prmuon_step(W, M, G, 0, ms.K, ms.gamma, ms.lr, ms.wd, ms.beta, ms.eps)
-                t_ns = time.perf_counter() - t0
-                ns_ref = (t_ns, flops)
-            else:
-                t_ns = ns_ref[0] * flops / ns_ref[1]
-            total_ms += counts[s] * (t_ns + 2 * t_rn) * 1e3
-        sample = ("one K=3 cycle (NS5 refresh + 2 RowNorm steps) on one full matrix of each of the "
-                  f"{len(shapes)} shapes, scaled by the shape counts; NS5 of shapes above 1.2 TFLOP "
-                  "extrapolated by FLOP count")
-    else:
-        # NS5 on the smallest shape's r x r square only, RowNorm on 256 rows /
-        # columns of every shape; both scaled (FLOPs, parameters).
-        r0 = min(min(s) for s in shapes)
-        rng = np.random.default_rng(0)
+    rng = np.random.default_rng(0)
+    if ms.mode == "muonbp":
+        blocks = {s: _block_shapes(s[0], s[1], ms.blocks) for s in set(ms.shapes)}
+        r0 = min(1024, max(min(b) for bl in blocks.values() for b in bl))
         X = rng.standard_normal((r0, r0))
         t0 = time.perf_counter()
         O.newton_schulz(X)
-        t_ns_ref = time.perf_counter() - t0
-        flops_ref = 5 * (4 * r0 ** 3 + 2 * r0 ** 3)
-        for s in shapes:
-            m, n = s
-            r, c = min(m, n), max(m, n)
-            flops = 5 * (4 * r * r * c + 2 * r ** 3)
-            sub = (256, n) if m <= n else (m, 256)
-            G = rng.standard_normal(sub)
-            t0 = time.perf_counter()
-            O.prmuon_step(np.zeros(sub), np.zeros(sub), G, 1, ms.K, ms.gamma, ms.lr, ms.wd, ms.beta, ms.eps)
-            t_rn = (time.perf_counter() - t0) * (m * n) / (sub[0] * sub[1])
-            t_ns = t_ns_ref * flops / flops_ref
-            total_ms += counts[s] * (t_ns + 2 * t_rn) * 1e3
-        sample = (f"NS5 on one {r0}x{r0} matrix scaled by FLOP count to every shape, RowNorm on 256 "
-                  "short-side vectors of each shape scaled by parameter count; one K=3 cycle")
-    return total_ms, sample, time.perf_counter() - t_start
-
-
-def _oracle_cycle_muonbp(ms):
-    """MuonBP: NS5 timed on one r0 x r0 matrix (r0 the smallest short side of
-    a block), every full and block NS5 of the cycle scaled by FLOP count."""
-    import numpy as np
-
-    import oracle as O
-    t_start = time.perf_counter()
-    blocks = {s: _block_shapes(s[0], s[1], ms.blocks) for s in set(ms.shapes)}
-    # the reference square: a typical block short side (tiny squares run BLAS far below its rate)
-    r0 = min(1024, max(min(b) for bl in blocks.values() for b in bl))
-    X = np.random.default_rng(0).standard_normal((r0, r0))
+        per_flop = (time.perf_counter() - t0) / _ns_flops(r0, r0)
+        total = 0.0
+        for s in ms.shapes:
+            total += per_flop * (_ns_flops(*s) + (ms.K - 1) * sum(_ns_flops(*b) for b in blocks[s]))
+        sample = (f"timed: NS5 of one {r0}x{r0} fp64 matrix; scaled by the metric's FLOP count to one K=3 "
+                  f"MuonBP cycle (full NS5 + {ms.K - 1} block-NS5 steps, {ms.blocks} blocks per matrix)")
+        return total * 1e3, sample, time.perf_counter() - t_start
+    counts = {}
+    for s in ms.shapes:
+        counts[s] = counts.get(s, 0) + 1
+    r0 = min(2048, min(min(s) for s in counts))
+    X = rng.standard_normal((r0, r0))
     t0 = time.perf_counter()
     O.newton_schulz(X)
-    per_flop = (time.perf_counter() - t0) / _ns_flops(r0, r0)
-    total = 0.0
-    for s in ms.shapes:
-        total += per_flop * (_ns_flops(*s) + (ms.K - 1) * sum(_ns_flops(*b) for b in blocks[s]))
-    sample = (f"NS5 on one {r0}x{r0} matrix; one K=3 MuonBP cycle (full NS5 + {ms.K - 1} block-NS5 steps "
-              f"with {ms.blocks} blocks per matrix) scaled by FLOP count")
-    return total * 1e3, sample, time.perf_counter() - t_start
+    t_ns_ref = time.perf_counter() - t0
+    total_ms = 0.0
+    for s, cnt in counts.items():
+        m, n = s
+        sub = (256, n) if m <= n else (m, 256)
+        sub = (min(sub[0], m), min(sub[1], n))
+        G = rng.standard_normal(sub)
+        t0 = time.perf_counter()
+        O.prmuon_step(np.zeros(sub), np.zeros(sub), G, 1, ms.K, ms.gamma, ms.lr, ms.wd, ms.beta, ms.eps)
+        t_rn = (time.perf_counter() - t0) * (m * n) / (sub[0] * sub[1])
+        t_ns = t_ns_ref * _ns_flops(m, n) / _ns_flops(r0, r0)
+        total_ms += cnt * (t_ns + (ms.K - 1) * t_rn) * 1e3
+    sample = (f"timed: NS5 of one {r0}x{r0} fp64 matrix and a RowNorm step on 256 short-side vectors of each "
+              f"of the {len(counts)} shapes; scaled (NS5 by the metric's FLOP count, RowNorm by parameter "
+              f"count) to one K=3 cycle of the {len(ms.shapes)} matrices")
+    return total_ms, sample, time.perf_counter() - t_start
 
 
 def max_over_ranks(value: float, device=None) -> float:
@@ -283,6 +280,16 @@ def host_cores():
         return os.cpu_count() or 1
 
 
+def cpu_threads_used():
+    """Threads the fp64 oracle's BLAS may use (numpy's matmul is its only
+    parallel step); the host core count when no limit is set."""
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        v = os.environ.get(var)
+        if v and v.isdigit():
+            return min(int(v), host_cores())
+    return host_cores()
+
+
 # ------------------------------------------------------------------ reference arm
 def run_reference(args):
     ws, rank, _ = dist_env()
@@ -291,22 +298,25 @@ def run_reference(args):
     from matrix_aware_optimizer_gb300 import synth
     ms = synth.MATRIX_SETS[args.workload]
     for _ in range(args.warmup):
-        oracle_cycle_estimate(ms, "small")
+        oracle_cycle_sample(ms)
     vals, wall = [], 0.0
     sample = ""
     for _ in range(args.steps):
-        v, sample, secs = oracle_cycle_estimate(ms, "small")
+        v, sample, secs = oracle_cycle_sample(ms)
         vals.append(v)
         wall += secs
-    value = sum(vals) / len(vals)
+    value = sum(vals) / len(vals) if vals else 0.0
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": value, "higher_is_better": False,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": args.workload, "matrices": len(ms.shapes), "params": ms.params, "K": ms.K},
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": host_cores(), "kind": "oracle", "sample": sample},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_threads_used(), "kind": "oracle",
+                         "sample": sample, "extrapolated": True,
+                         "measured_s_per_step": round(wall / max(1, args.steps), 3)},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
-        "wall_s": wall,
+        "extrapolated": True,
+        "wall_s": round(wall, 3),
     }
     print(json.dumps(line), flush=True)
     return 0
@@ -349,9 +359,181 @@ def bench_adamw(workload, dev, stream, hbm_peak, steps):
     d, nbk, ad = DIT_LAYOUT.get(workload, (2048, 24, 12288))
     nvec = synth.dit_vector_params(d, nbk, ad)
     ms_v = timed(nvec)
-    return {"sample_params": nb, "ms_per_step": round(ms_b, 4), "achieved_gbs": round(gbs, 1),
-            "frac": round(gbs / hbm_peak, 4), "bytes_per_param": 26,
-            "dit_vector_params": nvec, "dit_vector_ms_per_step": round(ms_v, 4)}
+    return {"gbs": round(gbs, 1), "frac": round(gbs / hbm_peak, 4), "bytes_per_param": 26,
+            "sample_params": nb, "dit_vector_ms_per_step": round(ms_v, 4)}
+
+
+class Workload:
+    """State of one matrix set on the device: W, M and the gradients in one
+    flat buffer (as a training loop's flattened gradient storage would hold
+    them), generated from the seeded recipe."""
+
+    def __init__(self, ms, dev):
+        import torch
+        from matrix_aware_optimizer_gb300 import synth
+        self.ms = ms
+        gdt = torch.bfloat16 if ms.grad_dtype == synth.GRAD_BF16 else torch.float32
+        self.Ws, self.Ms = synth.make_state(ms, device=dev)
+        self.offs, total = [], 0
+        for (m, n) in ms.shapes:
+            self.offs.append(total)
+            total += (m * n + 127) // 128 * 128  # keep every matrix 256-byte aligned
+        self.total = total
+        self.gflat = torch.empty(total, device=dev, dtype=gdt)
+        self.grads = []
+        for i, s in enumerate(ms.shapes):
+            g = self.gflat[self.offs[i]:self.offs[i] + s[0] * s[1]].view(s)
+            synth.make_grad(s, ms.seed, 0, i, ms.grad_std, ms.grad_dtype, ms.row_sigma, device=dev, out=g)
+            self.grads.append(g)
+        torch.cuda.synchronize()
+
+    def grad_views(self, flat):
+        return [flat[self.offs[i]:self.offs[i] + s[0] * s[1]].view(s) for i, s in enumerate(self.ms.shapes)]
+
+
+class Timer:
+    """K=3 cycles of direct prm_step calls between a barrier + synchronize on
+    both sides, optionally with the library's per-kernel event timer and with
+    events around every step."""
+
+    def __init__(self, opt, ms, stream, world, dev):
+        self.opt, self.ms, self.stream, self.world, self.dev = opt, ms, stream, world, dev
+        self.hp = dict(K=ms.K, gamma=ms.gamma, lr=ms.lr, wd=ms.wd, beta=ms.beta, eps=ms.eps)
+
+    def cycle(self, k, ev=None, positions=None):
+        for j in range(self.ms.K):
+            if positions is not None and j not in positions:
+                continue
+            t = k * self.ms.K + j
+            if ev is not None:
+                ev[j][0].record(self.stream)
+            self.opt.step(t, mode=self.ms.mode, **self.hp)
+            if ev is not None:
+                ev[j][1].record(self.stream)
+
+    def run(self, first, ncycles, profile=False, per_step=False, sampler=None, positions=None):
+        import torch
+        import torch.distributed as dist
+        from matrix_aware_optimizer_gb300 import native as N
+        K = self.ms.K
+        per = ([[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+                for _ in range(ncycles)] if per_step else None)
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if profile:
+            N.prm_profile(self.opt.ctx, True)
+        if self.world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        h0 = time.monotonic()
+        t0.record(self.stream)
+        for k in range(ncycles):
+            self.cycle(first + k, per[k] if per else None, positions)
+        t1.record(self.stream)
+        torch.cuda.synchronize()
+        if sampler is not None:
+            sampler.mark(h0, time.monotonic())
+        if self.world > 1:
+            dist.barrier()
+        if profile:
+            N.prm_profile(self.opt.ctx, False)
+        self.opt.sync_status()
+        ms_cycle = max_over_ranks(t0.elapsed_time(t1), self.dev) / ncycles
+        steps_ms = None
+        if per:
+            steps_ms = [[per[k][j][0].elapsed_time(per[k][j][1]) for j in range(K)] for k in range(ncycles)]
+        return ms_cycle, steps_ms
+
+
+def read_families(opt):
+    from matrix_aware_optimizer_gb300 import native as N
+    fam = {}
+    for f, name in enumerate(N.FAMILY_NAMES):
+        tms, recs, kern, work = N.prm_profile_read(opt.ctx, f)
+        fam[name] = dict(ms=tms, records=recs, kernels=kern, work=work)
+    return fam
+
+
+def ns5_summary(fam, alg_flops, cycles, tf_sus, tf_burst):
+    """NS5 over the profiled pass: executed TFLOP/s of the tensor-core GEMMs
+    (symmetric outputs counted for the super-blocks they compute) as a
+    fraction of the measured sustained and burst bf16 peaks, and the metric's
+    count (5 (4 r^2 c + 2 r^3) per matrix) over the same time -- an effective
+    rate that the Gram route lifts above the peak, not a fraction."""
+    ms_ = sum(fam[k]["ms"] for k in GEMM_FAMILIES)
+    fl = sum(fam[k]["work"] for k in GEMM_FAMILIES)
+    if ms_ <= 0:
+        return None
+    ex = fl / (ms_ * 1e-3) / 1e12
+    return {"gemm_ms_per_cycle": round(ms_ / cycles, 3), "tflops_executed": round(ex, 1),
+            "frac_executed": round(ex / tf_sus, 4), "frac_executed_burst": round(ex / tf_burst, 4),
+            "tflops_metric_count": round(alg_flops / (ms_ * 1e-3) / 1e12, 1)}
+
+
+def rownorm_summary(fam, hbm):
+    out = {}
+    tot_ms = tot_b = 0.0
+    for key, name in (("wide", "rownorm_wide"), ("tall", "rownorm_tall")):
+        d = fam[name]
+        if d["records"] and d["ms"] > 0:
+            gbs = d["work"] / (d["ms"] * 1e-3) / 1e9
+            out[key] = {"gbs": round(gbs, 1), "frac": round(gbs / hbm, 4)}
+            tot_ms += d["ms"]
+            tot_b += d["work"]
+    if tot_ms <= 0:
+        return None
+    gbs = tot_b / (tot_ms * 1e-3) / 1e9
+    out.update({"gbs": round(gbs, 1), "frac": round(gbs / hbm, 4), "bytes_per_param": 18})
+    return out
+
+
+def run_leg(name, args, dev, stream, world, local, peaks, wl=None):
+    """A short timing of another matrix set: one warm-up cycle, the timed
+    cycles with per-step events and a clock summary, a profiled pass for the
+    NS5 / RowNorm rates, and for MuonBP a profiled pass of block steps only."""
+    import torch
+    from matrix_aware_optimizer_gb300 import synth
+    from matrix_aware_optimizer_gb300.optimizer import PeriodicRowMuon
+    ms = synth.MATRIX_SETS[name]
+    own = wl is None
+    if own:
+        wl = Workload(ms, dev)
+    opt = PeriodicRowMuon(wl.Ws, wl.Ms, wl.grads, muonbp_blocks=ms.blocks)
+    tm = Timer(opt, ms, stream, world, dev)
+    n = max(1, args.leg_steps)
+    tm.run(0, 1)
+    clocks = ClockSampler(local)
+    clocks.start()
+    ms_cycle, steps_ms = tm.run(1, n, per_step=True, sampler=clocks)
+    clk = clocks.stop()
+    tm.run(1 + n, n, profile=True)
+    fam = read_families(opt)
+    hbm = peaks["hbm_gbs"]
+    tf_sus, tf_burst = peaks["bf16_tflops_sustained"], peaks["bf16_tflops"]
+    out = {"ms_per_cycle": round(ms_cycle, 3),
+           "ms_refresh_step": round(statistics.mean(r[0] for r in steps_ms), 3),
+           "ms_cheap_step": round(statistics.mean(x for r in steps_ms for x in r[1:]), 3),
+           "workspace_gb": round(opt.workspace_bytes / 2 ** 30, 2),
+           "ns5": ns5_summary(fam, ns_alg_flops_per_cycle(ms) * n, n, tf_sus, tf_burst)}
+    if ms.mode == "muonbp":
+        # block steps alone (t % K != 0), for the block step's own rate
+        tm.run(1 + 2 * n, n, profile=True, positions=set(range(1, ms.K)))
+        fb = read_families(opt)
+        bsh = {sh: _block_shapes(sh[0], sh[1], ms.blocks) for sh in set(ms.shapes)}
+        alg = sum(_ns_flops(*b) for sh in ms.shapes for b in bsh[sh]) * (ms.K - 1) * n
+        blk = ns5_summary(fb, alg, n * (ms.K - 1), tf_sus, tf_burst) or {}
+        blk["ms_per_step_profiled"] = round(sum(fb[k]["ms"] for k in fb) / (n * (ms.K - 1)), 3)
+        out["block_step"] = blk
+    else:
+        out["rownorm"] = rownorm_summary(fam, hbm)
+    out["clocks"] = clk
+    opt.sync_status()
+    opt.close()
+    del opt
+    if own:
+        del wl
+    gc.collect()
+    torch.cuda.empty_cache()
+    return out
 
 
 def run_ours(args):
@@ -377,79 +559,33 @@ def run_ours(args):
     mode = ms.mode
     blocks = ms.blocks
     hp = dict(K=ms.K, gamma=ms.gamma, lr=ms.lr, wd=ms.wd, beta=ms.beta, eps=ms.eps)
-    gdt = torch.bfloat16 if ms.grad_dtype == synth.GRAD_BF16 else torch.float32
+    peaks, peak_src = load_peaks()
+    for k, v in FALLBACK_PEAKS.items():
+        peaks.setdefault(k, v)
+    hbm, tf_sus, tf_burst = peaks["hbm_gbs"], peaks["bf16_tflops_sustained"], peaks["bf16_tflops"]
 
-    # state and one gradient set, generated on the device from the seeded recipe;
-    # the gradients live in one flat buffer (as a training loop's flattened
-    # gradient storage would), so the end-to-end leg moves them in one copy
-    Ws, Ms = synth.make_state(ms, device=dev)
-    offs, total = [], 0
-    for (m, n) in ms.shapes:
-        offs.append(total)
-        total += (m * n + 127) // 128 * 128  # keep every matrix 256-byte aligned
-    gflat = torch.empty(total, device=dev, dtype=gdt)
-    grads = []
-    for i, s in enumerate(ms.shapes):
-        g = gflat[offs[i]:offs[i] + s[0] * s[1]].view(s)
-        synth.make_grad(s, ms.seed, 0, i, ms.grad_std, ms.grad_dtype, ms.row_sigma, device=dev, out=g)
-        grads.append(g)
-    torch.cuda.synchronize()
+    wl = Workload(ms, dev)
+    Ws, Ms, grads, gflat = wl.Ws, wl.Ms, wl.grads, wl.gflat
     ws_limit = -1 if args.workspace_limit_gb < 0 else int(args.workspace_limit_gb * 2 ** 30)
-    opt = PeriodicRowMuon(Ws, Ms, grads, muonbp_blocks=blocks,
-                          workspace_limit=ws_limit, ns_form=args.ns_form)
+    opt = PeriodicRowMuon(Ws, Ms, grads, muonbp_blocks=blocks, workspace_limit=ws_limit, ns_form=args.ns_form)
+    ws_gb = round(opt.workspace_bytes / 2 ** 30, 2)
     stream = torch.cuda.current_stream()
+    tm = Timer(opt, ms, stream, world, dev)
 
-    def cycle(k, ev_ref=None):
-        for j in range(ms.K):
-            t = k * ms.K + j
-            if ev_ref is not None:
-                ev_ref[j][0].record(stream)
-            opt.step(t, mode=mode, **hp)
-            if ev_ref is not None:
-                ev_ref[j][1].record(stream)
-
-    for k in range(args.warmup):
-        cycle(k)
-    opt.sync_status()
-
-    def timed_cycles(first, profile, per_step, sampler=None):
-        """K cycles of direct prm_step calls between a barrier + synchronize on
-        both sides; optionally with the library's per-kernel event timer and
-        with events around every step. Returns (ms per cycle, step events)."""
-        per = ([[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                 for _ in range(ms.K)] for _ in range(args.steps)] if per_step else None)
-        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        if profile:
-            N.prm_profile(opt.ctx, True)
-        if world > 1:
-            dist.barrier()
-        torch.cuda.synchronize()
-        h0 = time.monotonic()
-        t0.record(stream)
-        for k in range(args.steps):
-            cycle(first + k, per[k] if per else None)
-        t1.record(stream)
-        torch.cuda.synchronize()
-        if sampler is not None:
-            sampler.mark(h0, time.monotonic())
-        if world > 1:
-            dist.barrier()
-        if profile:
-            N.prm_profile(opt.ctx, False)
-        opt.sync_status()
-        return max_over_ranks(t0.elapsed_time(t1), dev) / args.steps, per
+    tm.run(0, args.warmup)
 
     # ---- timed region (device-resident inputs): the headline, no library timer
     clocks = ClockSampler(local)
     clocks.start()
-    ms_cycle, per = timed_cycles(args.warmup, False, True, sampler=clocks)
+    ms_cycle, step_ms = tm.run(args.warmup, args.steps, per_step=True, sampler=clocks)
     clk = clocks.stop()
-    step_ms = [[per[k][j][0].elapsed_time(per[k][j][1]) for j in range(ms.K)] for k in range(args.steps)]
     refresh_ms = statistics.mean(r[0] for r in step_ms)
     cheap_ms = statistics.mean(x for r in step_ms for x in r[1:]) if ms.K > 1 else 0.0
     # ---- the same K cycles again with the per-kernel timer on (rooflines below)
-    ms_cycle_profiled, _ = timed_cycles(args.warmup + args.steps, True, False)
+    ms_cycle_profiled, _ = tm.run(args.warmup + args.steps, args.steps, profile=True)
     total_ms = ms_cycle_profiled * args.steps
+    fam = read_families(opt)
+    launches = sum(d["kernels"] for d in fam.values())
 
     # the same cycle captured once into a CUDA graph and replayed
     graph_ms = None
@@ -469,7 +605,7 @@ def run_ours(args):
             g.replay()
         r1.record(stream)
         torch.cuda.synchronize()
-        graph_ms = max_over_ranks(r0.elapsed_time(r1) / args.steps, dev)
+        graph_ms = round(max_over_ranks(r0.elapsed_time(r1) / args.steps, dev), 3)
         del g
         opt.sync_status()
     except Exception as exc:  # capture is an extra measurement; report why it is missing
@@ -489,244 +625,228 @@ def run_ours(args):
         v1.record(stream)
         torch.cuda.synchronize()
         vm = max_over_ranks(v0.elapsed_time(v1) / reps, dev)
-        vanilla = {"ms_per_3_steps": round(vm, 3),
-                   "optimizer_time_reduction": round(1.0 - ms_cycle / vm, 4),
-                   "note": "vanilla Muon = K=1 (NS5 every step) on the same matrices; reduction = 1 - PR-Muon "
-                           "cycle / 3 vanilla steps (the pages report 46.9-54.3 % on 32 H100 nodes, with "
-                           "communication)"}
+        vanilla = {"ms_per_3_steps": round(vm, 3), "optimizer_time_reduction": round(1.0 - ms_cycle / vm, 4)}
         opt.sync_status()
 
-    fam = {}
-    launches = 0
-    for f, name in enumerate(N.FAMILY_NAMES):
-        tms, recs, kern, work = N.prm_profile_read(opt.ctx, f)
-        fam[name] = dict(ms=tms, records=recs, kernels=kern, work=work)
-        launches += kern
-
-    peaks, peak_src = load_peaks()
-    hbm = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
-    tf_sus = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
     traffic = load_traffic()
 
     def roof(name):
         d = fam[name]
         if d["records"] == 0 or d["ms"] <= 0:
             return None
-        tensor = name in ("ns_gram", "ns_poly", "ns_combine", "ns_sym")
+        tensor = name in GEMM_FAMILIES
         if tensor:
             ach = d["work"] / (d["ms"] * 1e-3) / 1e12
             peak, unit = tf_sus, "TFLOP/s"
         else:
             ach = d["work"] / (d["ms"] * 1e-3) / 1e9
             peak, unit = hbm, "GB/s"
-        tr = traffic.get(name)
         return {"kernel": name, "bound": "tensor" if tensor else "hbm", "achieved": round(ach, 1),
-                "peak": peak, "unit": unit, "frac": round(ach / peak, 4),
-                "traffic": tr, "peak_source": f"{peak_src} ({'sustained bf16' if tensor else 'copy'})",
+                "peak": peak, "unit": unit, "frac": round(ach / peak, 4), "traffic": traffic.get(name),
                 "avg_launch_ms": round(d["ms"] / d["records"], 4), "launches": d["records"],
-                "share_of_timed": round(d["ms"] / total_ms, 4),
-                "timed_in": "the profiled pass (same K cycles as the headline, library event timer on)"}
+                "share": round(d["ms"] / total_ms, 4)}
 
     top = max(fam, key=lambda k: fam[k]["ms"])
-    ns_ms = sum(fam[k]["ms"] for k in ("ns_gram", "ns_poly", "ns_combine", "ns_sym"))
-    ns_flop = sum(fam[k]["work"] for k in ("ns_gram", "ns_poly", "ns_combine", "ns_sym"))
-    # the metric's algorithmic count, 5 (4 r^2 c + 2 r^3) per matrix and NS5 (the
-    # direct rounds), over the profiled pass's cycles
-    if mode == "muonbp":
-        bshapes = {sh: _block_shapes(sh[0], sh[1], blocks) for sh in set(ms.shapes)}
-        alg_per_cycle = sum(_ns_flops(*sh) + (ms.K - 1) * sum(_ns_flops(*b) for b in bshapes[sh])
-                            for sh in ms.shapes)
-    else:
-        alg_per_cycle = sum(_ns_flops(*sh) for sh in ms.shapes)
-    ns_alg_flop = alg_per_cycle * args.steps
-    rn_ms = fam["rownorm_wide"]["ms"] + fam["rownorm_tall"]["ms"]
-    rn_bytes = fam["rownorm_wide"]["work"] + fam["rownorm_tall"]["work"]
+    roofline = roof(top)
+    roofline["peak_source"] = f"{peak_src} ({'sustained bf16' if roofline['bound'] == 'tensor' else 'copy'})"
+    roofline["ns5"] = ns5_summary(fam, ns_alg_flops_per_cycle(ms) * args.steps, args.steps, tf_sus, tf_burst)
+    roofline["rownorm"] = rownorm_summary(fam, hbm)
+    kernels = {}
+    for k in fam:
+        r = roof(k)
+        if r is not None:
+            kernels[k] = {x: r[x] for x in ("avg_launch_ms", "launches", "achieved", "unit", "frac", "share")}
 
     # ---- end to end through the public API: pinned host grads in, a row out
     e2e = None
     if not args.no_e2e:
-        hflat = gflat.cpu().pin_memory()
-        h2d = sum(g.numel() * g.element_size() for g in grads)
-        gbytes = gflat.numel() * gflat.element_size()
-        # NBUF gradient buffers, one optimizer instance per buffer over the same
-        # params / momenta, all sharing one workspace (their steps are ordered
-        # on one stream): step s reads buffer s % NBUF while the gradients of
-        # the next steps stream into the others. Each upload runs as pieces on
-        # several copy streams and waits for the step that last read its
-        # buffer (s - NBUF); each step waits for its own upload, and its one-row
-        # read-back runs on a stream of its own.
-        free_b, _ = torch.cuda.mem_get_info(dev)
-        nbuf = max(2, min(4, 1 + int((free_b - (4 << 30)) // max(gbytes, 1))))
-        extra = [torch.empty_like(gflat) for _ in range(nbuf - 1)]
-        opts = [opt]
-        for buf in extra:
-            gl = [buf[offs[i]:offs[i] + s[0] * s[1]].view(s) for i, s in enumerate(ms.shapes)]
-            opts.append(PeriodicRowMuon(Ws, Ms, gl, muonbp_blocks=blocks, workspace=opt.workspace,
-                                        workspace_limit=ws_limit, ns_form=args.ns_form))
-        bufs = list(zip([gflat] + extra, opts))
-        out_row = torch.empty(ms.shapes[0][1], dtype=torch.float32).pin_memory()
-        d2h = out_row.numel() * 4
-        d2h_stream = torch.cuda.Stream(device=dev)  # the read-back never holds up the next step
-
-        stream_pool = [torch.cuda.Stream(device=dev) for _ in range(8)]
-
-        def upload_alone(nstreams):
-            css = stream_pool[:nstreams]
-            bnd = [total * q // nstreams // 128 * 128 for q in range(nstreams)] + [total]
-            best = None
-            for _ in range(3):
-                u0, u1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                u0.record(stream)
-                for q, cs in enumerate(css):
-                    cs.wait_stream(stream)
-                    with torch.cuda.stream(cs):
-                        gflat[bnd[q]:bnd[q + 1]].copy_(hflat[bnd[q]:bnd[q + 1]], non_blocking=True)
-                    stream.wait_stream(cs)
-                u1.record(stream)
-                torch.cuda.synchronize()
-                t_ = u0.elapsed_time(u1)
-                best = t_ if best is None else min(best, t_)
-            return best
-
-        # the host link rate behind the number, and the copy-stream count used
-        up_ms = {n: upload_alone(n) for n in (1, 4)}
-        ncopy = min(up_ms, key=up_ms.get)
-        copy_streams = stream_pool[:ncopy]
-        bounds = [total * q // ncopy // 128 * 128 for q in range(ncopy)] + [total]
-
-        def run(first_t, nsteps, per=None, up_ev=None):
-            step_done = {}
-            uploaded = {}
-
-            def upload(s):
-                dst = bufs[s % nbuf][0]
-                ev = []
-                for q, cs in enumerate(copy_streams):
-                    if s - nbuf in step_done:
-                        cs.wait_event(step_done[s - nbuf])
-                    if up_ev is not None:
-                        up_ev[s][q][0].record(cs)
-                    with torch.cuda.stream(cs):
-                        dst[bounds[q]:bounds[q + 1]].copy_(hflat[bounds[q]:bounds[q + 1]], non_blocking=True)
-                    e = torch.cuda.Event(enable_timing=up_ev is not None)
-                    e.record(cs)
-                    if up_ev is not None:
-                        up_ev[s][q][1] = e
-                    ev.append(e)
-                uploaded[s] = ev
-
-            for s in range(min(nbuf - 1, nsteps)):
-                upload(s)
-            for s in range(nsteps):
-                if s + nbuf - 1 < nsteps:
-                    upload(s + nbuf - 1)
-                for e in uploaded.pop(s):
-                    stream.wait_event(e)
-                if per is not None:
-                    per[s][0].record(stream)
-                bufs[s % nbuf][1].step(first_t + s, mode=mode, **hp)
-                if per is not None:
-                    per[s][1].record(stream)
-                done = torch.cuda.Event()
-                done.record(stream)
-                step_done[s] = done
-                d2h_stream.wait_event(done)
-                with torch.cuda.stream(d2h_stream):
-                    out_row.copy_(Ws[0][0], non_blocking=True)
-            stream.wait_stream(d2h_stream)
-
-        run(0, 2 * ms.K)  # warm-up (t = 0 starts a cycle)
-        torch.cuda.synchronize()
-        if world > 1:
-            dist.barrier()
-        nst = args.steps * ms.K
-        per = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(nst)]
-        up_ev = [[[torch.cuda.Event(enable_timing=True), None] for _ in copy_streams] for _ in range(nst)]
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        run((args.warmup + args.steps) * ms.K, nst, per, up_ev)
-        e1.record(stream)
-        torch.cuda.synchronize()
-        e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, dev)
-        # where the time went: the steps themselves, and the waits between them
-        # (a step waiting for its gradients)
-        busy = sum(a.elapsed_time(b) for a, b in per) / args.steps
-        waits = [per[s][1].elapsed_time(per[s + 1][0]) for s in range(nst - 1)]
-        # each upload from its first piece's start to its last piece's end (the
-        # uploads follow one another on the link)
-        up_busy = sum(max(up_ev[s][q][0].elapsed_time(up_ev[s][q][1]) for q in range(ncopy))
-                      for s in range(nst)) / args.steps
-        e2e = {"value": round(e2e_ms, 3), "unit": UNIT, "h2d_bytes_per_step": h2d * ms.K,
-               "d2h_bytes_per_step": d2h * ms.K,
-               "h2d_gbs_alone": round(h2d / up_ms[ncopy] / 1e6, 1), "copy_streams": ncopy,
-               "gradient_buffers": nbuf, "steps_ms_per_cycle": round(busy, 3),
-               "waits_ms_per_cycle": round(sum(waits) / args.steps, 3),
-               "longest_wait_ms": round(max(waits) if waits else 0.0, 3),
-               "uploads_ms_per_cycle": round(up_busy, 3),
-               "h2d_gbs_under_load": round(h2d * ms.K / up_busy / 1e6, 1) if up_busy > 0 else None,
-               "note": "per optimizer step: that step's gradients copied from pinned host memory (copy streams in "
-                       "parallel), the step, one parameter row read back; the gradient buffers rotate so that "
-                       "the uploads of the next steps overlap the current one"}
-        for o in opts:
-            o.sync_status()
-        for o in opts[1:]:
-            o.close()
-        del extra, opts, bufs
+        e2e = run_e2e(args, wl, opt, ms, stream, dev, world, ws_limit)
 
     adam = None
     if not args.no_adamw:
         adam = bench_adamw(args.workload, dev, stream, hbm, max(3, args.steps))
 
+    opt.close()
+    del opt, tm, Ws, Ms, grads, gflat
+    # legs on the same matrices (MuonBP on the 1.3B set) reuse the state; a
+    # leg on other matrices first frees it and builds its own
+    legs = {}
+    for name in leg_names(args):
+        same = synth.MATRIX_SETS[name].shapes == ms.shapes
+        if not same and wl is not None:
+            wl = None
+            gc.collect()
+            torch.cuda.empty_cache()
+        legs[name] = run_leg(name, args, dev, stream, world, local, peaks, wl if same else None)
+    wl = None
+    gc.collect()
+    torch.cuda.empty_cache()
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        v, sample, _ = oracle_cycle_estimate(ms, "large")
-        cpu = {"value": round(v, 1), "unit": UNIT, "cores": host_cores(), "kind": "oracle", "sample": sample}
+        v, sample, secs = oracle_cycle_sample(ms)
+        cpu = {"value": round(v, 1), "unit": UNIT, "cores": cpu_threads_used(), "kind": "oracle",
+               "sample": sample, "extrapolated": True, "measured_s": round(secs, 3)}
 
-    n_params = ms.params
     line = {
         "metric": METRIC, "value": round(ms_cycle, 3), "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_cycle, 3), "higher_is_better": False,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32 state, bf16 x bf16 -> f32 NS5", "data": "synthetic",
-        "config": {"workload": args.workload, "matrices": len(ms.shapes), "params": n_params, "K": ms.K,
+        "config": {"workload": args.workload, "matrices": len(ms.shapes), "params": ms.params, "K": ms.K,
                    "gamma": ms.gamma, "lr": ms.lr, "wd": ms.wd, "beta": ms.beta, "mode": mode,
                    "muonbp_blocks": blocks, "grad_dtype": ms.grad_dtype,
                    "l2": "inputs larger than L2 (no flush)", "parallelism": f"replicas x{world}",
                    "step": "one K=3 cycle: refresh + 2 cheap steps",
-                   "workspace_gb": round(opt.workspace_bytes / 2 ** 30, 2),
-                   "workspace_policy": ("automatic" if args.workspace_limit_gb == 0 else
-                                        "no cap" if args.workspace_limit_gb < 0 else
-                                        f"cap {args.workspace_limit_gb} GiB"),
-                   "ns_form": args.ns_form},
-        "ms_refresh_step": round(refresh_ms, 3), "ms_cheap_step": round(cheap_ms, 3),
-        "ns5_tflops": round(ns_alg_flop / (ns_ms * 1e-3) / 1e12, 1) if ns_ms else None,
-        "ns5_tflops_note": "NS5 TFLOP/s in the metric's count, 5 (4 r^2 c + 2 r^3) per matrix (the direct "
-                           "rounds), over the NS5 GEMM time; the Gram route forms fewer products, so this "
-                           "is an effective rate and can exceed the tensor peak. ns5_tflops_formed counts "
-                           "the products the launches form (symmetric outputs dense).",
-        "ns5_tflops_formed": round(ns_flop / (ns_ms * 1e-3) / 1e12, 1) if ns_ms else None,
-        "rownorm_gbs": round(rn_bytes / (rn_ms * 1e-3) / 1e9, 1) if rn_ms else None,
-        "roofline": roof(top),
-        "roofline_kernels": {k: roof(k) for k in fam if fam[k]["records"]},
-        "graph_replay_ms_per_cycle": round(graph_ms, 3) if isinstance(graph_ms, float) else graph_ms,
-        "profiled_pass_ms_per_cycle": round(ms_cycle_profiled, 3),
-        "vanilla_muon": vanilla,
-        "adamw": adam,
-        "cpu_baseline": cpu,
-        "e2e": e2e,
+                   "workspace_gb": ws_gb, "ns_form": args.ns_form},
         "gpu_launches": launches,
         "clocks": clk,
+        "e2e": e2e,
+        "cpu_baseline": cpu,
+        "roofline": roofline,
+        "ms_refresh_step": round(refresh_ms, 3), "ms_cheap_step": round(cheap_ms, 3),
+        "profiled_pass_ms_per_cycle": round(ms_cycle_profiled, 3),
+        "graph_replay_ms_per_cycle": graph_ms,
+        "kernels": kernels,
+        "vanilla_muon": vanilla,
+        "adamw": adam,
+        "legs": legs,
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
-    opt.close()
     if world > 1:
         dist.destroy_process_group()
     return 0
 
 
+def run_e2e(args, wl, opt, ms, stream, dev, world, ws_limit):
+    """The same K=3 cycles through the public API with every optimizer step's
+    gradients copied in from pinned host memory and one parameter row read
+    back. NBUF gradient buffers, one optimizer instance per buffer over the
+    same params / momenta, all sharing one workspace (their steps are ordered
+    on one stream): step s reads buffer s % NBUF while the gradients of the
+    next steps stream into the others. Each upload runs as pieces on one or
+    more copy streams and waits for the step that last read its buffer
+    (s - NBUF); each step waits for its own upload, and its one-row read-back
+    runs on a stream of its own."""
+    import torch
+    from matrix_aware_optimizer_gb300.optimizer import PeriodicRowMuon
+    hp = dict(K=ms.K, gamma=ms.gamma, lr=ms.lr, wd=ms.wd, beta=ms.beta, eps=ms.eps)
+    gflat, total, Ws = wl.gflat, wl.total, wl.Ws
+    hflat = gflat.cpu().pin_memory()
+    h2d = sum(g.numel() * g.element_size() for g in wl.grads)
+    gbytes = gflat.numel() * gflat.element_size()
+    free_b, _ = torch.cuda.mem_get_info(dev)
+    nbuf = max(2, min(4, 1 + int((free_b - (4 << 30)) // max(gbytes, 1))))
+    extra = [torch.empty_like(gflat) for _ in range(nbuf - 1)]
+    opts = [opt]
+    for buf in extra:
+        opts.append(PeriodicRowMuon(Ws, wl.Ms, wl.grad_views(buf), muonbp_blocks=ms.blocks,
+                                    workspace=opt.workspace, workspace_limit=ws_limit, ns_form=args.ns_form))
+    bufs = list(zip([gflat] + extra, opts))
+    out_row = torch.empty(ms.shapes[0][1], dtype=torch.float32).pin_memory()
+    d2h = out_row.numel() * 4
+    d2h_stream = torch.cuda.Stream(device=dev)  # the read-back never holds up the next step
+    stream_pool = [torch.cuda.Stream(device=dev) for _ in range(8)]
+
+    def upload_alone(nstreams):
+        css = stream_pool[:nstreams]
+        bnd = [total * q // nstreams // 128 * 128 for q in range(nstreams)] + [total]
+        best = None
+        for _ in range(3):
+            u0, u1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            u0.record(stream)
+            for q, cs in enumerate(css):
+                cs.wait_stream(stream)
+                with torch.cuda.stream(cs):
+                    gflat[bnd[q]:bnd[q + 1]].copy_(hflat[bnd[q]:bnd[q + 1]], non_blocking=True)
+                stream.wait_stream(cs)
+            u1.record(stream)
+            torch.cuda.synchronize()
+            t_ = u0.elapsed_time(u1)
+            best = t_ if best is None else min(best, t_)
+        return best
+
+    # the host link rate behind the number, and the copy-stream count used
+    up_ms = {n: upload_alone(n) for n in (1, 4)}
+    ncopy = min(up_ms, key=up_ms.get)
+    copy_streams = stream_pool[:ncopy]
+    bounds = [total * q // ncopy // 128 * 128 for q in range(ncopy)] + [total]
+
+    def run(first_t, nsteps, per=None, up_ev=None):
+        step_done = {}
+        uploaded = {}
+
+        def upload(s):
+            dst = bufs[s % nbuf][0]
+            ev = []
+            for q, cs in enumerate(copy_streams):
+                if s - nbuf in step_done:
+                    cs.wait_event(step_done[s - nbuf])
+                if up_ev is not None:
+                    up_ev[s][q][0].record(cs)
+                with torch.cuda.stream(cs):
+                    dst[bounds[q]:bounds[q + 1]].copy_(hflat[bounds[q]:bounds[q + 1]], non_blocking=True)
+                e = torch.cuda.Event(enable_timing=up_ev is not None)
+                e.record(cs)
+                if up_ev is not None:
+                    up_ev[s][q][1] = e
+                ev.append(e)
+            uploaded[s] = ev
+
+        for s in range(min(nbuf - 1, nsteps)):
+            upload(s)
+        for s in range(nsteps):
+            if s + nbuf - 1 < nsteps:
+                upload(s + nbuf - 1)
+            for e in uploaded.pop(s):
+                stream.wait_event(e)
+            if per is not None:
+                per[s][0].record(stream)
+            bufs[s % nbuf][1].step(first_t + s, mode=ms.mode, **hp)
+            if per is not None:
+                per[s][1].record(stream)
+            done = torch.cuda.Event()
+            done.record(stream)
+            step_done[s] = done
+            d2h_stream.wait_event(done)
+            with torch.cuda.stream(d2h_stream):
+                out_row.copy_(Ws[0][0], non_blocking=True)
+        stream.wait_stream(d2h_stream)
+
+    run(0, 2 * ms.K)  # warm-up (t = 0 starts a cycle)
+    torch.cuda.synchronize()
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    nst = args.steps * ms.K
+    per = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(nst)]
+    up_ev = [[[torch.cuda.Event(enable_timing=True), None] for _ in copy_streams] for _ in range(nst)]
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    run((args.warmup + args.steps) * ms.K, nst, per, up_ev)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, dev)
+    busy = sum(a.elapsed_time(b) for a, b in per) / args.steps
+    waits = [per[s][1].elapsed_time(per[s + 1][0]) for s in range(nst - 1)]
+    # each upload from its first piece's start to its last piece's end
+    up_busy = sum(max(up_ev[s][q][0].elapsed_time(up_ev[s][q][1]) for q in range(ncopy))
+                  for s in range(nst)) / args.steps
+    for o in opts:
+        o.sync_status()
+    for o in opts[1:]:
+        o.close()
+    del extra, opts, bufs
+    return {"value": round(e2e_ms, 3), "unit": UNIT, "h2d_bytes_per_step": h2d * ms.K,
+            "d2h_bytes_per_step": d2h * ms.K, "h2d_gbs_alone": round(h2d / up_ms[ncopy] / 1e6, 1),
+            "h2d_gbs_under_load": round(h2d * ms.K / up_busy / 1e6, 1) if up_busy > 0 else None,
+            "steps_ms_per_cycle": round(busy, 3), "waits_ms_per_cycle": round(sum(waits) / args.steps, 3),
+            "copy_streams": ncopy, "gradient_buffers": nbuf}
+
+
 def load_traffic():
-    """Per-launch DRAM bytes of each kernel family from the committed ncu
-    summary, if it was taken on the current kernel sources."""
+    """Per-launch DRAM bytes of each kernel family of the 1.3B set from the
+    committed ncu summary, if it was taken on the current kernel sources."""
     path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     try:
         with open(path) as f:

@@ -146,10 +146,17 @@ PRM_API int prm_set_workspace_limit(prm_ctx* ctx, size_t max_bytes);
 #define PRM_NS_FORM_DIRECT 1
 PRM_API int prm_set_ns_form(prm_ctx* ctx, int form);
 
-/* Pure helper: 1 if the planner puts an m x n matrix's NS5 on the Gram route
- * under `form`, 0 for the direct rounds; -PRM_ERR_INVALID_ARG for m or n < 1
- * or an unknown form. (The route also needs c != 0 in ns_coeffs at step
- * time.) */
+/* Pure helper: which NS5 evaluation the planner gives an m x n matrix under
+ * `form`: 2 when the short side is below 64 (in either form: fp32 rounds on
+ * CUDA cores, see below), 1 for the Gram route, 0 for the direct rounds on
+ * tensor cores; -PRM_ERR_INVALID_ARG for m or n < 1 or an unknown form. (The
+ * Gram route also needs c != 0 in ns_coeffs at step time.)
+ *
+ * Short sides below 64: such a matrix fills at most a quarter of the tensor
+ * cores' 256-wide tile, and with so few elements the bf16 rounding of X and
+ * of the r x r products no longer averages out. These matrices run the five
+ * rounds A = X X^T, P = a I + b A + c A A, X <- P X in fp32 on CUDA cores
+ * (sums in a fixed order), in both forms and in MuonBP block steps alike. */
 PRM_API int prm_ns_route(int64_t m, int64_t n, int form);
 
 /* Bytes of device scratch the registered plan needs (NS5 operands in bf16,
@@ -246,11 +253,14 @@ PRM_API int prm_debug_withhold_tall_norms(prm_ctx* ctx, int stripe, double wait_
  *   Limits: rows > cols (tall), ceil(rows / 256) * cols + cols <= 1,048,576
  *   floats (e.g. up to 32768 x 4096 or 20480 x 5120); larger shapes return
  *   PRM_ERR_UNSUPPORTED. shape_scale <= 0 selects sqrt(rows / cols).
- *   The first call on a device looks up the array's device address (a
- *   one-time set-up per device); make that first call before any stream
- *   capture. Every call shares the array: calls whose work may overlap on
- *   the GPU (other streams, unordered host threads) race and must not be
- *   issued. Errors: INVALID_ARG, SHAPE, UNSUPPORTED, CUDA. */
+ *   Every call looks up the array's device address on the current device
+ *   (cudaGetSymbolAddress, which allocates nothing); the first call on a
+ *   device also loads the library's device code there, so make that first
+ *   call before any stream capture. Every call shares the array and finds
+ *   the previous call's contents in it (each call writes every element it
+ *   reads before reading it): calls whose work may overlap on the GPU (other
+ *   streams, unordered host threads) race and must not be issued.
+ *   Errors: INVALID_ARG, SHAPE, UNSUPPORTED, CUDA. */
 PRM_API int prm_rownorm_tall_step_noalloc(float* param, float* momentum, const void* grad,
                                           int grad_dtype, int64_t rows, int64_t cols, float gamma,
                                           float lr, float wd, float beta, float eps,
@@ -278,13 +288,16 @@ PRM_API int prm_adamw_step(float* param, float* exp_avg, float* exp_avg_sq, cons
 /* ---- kernel timing (benchmarks) --------------------------------------
  * When enabled, every kernel family launched by prm_step is bracketed by a
  * pair of CUDA events recorded on the launching stream, and its algorithmic
- * work is accumulated: for the GEMM families the dense FLOPs of the products
- * they form, 2 M N K per matrix (symmetric outputs -- GRAM, POLY and the Gram
- * route's updates -- counted dense although only their upper 256 x 256
- * super-blocks are computed), bytes for the memory-bound
- * ones (RowNorm 18 B per parameter with bf16 gradients, 20 B with fp32;
- * prep 12 / 14 B). The refresh's parameter update runs in the epilogue of
- * the last COMBINE launch and is timed with it. Families: */
+ * work is accumulated: for the GEMM families the FLOPs they execute --
+ * 2 M N K per matrix for COMBINE; for the symmetric r x r outputs (GRAM,
+ * POLY and the Gram route's updates) the share of 2 r r K that their upper
+ * 256 x 256 super-blocks cover, nb (nb + 1) / 2 of nb^2 with
+ * nb = ceil(r / 256) (36 / 64 at r = 2048; the lower ones are mirrored, not
+ * multiplied); for the fp32 rounds of short sides below 64 the FLOPs of
+ * their Gram pairs, P X and P; bytes for the memory-bound ones (RowNorm
+ * 18 B per parameter with bf16 gradients, 20 B with fp32; prep 12 / 14 B).
+ * The refresh's parameter update runs in the epilogue of the last COMBINE
+ * launch and is timed with it. Families: */
 #define PRM_FAMILY_ROWNORM_WIDE 0
 #define PRM_FAMILY_ROWNORM_TALL 1
 #define PRM_FAMILY_NS_PREP      2
@@ -292,7 +305,8 @@ PRM_API int prm_adamw_step(float* param, float* exp_avg, float* exp_avg_sq, cons
 #define PRM_FAMILY_NS_POLY      4
 #define PRM_FAMILY_NS_COMBINE   5
 #define PRM_FAMILY_NS_SYM       6  /* Gram route: Q <- P Q, T <- P T */
-#define PRM_FAMILY_COUNT        7
+#define PRM_FAMILY_NS_SMALL     7  /* NS5 of short sides below 64 (fp32, CUDA cores; executed flops) */
+#define PRM_FAMILY_COUNT        8
 
 /* enable = 1 clears the records and starts recording; 0 stops. */
 PRM_API int prm_profile(prm_ctx* ctx, int enable);

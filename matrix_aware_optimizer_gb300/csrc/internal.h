@@ -78,6 +78,37 @@ cudaError_t launch_prep(const View* d_views, int count, int64_t rows, int64_t co
 cudaError_t launch_norm_finish(const float* partials, int64_t slots, float* scale, int count, float ns_eps,
                                cudaStream_t stream);
 
+// ---- NS5 of matrices with a short side below NS_SMALL_R (fp32, CUDA cores)
+// One same-shape group (wide orientation r x c); buffers in the workspace,
+// indexed by the views' batch slots: X tile-major (slot, tile, r x
+// NS_SMALL_TC), Gram partial sums (slot, chunk, r (r + 1) / 2 upper-triangle
+// pairs) and P (slot, r x r). Chunk q of a matrix covers its column tiles
+// [q tiles / chunks, (q + 1) tiles / chunks).
+constexpr int NS_SMALL_R = 64;
+constexpr int NS_SMALL_TC = 64;
+constexpr int NS_SMALL_THREADS = 256;
+constexpr int NS_SMALL_MAX_CHUNKS = 128;
+struct NsSmallArgs {
+  int r;
+  int64_t c;
+  int64_t tiles;   // ceil(c / NS_SMALL_TC)
+  int chunks;      // CTAs per matrix
+  float* X;
+  float* partials;
+  float* P;
+};
+int64_t ns_small_tiles(int64_t c);
+int ns_small_chunks(int64_t c);
+// momentum update (or plain read) and the round-0 Gram partials
+cudaError_t launch_ns_small_prep(const NsSmallArgs& a, const View* d_views, int count, bool tall, bool grad_bf16,
+                                 bool update_momentum, float beta, cudaStream_t stream);
+// P = a I + b A + c A A for every matrix of the group (first: s-scaled)
+cudaError_t launch_ns_small_poly(const NsSmallArgs& a, int count, bool first, const float coeffs[3], float ns_eps,
+                                 cudaStream_t stream);
+// X' = P X; last: the update W <- W decay - eta s X' (or D into the view's out)
+cudaError_t launch_ns_small_combine(const NsSmallArgs& a, const View* d_views, int count, bool tall, bool first,
+                                    bool last, float decay, float eta, cudaStream_t stream);
+
 
 
 // ---- tcgen05 GEMM stages of one NS5 round -------------------------------

@@ -64,11 +64,13 @@ struct NsGroup {
   int count = 0;
   int rclass = -1;        // direct route: index of its r-class
   bool gram = false;      // Gram route
+  bool small = false;     // r < NS_SMALL_R: fp32 rounds on CUDA cores (ns_small.cu), no tensor maps
   int64_t base_slot = 0;  // first slot of this group inside its r-class arrays
   int64_t slots = 0;      // Frobenius partial slots per matrix
   std::vector<LaunchSet> sets;
   size_t off_x0 = 0, off_x1 = 0, off_scale = 0, off_partials = 0;
   size_t off_c = 0, off_p = 0, off_ya = 0, off_yb = 0;  // Gram route
+  size_t off_sx = 0, off_spart = 0, off_sp = 0;          // small: X, Gram partials, P (fp32)
   // tensor maps for the bound workspace
   const void* maps_base = nullptr;
   NsMaps mx0{}, mx1{};
@@ -151,6 +153,14 @@ bool view_vec_ok(const View& v) {
   return base && ptrs && g;
 }
 
+// Share of a symmetric r x r output's dense products that the GEMM kernels
+// execute: the upper-triangle 256 x 256 super-blocks, nb (nb + 1) / 2 of nb^2
+// (36 / 64 at r = 2048).
+double sym_share(int64_t r) {
+  const double nb = static_cast<double>((r + 255) / 256);
+  return (nb + 1.0) / (2.0 * nb);
+}
+
 // Whether the Gram route (see run_ns) pays for an r x c group: its executed
 // work for the five default rounds (legs of three and two) against the
 // direct rounds', in units of r^3 with rho = c / r and f the executed share
@@ -204,6 +214,18 @@ void build_ns_plan(const std::vector<View>& views, NsPlan& plan, int form) {
   size_t off = 0;
   std::map<int64_t, int> rindex;
   for (auto& g : plan.groups) {
+    if (g.r < NS_SMALL_R) {
+      // short side below 64: fp32 rounds on CUDA cores, own buffers only
+      g.small = true;
+      const int64_t tiles = ns_small_tiles(g.c), chunks = ns_small_chunks(g.c);
+      g.off_sx = off;
+      off += align_up(static_cast<size_t>(g.count) * tiles * g.r * NS_SMALL_TC * 4, 256);
+      g.off_spart = off;
+      off += align_up(static_cast<size_t>(g.count) * chunks * (g.r * (g.r + 1) / 2) * 4, 256);
+      g.off_sp = off;
+      off += align_up(static_cast<size_t>(g.count) * g.r * g.r * 4, 256);
+      continue;
+    }
     g.slots = prep_slots(g.sets.front().rows, g.sets.front().cols);
     for (auto& s : g.sets) g.slots = std::max(g.slots, prep_slots(s.rows, s.cols));
     const size_t xb = align_up(static_cast<size_t>(g.count) * g.r * g.ldc * 2, 256);
@@ -476,7 +498,7 @@ int bind_maps(prm_ctx* c, NsPlan& plan, void* base) {
     rc.maps_base = base;
   }
   for (auto& g : plan.groups) {
-    if (g.maps_base == base) continue;
+    if (g.small || g.maps_base == base) continue;
     int e = encode_x_maps(&g.mx0, b + g.off_x0, g.count, g.r, g.c, g.ldc);
     if (e == 0) e = encode_x_maps(&g.mx1, b + g.off_x1, g.count, g.r, g.c, g.ldc);
     if (g.gram) {
@@ -500,16 +522,59 @@ int bind_maps(prm_ctx* c, NsPlan& plan, void* base) {
   return PRM_OK;
 }
 
+// NS5 of one group with a short side below NS_SMALL_R, all in fp32 on CUDA
+// cores (ns_small.cu): momentum and Gram partials, then per round P from the
+// partials and X' = P X over column chunks; the last round applies the update.
+int run_ns_small(prm_ctx* c, NsGroup& g, char* b, bool update_momentum, float beta, float decay, float eta,
+                 const float coeffs[3], int steps, cudaStream_t stream) {
+  NsSmallArgs a;
+  a.r = static_cast<int>(g.r);
+  a.c = g.c;
+  a.tiles = ns_small_tiles(g.c);
+  a.chunks = ns_small_chunks(g.c);
+  a.X = reinterpret_cast<float*>(b + g.off_sx);
+  a.partials = reinterpret_cast<float*>(b + g.off_spart);
+  a.P = reinterpret_cast<float*>(b + g.off_sp);
+  const double r = static_cast<double>(g.r), cw = static_cast<double>(g.c);
+  // executed flops per matrix: Gram pairs r (r + 1) c per round, P X 2 r^2 c, P 2 r^3
+  const double flops = g.count * steps * (r * (r + 1) * cw + 2 * r * r * cw + 2 * r * r * r);
+  const size_t ev = c->prof.begin(stream);
+  cudaError_t e;
+  for (auto& s : g.sets) {
+    e = launch_ns_small_prep(a, s.d_views, static_cast<int>(s.views.size()), s.rows > s.cols, s.bf16,
+                             update_momentum, beta, stream);
+    if (e != cudaSuccess) return cuda_fail(c, e, "small NS5 prep launch");
+  }
+  for (int it = 0; it < steps; ++it) {
+    if ((e = launch_ns_small_poly(a, g.count, it == 0, coeffs, NS_EPS, stream)) != cudaSuccess)
+      return cuda_fail(c, e, "small NS5 polynomial launch");
+    for (auto& s : g.sets) {
+      e = launch_ns_small_combine(a, s.d_views, static_cast<int>(s.views.size()), s.rows > s.cols, it == 0,
+                                  it == steps - 1, decay, eta, stream);
+      if (e != cudaSuccess) return cuda_fail(c, e, "small NS5 combine launch");
+    }
+  }
+  c->prof.end(ev, PRM_FAMILY_NS_SMALL, static_cast<int>(g.sets.size()) * (steps + 1) + steps, flops, stream);
+  return PRM_OK;
+}
+
 // One NS5 refresh over every group of `plan`: prep (momentum + pack + norm
-// partials), scale, five GRAM / POLY / COMBINE rounds, apply.
+// partials), scale, five GRAM / POLY / COMBINE rounds, apply. Groups with a
+// short side below NS_SMALL_R run on their own path (run_ns_small) first.
 int run_ns(prm_ctx* c, NsPlan& plan, void* base, bool update_momentum, float beta, float decay, float eta,
            const float coeffs[3], int steps, cudaStream_t stream) {
   char* b = static_cast<char*>(base);
   int rc = bind_maps(c, plan, base);
   if (rc != PRM_OK) return rc;
   cudaError_t e;
+  for (auto& g : plan.groups) {
+    if (!g.small) continue;
+    rc = run_ns_small(c, g, b, update_momentum, beta, decay, eta, coeffs, steps, stream);
+    if (rc != PRM_OK) return rc;
+  }
   // 1. momentum update, bf16 pack (transposed for tall views), Frobenius norms
   for (auto& g : plan.groups) {
+    if (g.small) continue;
     float* scale = reinterpret_cast<float*>(b + g.off_scale);
     float* partials = reinterpret_cast<float*>(b + g.off_partials);
     uint16_t* x0 = reinterpret_cast<uint16_t*>(b + g.off_x0);
@@ -596,8 +661,12 @@ int run_ns(prm_ctx* c, NsPlan& plan, void* base, bool update_momentum, float bet
     std::vector<GemmSegSpec> gram, poly, sym, comb;
     double f_gram = 0, f_poly = 0, f_sym = 0, f_comb = 0;
     for (const NsGroup& g : plan.groups) {
+      if (g.small) continue;
       const double n = g.count, r = static_cast<double>(g.r), cw = static_cast<double>(g.c);
-      const double r3 = 2 * n * r * r * r, r2c = 2 * n * r * r * cw;
+      // flops each launch executes: symmetric r x r outputs (GRAM, POLY, the
+      // Gram route's updates) compute only their upper super-blocks
+      const double sh = sym_share(g.r);
+      const double r3 = 2 * n * r * r * r * sh, r2c = 2 * n * r * r * cw;
       const float* scale0 = reinterpret_cast<const float*>(b + g.off_scale);
       if (g.gram && square) {
         const NsMaps& xs = (leg & 1) ? g.mx1 : g.mx0;
@@ -628,7 +697,7 @@ int run_ns(prm_ctx* c, NsPlan& plan, void* base, bool update_momentum, float bet
             f_comb += r2c;
           }
           gs.gain = gram_gain;
-          f_gram += r2c;
+          f_gram += r2c * sh;
         } else {
           gs = GemmSegSpec{&yprev.t.x_rows128, &yprev.q.x_rows128, &g.mc.store, nullptr, g.count, g.r, g.r, 0};
           gs.in_fp16 = true;
@@ -670,7 +739,7 @@ int run_ns(prm_ctx* c, NsPlan& plan, void* base, bool update_momentum, float bet
       gs.gain = gram_gain;
       gs.diag = gram_diag;
       gram.push_back(gs);
-      f_gram += r2c;
+      f_gram += r2c * sh;
       const SymMaps& pm = g.gram ? g.mc : (square ? g.mb : g.ma);
       GemmSegSpec cs{&pm.rows128, &cur.x_k64, &nxt.store, sc, g.count, g.r, g.c, 0};
       if (last) cs.views = g.d_slot_views;
@@ -684,7 +753,7 @@ int run_ns(prm_ctx* c, NsPlan& plan, void* base, bool update_momentum, float bet
         ps.gain = poly_gain;
         ps.diag = poly_diag;
         poly.push_back(ps);
-        f_poly += 2.0 * rcl.count * double(rcl.r) * rcl.r * rcl.r;
+        f_poly += 2.0 * rcl.count * double(rcl.r) * rcl.r * rcl.r * sym_share(rcl.r);
       }
     // 3. the last round applies D = X_steps instead of storing it:
     // W <- W (1 - lr wd) - eta s D, transposed back for tall views
@@ -941,6 +1010,7 @@ int prm_set_workspace(prm_ctx* c, void* dev_ptr, size_t bytes) {
 
 int prm_ns_route(int64_t m, int64_t n, int form) {
   if (m < 1 || n < 1 || (form != PRM_NS_FORM_AUTO && form != PRM_NS_FORM_DIRECT)) return -PRM_ERR_INVALID_ARG;
+  if (std::min(m, n) < NS_SMALL_R) return 2;
   return (form == PRM_NS_FORM_AUTO && gram_route_pays(std::min(m, n), std::max(m, n))) ? 1 : 0;
 }
 

@@ -21,7 +21,6 @@
 
 #include <algorithm>
 #include <cmath>
-#include <mutex>
 
 #include "internal.h"
 #include "prm.h"
@@ -101,21 +100,15 @@ __global__ void __launch_bounds__(NA_TX* NA_TY) na_update(TallArgs a, const floa
   }
 }
 
-// Device address of the scratch array, looked up once per device.
-constexpr int MAX_DEVICES = 64;
-std::mutex g_na_mutex;
-float* g_na_ptr[MAX_DEVICES] = {};
-
+// Device address of the scratch array on the current device. Looked up on
+// every call rather than cached: the address belongs to the device's
+// context, and a context that was torn down and recreated (a device reset in
+// the host process) places the array elsewhere. The lookup allocates
+// nothing; on the first call on a device it also loads this module there.
 int scratch_for_current_device(float** out) {
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEVICES) return PRM_ERR_CUDA;
-  std::lock_guard<std::mutex> lock(g_na_mutex);
-  if (g_na_ptr[dev] == nullptr) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return PRM_ERR_CUDA;
-    g_na_ptr[dev] = static_cast<float*>(p);
-  }
-  *out = g_na_ptr[dev];
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return PRM_ERR_CUDA;
+  *out = static_cast<float*>(p);
   return PRM_OK;
 }
 

@@ -27,7 +27,8 @@ PRM_FAMILY_NS_PREP = 2
 PRM_FAMILY_NS_GRAM = 3
 PRM_FAMILY_NS_POLY = 4
 PRM_FAMILY_NS_COMBINE = 5
-FAMILY_NAMES = ["rownorm_wide", "rownorm_tall", "ns_prep", "ns_gram", "ns_poly", "ns_combine", "ns_sym"]
+FAMILY_NAMES = ["rownorm_wide", "rownorm_tall", "ns_prep", "ns_gram", "ns_poly", "ns_combine", "ns_sym",
+                "ns_small"]
 
 PRM_FP32 = 0
 PRM_BF16 = 1

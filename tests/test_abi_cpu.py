@@ -58,20 +58,26 @@ def test_branch_schedule_matches_oracle(lib):
 
 
 def test_ns_route_thresholds(lib):
-    """The planner's Gram-route choice: taken when its executed work for five
-    rounds is at least 10 % below the direct rounds' -- from c = 1.37 r at
-    r = 2048, c = 1.9 r for r <= 256 -- never for square matrices, never in
-    the direct form; the orientation does not matter."""
+    """The planner's route choice. Short sides below 64 take the fp32
+    CUDA-core rounds (2). Otherwise the Gram route (1) is taken when its
+    executed work for five rounds is at least 10 % below the direct rounds'
+    -- from c = 1.37 r at r = 2048, c = 1.9 r for r <= 256 -- never for
+    square matrices, never in the direct form; the orientation does not
+    matter."""
     def first_c(r):
         return next(c for c in range(r, 4 * r) if N.prm_ns_route(r, c) == 1)
     assert first_c(2048) == 2802   # 1.368 r
     assert first_c(256) == 487     # 1.902 r
     assert first_c(64) == 122
-    for (m, n) in [(2048, 8192), (8192, 2048), (2048, 6144), (5120, 20480), (768, 2048), (256, 2048), (1, 300)]:
+    for (m, n) in [(2048, 8192), (8192, 2048), (2048, 6144), (5120, 20480), (768, 2048), (256, 2048), (64, 300)]:
         assert N.prm_ns_route(m, n) == 1, (m, n)
         assert N.prm_ns_route(m, n, N.PRM_NS_FORM_DIRECT) == 0
-    for (m, n) in [(2048, 2048), (5120, 5120), (1536, 2048), (2, 3), (8, 8), (320, 400)]:
+    for (m, n) in [(2048, 2048), (5120, 5120), (1536, 2048), (64, 64), (320, 400)]:
         assert N.prm_ns_route(m, n) == 0, (m, n)
+    # short sides below 64 take the fp32 CUDA-core rounds in both forms
+    for (m, n) in [(1, 300), (300, 1), (2, 3), (8, 8), (63, 100000), (100000, 63)]:
+        assert N.prm_ns_route(m, n) == 2, (m, n)
+        assert N.prm_ns_route(m, n, N.PRM_NS_FORM_DIRECT) == 2, (m, n)
     assert N.prm_ns_route(0, 5) == -N.PRM_ERR_INVALID_ARG
     assert N.prm_ns_route(5, 5, 9) == -N.PRM_ERR_INVALID_ARG
 

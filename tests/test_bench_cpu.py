@@ -45,3 +45,41 @@ def test_ns5_algorithmic_flop_counts():
     assert abs(blk / 2.774e13 - 1) < 1e-3
     # a square matrix: 5 (4 + 2) r^3
     assert bench._ns_flops(64, 64) == 30 * 64 ** 3
+
+
+def test_leg_selection():
+    a = bench.parse_args([])
+    assert bench.leg_names(a) == ["dit_1p3b_muonbp", "dit_15b"]
+    assert bench.leg_names(bench.parse_args(["--legs", "none"])) == []
+    assert bench.leg_names(bench.parse_args(["--workload", "dit_15b"])) == []
+    # the headline workload is never repeated as a leg
+    assert bench.leg_names(bench.parse_args(["--workload", "dit_15b", "--legs", "dit_15b,dit_1p3b_muonbp"])) == \
+        ["dit_1p3b_muonbp"]
+
+
+def test_rate_summaries_are_fractions_of_the_peaks():
+    """Executed NS5 rate and RowNorm bandwidth from per-family totals: the
+    NS5 fraction divides executed FLOPs (what the launches compute) by the
+    GEMM time; the metric count over the same time is reported beside it."""
+    fam = {k: dict(ms=0.0, records=0, kernels=0, work=0.0) for k in
+           ("rownorm_wide", "rownorm_tall", "ns_prep", "ns_gram", "ns_poly", "ns_combine", "ns_sym", "ns_small")}
+    fam["ns_gram"].update(ms=2.0, records=1, work=3.0e12)
+    fam["ns_combine"].update(ms=3.0, records=1, work=5.0e12)
+    out = bench.ns5_summary(fam, alg_flops=1.2e13, cycles=2, tf_sus=1600.0, tf_burst=1900.0)
+    assert out["gemm_ms_per_cycle"] == 2.5
+    assert out["tflops_executed"] == 1600.0 and out["frac_executed"] == 1.0
+    assert out["tflops_metric_count"] == 2400.0
+    fam["rownorm_wide"].update(ms=1.0, records=2, work=6.0e9)
+    fam["rownorm_tall"].update(ms=1.0, records=2, work=4.0e9)
+    rn = bench.rownorm_summary(fam, hbm=6000.0)
+    assert rn["wide"] == {"gbs": 6000.0, "frac": 1.0} and rn["tall"]["frac"] == round(4000 / 6000, 4)
+    assert rn["gbs"] == 5000.0
+
+
+def test_oracle_sample_is_bounded_and_labelled():
+    """The one sampling both arms use: on the tiny set it times a 64 x 64 NS5
+    and the RowNorm of every shape, well under a second, and says so."""
+    from matrix_aware_optimizer_gb300 import synth
+    v, sample, secs = bench.oracle_cycle_sample(synth.MATRIX_SETS["tiny"])
+    assert v > 0 and secs < 5.0
+    assert sample.startswith("timed:") and "64x64" in sample

@@ -25,20 +25,7 @@ pytestmark = pytest.mark.gpu
 TOL_M = 1e-6
 TOL_W_ROWNORM = 1e-5
 TOL_D_ROWNORM = 1e-4
-TOL_D_NS5 = 2e-2
-# Matrices with a short side below 16 hold too few elements for rounding
-# errors to average out. Each of the five rounds rounds X, C and P to 16 bits
-# (relative 2^-9 for bf16), and the quintic's slope, at most a = 3.44 near 0,
-# amplifies what came before: 5 rounds x 3 roundings x 3.44 x 2^-9 ~ 0.1 is
-# the worst case when nothing averages. An emulation of the kernels'
-# arithmetic over 400 random inputs reaches 7.2% on 2x3 and 6.2% on 8x8
-# matrices (95th percentiles 2.6% and 2.1%); evaluating a X + B X with bf16 A
-# instead gives 7.7% and 8.7%.
-TOL_D_NS5_TINY = 1e-1
-
-
-def tol_ns5(r: int) -> float:
-    return TOL_D_NS5 if r >= 16 else TOL_D_NS5_TINY
+TOL_D_NS5 = 2e-2  # every shape: short sides below 64 run their rounds in fp32
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -47,18 +34,18 @@ def _lib():
     N.load()
 
 
-def _hp(ms):
-    return dict(K=ms.K, gamma=ms.gamma, lr=ms.lr, wd=ms.wd, beta=ms.beta, eps=ms.eps)
+def _hp(ms, K=None):
+    return dict(K=ms.K if K is None else K, gamma=ms.gamma, lr=ms.lr, wd=ms.wd, beta=ms.beta, eps=ms.eps)
 
 
-def _run_teacher_forced(ms, steps, check_idx=None, mode="prmuon", blocks=0, ns_form="auto"):
+def _run_teacher_forced(ms, steps, check_idx=None, mode="prmuon", blocks=0, ns_form="auto", K=None):
     shapes = ms.shapes
     Ws, Ms = synth.make_state(ms, device="cuda")
     gdt = torch.bfloat16 if ms.grad_dtype == synth.GRAD_BF16 else torch.float32
     grads = [torch.empty(s, device="cuda", dtype=gdt) for s in shapes]
     opt = PeriodicRowMuon(Ws, Ms, grads, muonbp_blocks=blocks, ns_form=ns_form)
     opt.workspace.fill_(0xFF)  # NaN bit patterns: any read of unwritten scratch shows up
-    hp = _hp(ms)
+    hp = _hp(ms, K)
     idx = range(len(shapes)) if check_idx is None else check_idx
     report = []
     for t in steps:
@@ -66,9 +53,9 @@ def _run_teacher_forced(ms, steps, check_idx=None, mode="prmuon", blocks=0, ns_f
             synth.make_grad(shapes[i], ms.seed, t, i, ms.grad_std, ms.grad_dtype, ms.row_sigma, device="cuda", out=g)
         torch.cuda.synchronize()
         prev = {i: (host64(Ws[i]), host64(Ms[i]), host64(grads[i])) for i in idx}
-        branch = opt.step(t, K=ms.K, gamma=ms.gamma, lr=ms.lr, wd=ms.wd, beta=ms.beta, eps=ms.eps, mode=mode)
+        branch = opt.step(t, mode=mode, **hp)
         opt.sync_status()
-        assert branch == O.refresh_indicator(t, ms.K)
+        assert branch == O.refresh_indicator(t, hp["K"])
         for i in idx:
             W0, M0, G0 = prev[i]
             m, n = shapes[i]
@@ -134,6 +121,54 @@ def test_free_running_tiny_matches_oracle():
     opt.close()
 
 
+@pytest.mark.parametrize("set_name", ["tiny", "dit_block_d2048"])
+def test_vanilla_muon_k1_teacher_forced(set_name):
+    """K = 1 (vanilla Muon): every step is a refresh, so each step's NS5 reads
+    the momentum that the previous refresh left behind. Four consecutive
+    refreshes, each checked on its own against the oracle."""
+    ms = synth.MATRIX_SETS[set_name]
+    rep = _run_teacher_forced(ms, range(4), K=1)
+    assert all(r[2] == 1 for r in rep)
+
+
+def test_vanilla_muon_k1_free_running():
+    """Five K = 1 steps on the tiny set without teacher forcing, against
+    oracle.run_steps(..., K=1). The momentum does not depend on W, so it must
+    match to fp32 rounding; W differs from the oracle's only through the NS5
+    direction errors, each within TOL_D_NS5 of the oracle's direction, which
+    enter W as lr * s * (error in D): the bound below adds them up over the
+    steps (decayed like W)."""
+    ms = synth.MATRIX_SETS["tiny"]
+    steps, K = 5, 1
+    Ws, Ms = synth.make_state(ms, device="cuda")
+    W0 = [host64(w) for w in Ws]
+    grads = [torch.empty(s, device="cuda") for s in ms.shapes]
+    opt = PeriodicRowMuon(Ws, Ms, grads)
+    opt.workspace.fill_(0xFF)
+    host_grads = {}
+    for t in range(steps):
+        for i, g in enumerate(grads):
+            synth.make_grad(ms.shapes[i], ms.seed, t, i, ms.grad_std, ms.grad_dtype, ms.row_sigma, device="cuda", out=g)
+            host_grads[(t, i)] = host64(g)
+        assert opt.step(t, K=K, gamma=ms.gamma, lr=ms.lr, wd=ms.wd, beta=ms.beta, eps=ms.eps) == 1
+    opt.sync_status()
+    Wo, Mo, br = O.run_steps(W0, [np.zeros(s) for s in ms.shapes], lambda t, i: host_grads[(t, i)], 0, steps,
+                             K, ms.gamma, ms.lr, ms.wd, ms.beta, ms.eps)
+    assert br == [1] * steps
+    decay = 1.0 - ms.lr * ms.wd
+    for i, (m, n) in enumerate(ms.shapes):
+        # the oracle's own directions, step by step, for the error budget
+        M = np.zeros((m, n))
+        bound = 0.0
+        for t in range(steps):
+            M = O.momentum_update(M, host_grads[(t, i)], ms.beta)
+            bound = bound * decay + ms.lr * O.lr_shape_scale(m, n) * TOL_D_NS5 * np.linalg.norm(O.newton_schulz(M))
+        assert rel_frob(host64(Ms[i]), Mo[i]) <= TOL_M
+        err = np.linalg.norm(host64(Ws[i]) - Wo[i])
+        assert err <= bound, (i, err, bound)
+    opt.close()
+
+
 EDGE_SHAPES = [(1, 300), (300, 1), (37, 104), (100, 40), (129, 257), (257, 129), (8, 8), (64, 4100), (2, 3)]
 
 
@@ -169,8 +204,7 @@ def test_edge_shapes_directions(gdtype):
             Dg = -host64(Ws[i]) / (eta * s)
             if t % K == 0:
                 Do = O.newton_schulz(Gh[i])
-                tol = tol_ns5(min(m, n))
-                assert rel_frob(Dg, Do) <= tol, ((m, n), rel_frob(Dg, Do))
+                assert rel_frob(Dg, Do) <= TOL_D_NS5, ((m, n), rel_frob(Dg, Do))
             else:
                 Do = O.row_normalize(Gh[i], eps)
                 assert rel_frob(Dg, Do) <= 1e-6, ((m, n), rel_frob(Dg, Do))
@@ -211,6 +245,29 @@ def test_muonbp_block_and_full_steps():
             Dg = -host64(Ws[i]) / (eta * O.lr_shape_scale(m, n))
             assert rel_frob(Dg, Do) <= TOL_D_NS5, ((m, n), t, rel_frob(Dg, Do))
         opt.close()
+
+
+# Long sides that the block count does not divide: the last block takes the
+# remainder, so block shapes differ within one matrix and block offsets are
+# not multiples of 16 bytes (300 x 1003: 125 columns = 500 bytes; 385 x 385
+# with P = 3: rows of 1540 bytes). 1003 x 301 splits into wide 125 x 301
+# blocks; 96 x 645 into tall 96 x 80 blocks and a 96 x 85 one; 40 x 1001 and
+# 100 x 40 have blocks with short sides below 64 (the fp32 rounds).
+REMAINDER_SETS = {
+    8: ((300, 1003), (1003, 301), (96, 645), (40, 1001), (100, 40)),
+    3: ((385, 385), (300, 1003), (1003, 301), (100, 40)),
+}
+
+
+@pytest.mark.parametrize("P", [8, 3])
+def test_muonbp_remainder_blocks(P):
+    """MuonBP with P not dividing the long side, teacher-forced against
+    oracle.muonbp_step: a full step (t = 0), two block steps (t = 1, 2) and the
+    next full step (t = 3)."""
+    assert all(max(shp) % P != 0 for shp in REMAINDER_SETS[P])
+    ms = make_set(REMAINDER_SETS[P], synth.GRAD_BF16, seed=40 + P)
+    rep = _run_teacher_forced(ms, range(4), mode="muonbp", blocks=P)
+    assert [r[2] for r in rep[::len(REMAINDER_SETS[P])]] == [1, 0, 0, 1]
 
 
 def test_resume_is_bitwise():

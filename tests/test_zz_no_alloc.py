@@ -1,10 +1,13 @@
 """The allocation-free tall RowNorm step (for callers that cannot allocate
 device memory while the update runs) against the regular workspace-based
-path of prm_step, on two calls in a row. Collected last on purpose."""
+path of prm_step, on two calls in a row, against the fp64 oracle, and at the
+edge of its fixed scratch array. Collected last on purpose."""
 
+import numpy as np
 import pytest
 import torch
 
+import oracle as O
 from matrix_aware_optimizer_gb300 import native as N
 from matrix_aware_optimizer_gb300.optimizer import PeriodicRowMuon
 
@@ -61,3 +64,56 @@ def test_noalloc_rejects_what_it_cannot_hold():
                                              None) == N.PRM_ERR_SHAPE
     assert lib.prm_rownorm_tall_step_noalloc(None, p, p, N.PRM_FP32, 64, 8, 0.15, 0.02, 0.01, 0.95, 1e-8, 0.0,
                                              None) == N.PRM_ERR_INVALID_ARG
+
+
+def _rel_frob_dev(a, b):
+    """Relative Frobenius error in fp64, on the device (large tensors)."""
+    a64, b64 = a.double(), b.double()
+    return float(torch.linalg.norm(a64 - b64) / torch.linalg.norm(b64))
+
+
+def _noalloc(W, M, G, shape, stream=None):
+    gcode = N.PRM_BF16 if G.dtype == torch.bfloat16 else N.PRM_FP32
+    N.prm_rownorm_tall_step_noalloc(W.data_ptr(), M.data_ptr(), G.data_ptr(), gcode, shape[0], shape[1],
+                                    HP["gamma"], HP["lr"], HP["wd"], HP["beta"], HP["eps"], 0.0,
+                                    stream if stream is not None else torch.cuda.current_stream().cuda_stream)
+
+
+@pytest.mark.parametrize("shape,gdtype", [((1000, 40), torch.float32), ((4100, 132), torch.bfloat16)])
+def test_noalloc_matches_oracle_twice(shape, gdtype):
+    """Two allocation-free calls in a row, each checked against
+    oracle.prmuon_step on the state the call started from."""
+    W, M, G = _state(shape, gdtype, seed=7 + shape[1])
+    for t in (1, 2):
+        W0, M0, G0 = (x.double().cpu().numpy() for x in (W, M, G))
+        _noalloc(W, M, G, shape)
+        torch.cuda.synchronize()
+        W1, M1, _, rho = O.prmuon_step(W0, M0, G0, t, **HP)
+        assert rho == 0
+        assert rel_frob(M.double().cpu().numpy(), M1) <= TOL_M
+        assert rel_frob(W.double().cpu().numpy(), W1) <= TOL_W
+
+
+def test_noalloc_at_capacity_and_just_beyond():
+    """130816 x 2048 needs exactly 511 * 2048 + 2048 = 1,048,576 scratch
+    floats, the whole array: accepted, and equal to prm_step within the
+    tolerances on two calls in a row. One more 256-row block (131072 x 2048)
+    is refused before any launch."""
+    shape = (130816, 2048)
+    assert (shape[0] + 255) // 256 * shape[1] + shape[1] == 1 << 20
+    W, M, G = _state(shape, torch.bfloat16, seed=5)
+    W2, M2 = W.clone(), M.clone()
+    opt = PeriodicRowMuon([W], [M], [G])
+    for t in (1, 2):
+        opt.step(t, **HP)
+        _noalloc(W2, M2, G, shape)
+        torch.cuda.synchronize()
+        assert _rel_frob_dev(M2, M) <= TOL_M
+        assert _rel_frob_dev(W2, W) <= TOL_W
+    opt.close()
+    del W, M, G, W2, M2
+    lib = N.load()
+    buf = torch.zeros(64, device="cuda")
+    p = buf.data_ptr()
+    assert lib.prm_rownorm_tall_step_noalloc(p, p, p, N.PRM_BF16, 131072, 2048, 0.15, 0.02, 0.01, 0.95, 1e-8, 0.0,
+                                             None) == N.PRM_ERR_UNSUPPORTED
