@@ -60,10 +60,18 @@ struct TallFusedScratch {
 };
 bool tall_fused_fits(int count, int64_t rows, int64_t cols);  // queue and offsets within 32-bit limits
 TallFusedScratch tall_fused_scratch(int count, int64_t rows, int64_t cols);
+// ring: the TMA form (tall_ring_kernel, one CTA per SM with a producer warp
+// and a ring of shared-memory stages); needs tall_ring_ok.
+bool tall_ring_ok(int64_t cols, bool grad_bf16);
+cudaError_t rownorm_setup_attributes();
+// Ring form: tensor maps of each view's M, G and W (3 per view, device
+// memory, in view order), boxes of tall_ring_box_cols() x tall_ring_box_rows().
+int tall_ring_box_cols();
+int tall_ring_box_rows();
 cudaError_t launch_rownorm_tall_fused(const View* d_views, int count, int64_t rows, int64_t cols, bool grad_bf16,
                                       StepScalars s, float* partials, float* inv, void* flags, int* err,
-                                      int num_sms, cudaStream_t stream, int withhold_stripe = -1,
-                                      uint64_t wait_ns = 0);
+                                      int num_sms, cudaStream_t stream, const CUtensorMap* ring_maps,
+                                      int withhold_stripe = -1, uint64_t wait_ns = 0);
 
 // ---- refresh (NS5) branch ---------------------------------------------
 // Momentum update + bf16 pack into X (wide: same orientation; tall:
@@ -127,6 +135,9 @@ struct SymMaps {
 };
 
 int encode_x_maps(NsMaps* maps, const void* X, int batch, int64_t r, int64_t c, int64_t ldc);
+// 2-D map over one row-major fp32 or bf16 matrix (no swizzle; box_cols x box_rows boxes)
+int encode_rows_2d(CUtensorMap* map, const void* base, bool bf16_elems, int64_t rows, int64_t cols, int64_t ld,
+                   uint32_t box_cols, uint32_t box_rows);
 int encode_sym_maps(SymMaps* maps, const void* A, int batch, int64_t r, int64_t ldr);
 
 // One same-shape batch of a GEMM launch: `batch` matrices. GRAM: out =

@@ -688,6 +688,24 @@ cudaError_t launch_kind(const GemmParams& p, int num_sms, cudaStream_t stream) {
 
 }  // namespace
 
+// 2-D map over a row-major rows x cols matrix of fp32 or bf16 elements with
+// row pitch ld (elements), box = box_cols x box_rows, no swizzle;
+// out-of-range elements of a box read as zero.
+int encode_rows_2d(CUtensorMap* map, const void* base, bool bf16_elems, int64_t rows, int64_t cols, int64_t ld,
+                   uint32_t box_cols, uint32_t box_rows) {
+  auto enc = tensor_map_encoder();
+  if (enc == nullptr) return -1;
+  const cuuint64_t esize = bf16_elems ? 2 : 4;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * esize};
+  cuuint32_t box[2] = {box_cols, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(map, bf16_elems ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
+                   const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? 0 : static_cast<int>(r);
+}
+
 size_t gemm_smem_bytes() { return SMEM_BYTES; }
 
 cudaError_t gemm_setup_attributes() {

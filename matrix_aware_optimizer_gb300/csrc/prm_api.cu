@@ -46,6 +46,8 @@ struct LaunchSet {
   // tall RowNorm: the one-launch form (aligned views within its size limits)
   // or three launches; scratch offsets relative to the workspace base
   bool fused = false;
+  bool ring = false;  // the one-launch form with the TMA ring (needs tall_ring_ok)
+  CUtensorMap* d_maps = nullptr;  // ring: per view the tensor maps of M, G and W (device)
   size_t off_partials = 0, off_inv = 0, off_flags = 0;
 };
 
@@ -108,8 +110,29 @@ struct RowNormPlan {
 void free_sets(std::vector<LaunchSet>& sets) {
   for (auto& s : sets) {
     if (s.d_views) cudaFree(s.d_views);
+    if (s.d_maps) cudaFree(s.d_maps);
     s.d_views = nullptr;
+    s.d_maps = nullptr;
   }
+}
+
+// Tensor maps of a ring-form tall launch set: per view M (fp32), G (fp32 or
+// bf16) and W (fp32), boxes of the ring kernel's stage shape, copied to
+// device memory (the kernel reads them from there).
+cudaError_t upload_ring_maps(LaunchSet& s) {
+  std::vector<CUtensorMap> maps(3 * s.views.size());
+  const uint32_t bc = static_cast<uint32_t>(tall_ring_box_cols()), br = static_cast<uint32_t>(tall_ring_box_rows());
+  for (size_t i = 0; i < s.views.size(); ++i) {
+    const View& v = s.views[i];
+    if (encode_rows_2d(&maps[3 * i + 0], v.M, false, v.rows, v.cols, v.ld, bc, br) != 0 ||
+        encode_rows_2d(&maps[3 * i + 1], v.G, s.bf16, v.rows, v.cols, v.ld, bc, br) != 0 ||
+        encode_rows_2d(&maps[3 * i + 2], v.W, false, v.rows, v.cols, v.ld, bc, br) != 0)
+      return cudaErrorInvalidValue;
+  }
+  const size_t bytes = maps.size() * sizeof(CUtensorMap);
+  cudaError_t e = cudaMalloc(reinterpret_cast<void**>(&s.d_maps), bytes);
+  if (e != cudaSuccess) return e;
+  return cudaMemcpy(s.d_maps, maps.data(), bytes, cudaMemcpyHostToDevice);
 }
 
 void free_plan(NsPlan& p) {
@@ -785,7 +808,8 @@ int run_rownorm(prm_ctx* c, void* base, StepScalars sc, cudaStream_t stream) {
     const int n = static_cast<int>(s.views.size());
     if (s.fused)
       e = launch_rownorm_tall_fused(s.d_views, n, s.rows, s.cols, s.bf16, sc, partials, inv, b + s.off_flags,
-                                    c->d_err, c->num_sms, stream, c->withhold.stripe, c->withhold.wait_ns);
+                                    c->d_err, c->num_sms, stream, s.ring ? s.d_maps : nullptr, c->withhold.stripe,
+                                    c->withhold.wait_ns);
     else
       e = launch_rownorm_tall(s.d_views, n, s.rows, s.cols, s.vec_ok, s.bf16, sc, partials, inv, stream);
     if (e != cudaSuccess) return cuda_fail(c, e, "rownorm tall launch");
@@ -817,7 +841,7 @@ int device_state(DeviceState** out) {
     if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return PRM_ERR_CUDA;
     if (prop.major != 10) return PRM_ERR_UNSUPPORTED;
     d.num_sms = prop.multiProcessorCount;
-    if (gemm_setup_attributes() != cudaSuccess) return PRM_ERR_CUDA;
+    if (gemm_setup_attributes() != cudaSuccess || rownorm_setup_attributes() != cudaSuccess) return PRM_ERR_CUDA;
     if (cudaMalloc(reinterpret_cast<void**>(&d.d_err), sizeof(int)) != cudaSuccess) return PRM_ERR_CUDA;
     if (cudaMemset(d.d_err, 0, sizeof(int)) != cudaSuccess) return PRM_ERR_CUDA;
     d.ready = true;
@@ -849,7 +873,7 @@ int prm_create(prm_ctx** out, int cuda_device) {
   c->device = cuda_device;
   c->num_sms = prop.multiProcessorCount;
   DeviceGuard guard(cuda_device);
-  if ((e = gemm_setup_attributes()) != cudaSuccess) {
+  if ((e = gemm_setup_attributes()) != cudaSuccess || (e = rownorm_setup_attributes()) != cudaSuccess) {
     delete c;
     return fail(nullptr, PRM_ERR_CUDA, std::string("cudaFuncSetAttribute: ") + cudaGetErrorString(e));
   }
@@ -930,6 +954,7 @@ int prm_register_matrices(prm_ctx* c, const prm_matrix_desc* d, int count, int m
   size_t off = 0;
   for (auto& s : c->rn.tall) {
     s.fused = s.vec_ok && tall_fused_fits(static_cast<int>(s.views.size()), s.rows, s.cols);
+    s.ring = s.fused && tall_ring_ok(s.cols, s.bf16);
     if (s.fused) {
       const TallFusedScratch t = tall_fused_scratch(static_cast<int>(s.views.size()), s.rows, s.cols);
       s.off_partials = off;
@@ -950,6 +975,8 @@ int prm_register_matrices(prm_ctx* c, const prm_matrix_desc* d, int count, int m
   if (muonbp_blocks > 0) build_ns_subplans(blocks, c->ws_limit, c->ns_form, c->ns_blocks);
   cudaError_t e = upload_sets(c->rn.wide);
   if (e == cudaSuccess) e = upload_sets(c->rn.tall);
+  for (auto& s : c->rn.tall)
+    if (e == cudaSuccess && s.ring) e = upload_ring_maps(s);
   for (auto* plans : {&c->ns_full, &c->ns_blocks})
     for (auto& p : *plans)
       for (auto& g : p.groups)
@@ -1071,12 +1098,12 @@ int prm_step(prm_ctx* c, int64_t t, int K, float gamma, float lr, float wd, floa
   return PRM_OK;
 }
 
-// Whether the RowNorm step ran the one-launch tall kernel for this view's
-// launch set.
-static bool step_used_fused(const prm_ctx* c, const View& v) {
+// The launch set of the RowNorm step that holds this tall view (its choice
+// of the one-launch kernel and of the ring form), or nullptr.
+static const LaunchSet* tall_set_of(const prm_ctx* c, const View& v) {
   for (const auto& s : c->rn.tall)
-    if (s.rows == v.rows && s.cols == v.cols && s.bf16 == (v.grad_bf16 != 0)) return s.fused;
-  return false;
+    if (s.rows == v.rows && s.cols == v.cols && s.bf16 == (v.grad_bf16 != 0)) return &s;
+  return nullptr;
 }
 
 // Recomputes the direction D of the last step for one matrix from its
@@ -1140,7 +1167,7 @@ int prm_debug_last_direction(prm_ctx* c, int idx, float* host_out) {
     const LaunchSet& s = sets.front();
     if (v.rows <= v.cols) {
       e = launch_rownorm_wide(s.d_views, 1, v.rows, v.cols, s.vec_ok, false, sc, st);
-    } else if (step_used_fused(c, v) && tall_fused_fits(1, v.rows, v.cols)) {
+    } else if (tall_set_of(c, v) != nullptr && tall_set_of(c, v)->fused && tall_fused_fits(1, v.rows, v.cols)) {
       // the step's own one-launch kernel, so that D matches what it applied
       const TallFusedScratch t = tall_fused_scratch(1, v.rows, v.cols);
       float* d_part = static_cast<float*>(dev_alloc(t.partials_bytes));
@@ -1150,8 +1177,16 @@ int prm_debug_last_direction(prm_ctx* c, int idx, float* host_out) {
         free_sets(sets);
         return finish(fail(c, PRM_ERR_OOM, "no device memory for scratch"));
       }
-      e = launch_rownorm_tall_fused(s.d_views, 1, v.rows, v.cols, false, sc, d_part, d_inv, d_flags, c->d_err,
-                                    c->num_sms, st);
+      // the same form as the step (the fp32 zero G here qualifies for the
+      // ring whenever the step's gradients did)
+      LaunchSet& ls = sets.front();
+      const bool ring = tall_set_of(c, v)->ring;
+      if (ring && (e = upload_ring_maps(ls)) != cudaSuccess) {
+        free_sets(sets);
+        return finish(cuda_fail(c, e, "ring tensor maps"));
+      }
+      e = launch_rownorm_tall_fused(ls.d_views, 1, v.rows, v.cols, false, sc, d_part, d_inv, d_flags, c->d_err,
+                                    c->num_sms, st, ring ? ls.d_maps : nullptr);
     } else {
       const size_t pb = static_cast<size_t>(tall_row_blocks(v.rows)) * v.cols * sizeof(float);
       float* d_part = static_cast<float*>(dev_alloc(pb));

@@ -333,6 +333,7 @@ struct FusedTall {
   int* err;
   int withhold;      // test aid: stripe whose norms are not published (-1: none)
   uint64_t wait_ns;  // limit of one update tile's wait
+  const CUtensorMap* maps;  // ring form: per view the maps of M, G and W
 };
 
 // Queue position -> (phase 3?, stripe, row block); the queue holds fewer
@@ -555,6 +556,277 @@ __global__ void __launch_bounds__(FT_THREADS, FT_CTAS_PER_SM) tall_fused_kernel(
   }
 }
 
+// ------------------------------------------ tall columns, fused, TMA ring
+// The same queue of phase-1 / phase-3 tiles and the same stripe protocol as
+// tall_fused_kernel, with the loads moved off the compute warps: one CTA per
+// SM, a producer warp that claims tiles and streams each tile into a ring of
+// shared-memory stages with TMA tensor loads (a 128-column x 32-row box of M
+// and one of G or W per stage, six stages: up to ~190 KB of loads in flight
+// per SM), and eight consumer warps that update M or W from the staged rows
+// and store the results. A phase-3 tile's loads of M are issued only after
+// its stripe's inverse norms are published (acquire, then a proxy fence, so
+// that the tensor loads see the momentum other CTAs stored). The maps need
+// 16-byte row pitches: cols % 4 == 0, and cols % 8 == 0 with bf16 gradients.
+constexpr int RG_CONSUMER_WARPS = 8;
+constexpr int RG_CONSUMERS = 32 * RG_CONSUMER_WARPS;
+constexpr int RG_THREADS = 32 + RG_CONSUMERS;
+constexpr int RG_SR = 32;                              // rows per stage (one per producer lane)
+constexpr int RG_STAGES = 6;
+constexpr int RG_ROWS_PER_WARP = RG_SR / RG_CONSUMER_WARPS;  // 4
+constexpr uint32_t RG_ROW_BYTES = FT_COLS * 4;         // 512 (fp32 box rows)
+constexpr uint32_t RG_GROW_BYTES = FT_COLS * 2;        // 256 (bf16 box rows)
+constexpr uint32_t RG_ARR_BYTES = RG_SR * RG_ROW_BYTES;  // 16 KB
+constexpr uint32_t RG_STAGE_BYTES = 2 * RG_ARR_BYTES + FT_COLS * 4;  // M, G or W, inverse norms
+constexpr int RG_KIND_P1 = 0, RG_KIND_P3 = 1, RG_KIND_DONE = 2;
+static_assert(FT_TILE_ROWS % RG_SR == 0, "a tile is a whole number of stages");
+static_assert(FT_COLS == 4 * 32, "one float4 column group per consumer lane");
+
+struct RgMeta {
+  int kind, s, rb, view;
+  int64_t row0;  // first row of the stage
+  int nrows;     // rows in the stage (the last stage of a ragged tile has fewer)
+  int ncols;     // valid columns of the stripe (the ragged last stripe has fewer)
+  int last;      // last stage of its tile
+  int pad;
+};
+constexpr size_t RG_SMEM_BYTES = 128 + RG_STAGES * RG_STAGE_BYTES + RG_STAGES * sizeof(RgMeta) +
+                                 2 * RG_STAGES * sizeof(uint64_t) + RG_CONSUMER_WARPS * FT_COLS * 4 + 64;
+static_assert(RG_SMEM_BYTES <= 232448, "ring above the 227 KB per-block limit");
+
+__device__ __forceinline__ int shfl0(int v) { return __shfl_sync(0xffffffffu, v, 0); }
+
+template <bool BF16>
+__global__ void __launch_bounds__(RG_THREADS, 1) tall_ring_kernel(const FusedTall a) {
+  extern __shared__ uint8_t rg_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(rg_raw) + 127) & ~uintptr_t(127));
+  uint8_t* stages = base;
+  RgMeta* meta = reinterpret_cast<RgMeta*>(base + RG_STAGES * RG_STAGE_BYTES);
+  uint64_t* full = reinterpret_cast<uint64_t*>(meta + RG_STAGES);
+  uint64_t* empty = full + RG_STAGES;
+  float* red = reinterpret_cast<float*>(empty + RG_STAGES);  // [RG_CONSUMER_WARPS][FT_COLS]
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(red + RG_CONSUMER_WARPS * FT_COLS);
+  int* flag_sh = const_cast<int*>(abort_flag) + 1;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  if (threadIdx.x == 0) {
+    for (int k = 0; k < RG_STAGES; ++k) {
+      mbar_init(&full[k], 1);
+      mbar_init(&empty[k], RG_CONSUMER_WARPS);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  if (warp == 0) {
+    // ---- producer: claim tiles, wait for phase-3 flags, stream rows in
+    const uint64_t pol_first = l2_policy_evict_first();
+    int stage = 0;
+    uint32_t phase = 0;
+    uint32_t issued = 0, issued_parity = 0;  // stages with copies in flight (for the abort drain)
+    bool ok = true;
+    for (;;) {
+      int tile = 0;
+      if (lane == 0) tile = static_cast<int>(min(atomicAdd(a.claim, 1ull), 0x7fffffffull));
+      tile = shfl0(tile);
+      if (tile >= a.total) break;
+      bool p3;
+      int s, rb;
+      ft_decode(a, tile, p3, s, rb);
+      const int view = s / a.spv;
+      const View* v = a.views + view;
+      const int64_t c0 = static_cast<int64_t>(s % a.spv) * FT_COLS;
+      const int ncols = static_cast<int>(a.cols - c0 < FT_COLS ? a.cols - c0 : FT_COLS);
+      const int64_t row0 = static_cast<int64_t>(rb) * FT_TILE_ROWS;
+      const int tile_rows = static_cast<int>(a.rows - row0 < FT_TILE_ROWS ? a.rows - row0 : FT_TILE_ROWS);
+      if (p3) {
+        int go = 0;
+        if (lane == 0) {
+          bool got = ld_acquire_gpu(a.ready + s) != 0;
+          if (!got) {
+            const uint64_t t0 = global_timer_ns();
+            while (!(got = ld_acquire_gpu(a.ready + s) != 0)) {
+              if (global_timer_ns() - t0 > a.wait_ns) {
+                atomicExch(a.err, DEV_ERR_TIMEOUT);
+                break;
+              }
+              __nanosleep(200);
+            }
+          }
+          if (got) fence_proxy_async_global();
+          go = got ? 1 : 0;
+        }
+        if (!shfl0(go)) continue;  // the stripe's norms never came: its W stays as it was
+      }
+      const int nst = (tile_rows + RG_SR - 1) / RG_SR;
+      for (int k = 0; k < nst && ok; ++k) {
+        int got = 1;
+        if (lane == 0) got = wait_bounded(&empty[stage], phase ^ 1u, abort_flag, a.err, FT_WAIT_LIMIT_NS) ? 1 : 0;
+        if (!shfl0(got)) {
+          ok = false;
+          break;
+        }
+        const int nrows = min(RG_SR, tile_rows - k * RG_SR);
+        const int64_t r0 = row0 + static_cast<int64_t>(k) * RG_SR;
+        uint8_t* st = stages + static_cast<size_t>(stage) * RG_STAGE_BYTES;
+        if (lane == 0) {
+          RgMeta& m = meta[stage];
+          m.kind = p3 ? RG_KIND_P3 : RG_KIND_P1;
+          m.s = s;
+          m.rb = rb;
+          m.view = view;
+          m.row0 = r0;
+          m.nrows = nrows;
+          m.ncols = ncols;
+          m.last = k == nst - 1;
+          // whole boxes land (rows or columns past the matrix read as zero)
+          const uint32_t bbytes = p3 || !BF16 ? RG_ARR_BYTES : RG_SR * RG_GROW_BYTES;
+          mbar_arrive_expect_tx(&full[stage], RG_ARR_BYTES + bbytes + (p3 ? FT_COLS * 4 : 0));
+          const CUtensorMap* mp = a.maps + 3 * view;
+          const int x = static_cast<int>(c0), y = static_cast<int>(r0);
+          tma_load_2d_hint(st, mp, &full[stage], x, y, pol_first);
+          tma_load_2d_hint(st + RG_ARR_BYTES, mp + (p3 ? 2 : 1), &full[stage], x, y, pol_first);
+          if (p3)
+            bulk_load_hint(st + 2 * RG_ARR_BYTES, a.inv + static_cast<int64_t>(s) * FT_COLS, FT_COLS * 4,
+                           &full[stage], pol_first);
+        }
+        __syncwarp();
+        issued |= 1u << stage;
+        issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+        if (++stage == RG_STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      if (!ok) break;
+    }
+    if (ok) {
+      // tell the consumers that the queue is empty
+      int got = 1;
+      if (lane == 0) got = wait_bounded(&empty[stage], phase ^ 1u, abort_flag, a.err, FT_WAIT_LIMIT_NS) ? 1 : 0;
+      if (shfl0(got) && lane == 0) {
+        meta[stage].kind = RG_KIND_DONE;
+        mbar_arrive(&full[stage]);
+      }
+    } else if (lane == 0) {
+      // let every copy in flight land before the CTA's shared memory goes away
+      for (int k = 0; k < RG_STAGES; ++k)
+        if (issued & (1u << k)) wait_drain(&full[k], (issued_parity >> k) & 1u, 50000000ull);
+    }
+  } else {
+    // ---- consumers: warp w takes rows w * 4 .. w * 4 + 3 of every stage
+    const int w = warp - 1, ctid = threadIdx.x - 32;
+    const uint64_t pol_last = l2_policy_evict_last();
+    int stage = 0;
+    uint32_t phase = 0;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (;;) {
+      int got = 1;
+      if (lane == 0) got = wait_bounded(&full[stage], phase, abort_flag, a.err, FT_WAIT_LIMIT_NS) ? 1 : 0;
+      if (!shfl0(got)) break;
+      const RgMeta m = meta[stage];
+      if (m.kind == RG_KIND_DONE) break;
+      const View* v = a.views + m.view;
+      const bool p3 = m.kind == RG_KIND_P3;
+      const int64_t c = static_cast<int64_t>(m.s % a.spv) * FT_COLS + lane * 4;
+      const bool col_in = lane * 4 < m.ncols;  // ncols % 4 == 0
+      const uint8_t* st = stages + static_cast<size_t>(stage) * RG_STAGE_BYTES;
+      float4 k4 = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (p3 && col_in) {
+        const float sc = a.eta * v->shape_scale;
+        const float4 q = *reinterpret_cast<const float4*>(st + 2 * RG_ARR_BYTES + lane * 16);
+        k4 = make_float4(sc * q.x, sc * q.y, sc * q.z, sc * q.w);
+      }
+#pragma unroll
+      for (int rr = 0; rr < RG_ROWS_PER_WARP; ++rr) {
+        const int row = w * RG_ROWS_PER_WARP + rr;
+        if (row < m.nrows && col_in) {
+          const float4 mm = *reinterpret_cast<const float4*>(st + row * RG_ROW_BYTES + lane * 16);
+          const int64_t off = (m.row0 + row) * v->ld + c;
+          float4 o;
+          if (!p3) {
+            float4 g;
+            if (BF16) {
+              const uint2 u = *reinterpret_cast<const uint2*>(st + RG_ARR_BYTES + row * RG_GROW_BYTES + lane * 8);
+              g = make_float4(bf16_bits_to_float(u.x & 0xFFFFu), bf16_bits_to_float(u.x >> 16),
+                              bf16_bits_to_float(u.y & 0xFFFFu), bf16_bits_to_float(u.y >> 16));
+            } else {
+              g = *reinterpret_cast<const float4*>(st + RG_ARR_BYTES + row * RG_ROW_BYTES + lane * 16);
+            }
+            o.x = fmaf(a.beta, mm.x, g.x);
+            o.y = fmaf(a.beta, mm.y, g.y);
+            o.z = fmaf(a.beta, mm.z, g.z);
+            o.w = fmaf(a.beta, mm.w, g.w);
+            acc.x = fmaf(o.x, o.x, acc.x);
+            acc.y = fmaf(o.y, o.y, acc.y);
+            acc.z = fmaf(o.z, o.z, acc.z);
+            acc.w = fmaf(o.w, o.w, acc.w);
+            st_hint(v->M + off, o, pol_last);  // kept in L2 for the stripe's update
+          } else {
+            const float4 ww = *reinterpret_cast<const float4*>(st + RG_ARR_BYTES + row * RG_ROW_BYTES + lane * 16);
+            o.x = fmaf(ww.x, a.decay, -k4.x * mm.x);
+            o.y = fmaf(ww.y, a.decay, -k4.y * mm.y);
+            o.z = fmaf(ww.z, a.decay, -k4.z * mm.z);
+            o.w = fmaf(ww.w, a.decay, -k4.w * mm.w);
+            __stcs(reinterpret_cast<float4*>(v->W + off), o);
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[stage]);
+      if (++stage == RG_STAGES) {
+        stage = 0;
+        phase ^= 1u;
+      }
+      if (p3 || !m.last) continue;
+      // ---- the end of a phase-1 tile: its column partial sums (fixed order:
+      // rows within a warp, then warps), then the stripe protocol
+      red[w * FT_COLS + lane * 4 + 0] = acc.x;
+      red[w * FT_COLS + lane * 4 + 1] = acc.y;
+      red[w * FT_COLS + lane * 4 + 2] = acc.z;
+      red[w * FT_COLS + lane * 4 + 3] = acc.w;
+      acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      named_barrier_sync(1, RG_CONSUMERS);
+      if (ctid < FT_COLS) {
+        float sum = 0.f;
+#pragma unroll
+        for (int y = 0; y < RG_CONSUMER_WARPS; ++y) sum += red[y * FT_COLS + ctid];
+        a.partials[(static_cast<int64_t>(m.s) * a.R + m.rb) * FT_COLS + ctid] = sum;
+      }
+      // Release: the barrier orders every consumer's M and partial stores
+      // before thread 0's fence, and the fence before its count.
+      named_barrier_sync(1, RG_CONSUMERS);
+      if (ctid == 0) {
+        fence_acq_rel_gpu();
+        const int done = atomicAdd(a.counters + m.s, 1) == a.R - 1;
+        if (done) fence_acq_rel_gpu();  // acquire: the other tiles' partials
+        *flag_sh = done;
+      }
+      named_barrier_sync(1, RG_CONSUMERS);
+      if (*flag_sh) {
+        // the stripe's last phase-1 tile: inverse column norms, two threads per
+        // column over alternate row blocks, then their sum (a fixed order)
+        const int col = ctid % FT_COLS, q = ctid / FT_COLS;
+        const float* pp = a.partials + (static_cast<int64_t>(m.s) * a.R + q) * FT_COLS + col;
+        float sum = 0.f;
+#pragma unroll 8
+        for (int b = q; b < a.R; b += RG_CONSUMERS / FT_COLS, pp += (RG_CONSUMERS / FT_COLS) * FT_COLS)
+          sum += __ldcg(pp);
+        red[ctid] = sum;
+        named_barrier_sync(1, RG_CONSUMERS);
+        if (ctid < FT_COLS) {
+          float tot = 0.f;
+#pragma unroll
+          for (int k = 0; k < RG_CONSUMERS / FT_COLS; ++k) tot += red[k * FT_COLS + ctid];
+          a.inv[static_cast<int64_t>(m.s) * FT_COLS + ctid] = 1.f / fmaxf(sqrtf(tot), a.eps);
+        }
+        named_barrier_sync(1, RG_CONSUMERS);
+        if (ctid == 0 && m.s != a.withhold) st_release_gpu(a.ready + m.s, 1);
+      }
+      named_barrier_sync(1, RG_CONSUMERS);  // red and flag_sh are rewritten by the next tile end
+    }
+  }
+}
+
 template <int THREADS, int NV, bool BF16>
 cudaError_t launch_wide_t(const View* d_views, int count, int64_t rows, int64_t cols, bool vec_ok, StepScalars s,
                           cudaStream_t stream) {
@@ -611,10 +883,29 @@ TallFusedScratch tall_fused_scratch(int count, int64_t rows, int64_t cols) {
   return t;
 }
 
+bool tall_ring_ok(int64_t cols, bool grad_bf16) {
+  // TMA coordinates are 32-bit: rows below 2^31 are guaranteed by registration
+  return cols % 4 == 0 && (!grad_bf16 || cols % 8 == 0);
+}
+
+int tall_ring_box_cols() { return FT_COLS; }
+int tall_ring_box_rows() { return RG_SR; }
+
+cudaError_t rownorm_setup_attributes() {
+  cudaError_t e = cudaFuncSetAttribute(tall_ring_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(RG_SMEM_BYTES));
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(tall_ring_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              static_cast<int>(RG_SMEM_BYTES));
+}
+
 cudaError_t launch_rownorm_tall_fused(const View* d_views, int count, int64_t rows, int64_t cols, bool grad_bf16,
                                       StepScalars s, float* partials, float* inv, void* flags, int* err,
-                                      int num_sms, cudaStream_t stream, int withhold_stripe, uint64_t wait_ns) {
+                                      int num_sms, cudaStream_t stream, const CUtensorMap* ring_maps,
+                                      int withhold_stripe, uint64_t wait_ns) {
   if (count == 0 || rows == 0) return cudaSuccess;
+  const bool ring = ring_maps != nullptr;
+  if (ring && !tall_ring_ok(cols, grad_bf16)) return cudaErrorInvalidValue;
   const TallFusedScratch t = tall_fused_scratch(count, rows, cols);
   FusedTall a{};
   a.views = d_views;
@@ -626,7 +917,8 @@ cudaError_t launch_rownorm_tall_fused(const View* d_views, int count, int64_t ro
   if (!tall_fused_fits(count, rows, cols)) return cudaErrorInvalidValue;
   const int64_t total = 2 * static_cast<int64_t>(a.S) * a.R;
   a.total = static_cast<int>(total);
-  const int64_t grid = std::min<int64_t>(total, static_cast<int64_t>(std::max(1, num_sms)) * FT_CTAS_PER_SM);
+  const int64_t grid =
+      std::min<int64_t>(total, static_cast<int64_t>(std::max(1, num_sms)) * (ring ? 1 : FT_CTAS_PER_SM));
   // the lag covers the CTAs' window on the queue, so updates rarely wait
   a.D = static_cast<int>(std::min<int64_t>(a.S, FT_LAG_MUL * ((grid + a.R - 1) / a.R) + 1));
   a.beta = s.beta;
@@ -640,13 +932,20 @@ cudaError_t launch_rownorm_tall_fused(const View* d_views, int count, int64_t ro
   a.ready = a.counters + a.S;
   a.err = err;
   a.withhold = withhold_stripe;
+  a.maps = ring_maps;
   a.wait_ns = (wait_ns == 0 || wait_ns > FT_WAIT_LIMIT_NS) ? FT_WAIT_LIMIT_NS : wait_ns;
   cudaError_t e = cudaMemsetAsync(flags, 0, t.flag_bytes, stream);
   if (e != cudaSuccess) return e;
-  if (grad_bf16)
+  if (ring) {
+    if (grad_bf16)
+      tall_ring_kernel<true><<<static_cast<unsigned>(grid), RG_THREADS, RG_SMEM_BYTES, stream>>>(a);
+    else
+      tall_ring_kernel<false><<<static_cast<unsigned>(grid), RG_THREADS, RG_SMEM_BYTES, stream>>>(a);
+  } else if (grad_bf16) {
     tall_fused_kernel<true><<<static_cast<unsigned>(grid), FT_THREADS, 0, stream>>>(a);
-  else
+  } else {
     tall_fused_kernel<false><<<static_cast<unsigned>(grid), FT_THREADS, 0, stream>>>(a);
+  }
   return cudaGetLastError();
 }
 

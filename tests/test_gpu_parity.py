@@ -366,12 +366,15 @@ def test_argument_errors_on_device():
 
 @pytest.mark.parametrize("gdtype", [torch.float32, torch.bfloat16])
 def test_tall_rownorm_one_launch_ragged(gdtype):
-    """The one-launch tall RowNorm: stripes of 128 columns with a ragged last
-    stripe (388 = 3 x 128 + 4, 132 = 128 + 4), row tiles of 64 with ragged
-    last tiles (1000, 4100, 130 rows), several views in one launch; checked
-    against the oracle, and bit for bit against a second run (the column
-    sums are reduced in a fixed order whichever tile finishes a stripe)."""
-    shapes = [(1000, 388), (1000, 388), (4100, 132), (130, 64), (130, 64)]
+    """The one-launch tall RowNorm in both of its forms: stripes of 128
+    columns with a ragged last stripe (388 = 3 x 128 + 4 and 132 = 128 + 4
+    take the register form with bf16 gradients, the bulk-copy ring with fp32
+    ones; 392 = 3 x 128 + 8 and 136 = 128 + 8 the ring with either), row
+    tiles of 256 with ragged last tiles (1000, 4100, 130 rows), several views
+    in one launch; checked against the oracle, and bit for bit against a
+    second run (the column sums are reduced in a fixed order whichever tile
+    finishes a stripe)."""
+    shapes = [(1000, 388), (1000, 388), (4100, 132), (130, 64), (130, 64), (1000, 392), (1000, 392), (4100, 136)]
     gen = torch.Generator().manual_seed(13)
     Gh = [torch.randn(s, generator=gen).to(gdtype) for s in shapes]
     M0 = [torch.randn(s, generator=gen) * 0.5 for s in shapes]
