@@ -195,13 +195,13 @@ __device__ __forceinline__ uint32_t stage_off(int row, int chunk) {
 
 // ---- last round: D = X5 applied to W in the COMBINE epilogue -------------
 // (the parameter update of the refresh, W <- W (1 - lr wd) - eta s D, with D
-// the bf16 X5 as the separate update pass would read it). Wide views update
-// W in X's orientation, 8 rows x 128 contiguous bytes per instruction (D
-// from the staged box); tall views store X transposed, so lane = W column
-// and every instruction covers one W row segment of 128 bytes. A warp loads
-// the W values of its first two chunks while the accumulator is computed,
-// and those of chunk q + 2 right after using chunk q's, so each load has a
-// whole chunk of work to hide behind.
+// the bf16 X5 as the separate update pass would read it). Each 32 x 32 chunk
+// of X5 is staged in W's orientation (tall views transposed while staging),
+// so both orientations update W the same way: 8 W rows x 128 contiguous bytes
+// per instruction, each lane two float4 of one row. A warp loads the W values
+// of its first two chunks while the accumulator is computed, and those of
+// chunk q + 2 right after using chunk q's, so each load has a whole chunk of
+// work to hide behind.
 
 struct ApplyTarget {
   float* dst;    // W, or the D output of a view without W (orthogonaliser only)
@@ -209,7 +209,7 @@ struct ApplyTarget {
   float step;    // eta * shape_scale
   bool tall;
   bool upd;      // dst is W (update) rather than D's output
-  bool vec;      // 16-byte aligned rows (wide views)
+  bool vec;      // 16-byte aligned rows
 };
 
 __device__ __forceinline__ ApplyTarget apply_target(const GemmParams& p, const View* views, int mat) {
@@ -229,82 +229,70 @@ __device__ __forceinline__ float bf16_half(uint32_t word, int hi) {
   return __uint_as_float(hi ? (word & 0xFFFF0000u) : (word << 16));
 }
 
-// W values of the chunk (rows i0.., columns j0.. of X): wide views in the
-// 8-rows-per-instruction layout (value 8 * it + e: row i0 + 8 it + lane / 4,
-// column j0 + 8 (lane % 4) + e), tall views as W[j0 + k][i0 + lane] (value
-// k). Out-of-range values are 0 and never stored.
-__device__ __forceinline__ void apply_load(const ApplyTarget& t, int M, int N, int i0, int j0, int lane,
-                                           float (&wv)[32]) {
+// The chunk of X rows i0.., X columns j0.. in W's orientation: first row,
+// first column and extents of W (wide: the same; tall: transposed).
+struct ApplyBox {
+  int r0, c0, R, C;
+};
+
+__device__ __forceinline__ ApplyBox apply_box(const ApplyTarget& t, int M, int N, int i0, int j0) {
+  return t.tall ? ApplyBox{j0, i0, N, M} : ApplyBox{i0, j0, M, N};
+}
+
+// W values of the chunk, value 8 * it + e at W row b.r0 + 8 it + lane / 4,
+// column b.c0 + 8 (lane % 4) + e. Out-of-range values are 0 and never stored.
+__device__ __forceinline__ void apply_load(const ApplyTarget& t, const ApplyBox& b, int lane, float (&wv)[32]) {
   if (!t.upd) return;
-  if (!t.tall) {
-    const int j = j0 + 8 * (lane & 3);
+  const int j = b.c0 + 8 * (lane & 3);
 #pragma unroll
-    for (int it = 0; it < 4; ++it) {
-      const int i = i0 + 8 * it + (lane >> 2);
-      const float* row = t.dst + static_cast<int64_t>(i) * t.ld + j;
-      if (i < M && t.vec && j + 8 <= N) {
-        const float4 a = *reinterpret_cast<const float4*>(row);
-        const float4 b = *reinterpret_cast<const float4*>(row + 4);
-        wv[8 * it + 0] = a.x;
-        wv[8 * it + 1] = a.y;
-        wv[8 * it + 2] = a.z;
-        wv[8 * it + 3] = a.w;
-        wv[8 * it + 4] = b.x;
-        wv[8 * it + 5] = b.y;
-        wv[8 * it + 6] = b.z;
-        wv[8 * it + 7] = b.w;
-      } else {
+  for (int it = 0; it < 4; ++it) {
+    const int i = b.r0 + 8 * it + (lane >> 2);
+    const float* row = t.dst + static_cast<int64_t>(i) * t.ld + j;
+    if (i < b.R && t.vec && j + 8 <= b.C) {
+      const float4 a = *reinterpret_cast<const float4*>(row);
+      const float4 c = *reinterpret_cast<const float4*>(row + 4);
+      wv[8 * it + 0] = a.x;
+      wv[8 * it + 1] = a.y;
+      wv[8 * it + 2] = a.z;
+      wv[8 * it + 3] = a.w;
+      wv[8 * it + 4] = c.x;
+      wv[8 * it + 5] = c.y;
+      wv[8 * it + 6] = c.z;
+      wv[8 * it + 7] = c.w;
+    } else {
 #pragma unroll
-        for (int e = 0; e < 8; ++e) wv[8 * it + e] = (i < M && j + e < N) ? row[e] : 0.f;
-      }
+      for (int e = 0; e < 8; ++e) wv[8 * it + e] = (i < b.R && j + e < b.C) ? row[e] : 0.f;
     }
-  } else {
-    const int i = i0 + lane;
-#pragma unroll
-    for (int k = 0; k < 32; ++k)
-      wv[k] = (i < M && j0 + k < N) ? t.dst[static_cast<int64_t>(j0 + k) * t.ld + i] : 0.f;
   }
 }
 
-__device__ __forceinline__ void apply_store(const GemmParams& p, const ApplyTarget& t, int M, int N, int i0, int j0,
-                                            int lane, const float (&wv)[32], const uint8_t* box,
-                                            const uint32_t (&w)[16]) {
-  if (!t.tall) {
-    const int c4 = lane & 3;
-    const int j = j0 + 8 * c4;
+// W <- W decay - step D (or D itself for a view without W) over the chunk,
+// D from the staged box (row = W row - b.r0, column = W column - b.c0).
+__device__ __forceinline__ void apply_store(const GemmParams& p, const ApplyTarget& t, const ApplyBox& b, int lane,
+                                            const float (&wv)[32], const uint8_t* box) {
+  const int c4 = lane & 3;
+  const int j = b.c0 + 8 * c4;
 #pragma unroll
-    for (int it = 0; it < 4; ++it) {
-      const int rho = 8 * it + (lane >> 2);
-      const int i = i0 + rho;
-      if (i >= M) continue;
-      const uint4 u = *reinterpret_cast<const uint4*>(box + stage_off(rho, c4));
-      const uint32_t uw[4] = {u.x, u.y, u.z, u.w};
-      float o[8];
+  for (int it = 0; it < 4; ++it) {
+    const int rho = 8 * it + (lane >> 2);
+    const int i = b.r0 + rho;
+    if (i >= b.R) continue;
+    const uint4 u = *reinterpret_cast<const uint4*>(box + stage_off(rho, c4));
+    const uint32_t uw[4] = {u.x, u.y, u.z, u.w};
+    float o[8];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const float d = bf16_half(uw[e >> 1], e & 1);
-        o[e] = t.upd ? fmaf(wv[8 * it + e], p.decay, -t.step * d) : d;
-      }
-      float* row = t.dst + static_cast<int64_t>(i) * t.ld + j;
-      if (t.vec && j + 8 <= N) {
-        *reinterpret_cast<float4*>(row) = make_float4(o[0], o[1], o[2], o[3]);
-        *reinterpret_cast<float4*>(row + 4) = make_float4(o[4], o[5], o[6], o[7]);
-      } else {
-#pragma unroll
-        for (int e = 0; e < 8; ++e)
-          if (j + e < N) row[e] = o[e];
-      }
+    for (int e = 0; e < 8; ++e) {
+      const float d = bf16_half(uw[e >> 1], e & 1);
+      o[e] = t.upd ? fmaf(wv[8 * it + e], p.decay, -t.step * d) : d;
     }
-  } else {
-    const int i = i0 + lane;
-    if (i < M) {
+    float* row = t.dst + static_cast<int64_t>(i) * t.ld + j;
+    if (t.vec && j + 8 <= b.C) {
+      *reinterpret_cast<float4*>(row) = make_float4(o[0], o[1], o[2], o[3]);
+      *reinterpret_cast<float4*>(row + 4) = make_float4(o[4], o[5], o[6], o[7]);
+    } else {
 #pragma unroll
-      for (int k = 0; k < 32; ++k) {
-        if (j0 + k < N) {
-          const float d = bf16_half(w[k >> 1], k & 1);
-          t.dst[static_cast<int64_t>(j0 + k) * t.ld + i] = t.upd ? fmaf(wv[k], p.decay, -t.step * d) : d;
-        }
-      }
+      for (int e = 0; e < 8; ++e)
+        if (j + e < b.C) row[e] = o[e];
     }
   }
 }
@@ -393,14 +381,23 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const Segment
         uint8_t* bd = stage;
         if (lane == 0) bulk_wait_group_read<0>();
         __syncwarp();
+        if (!at.tall) {
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
-          *reinterpret_cast<uint4*>(bd + stage_off(lane, c)) =
-              make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+          for (int c = 0; c < 4; ++c)
+            *reinterpret_cast<uint4*>(bd + stage_off(lane, c)) =
+                make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+        } else {
+          // W's orientation: box row k = X column j0 + k, this lane's X row
+          // i0 + lane in box column `lane`
+#pragma unroll
+          for (int k = 0; k < 32; ++k)
+            *reinterpret_cast<uint16_t*>(bd + stage_off(k, lane >> 3) + (lane & 7) * 2) =
+                static_cast<uint16_t>(w[k >> 1] >> ((k & 1) * 16));
+        }
         float(&wcur)[32] = (qq & 1) ? wodd : weven;
         __syncwarp();
-        if (rows_in) apply_store(p, at, sg.M, sg.N, i0, j0, lane, wcur, bd, w);
-        if (qq + 2 < EPI_CHUNKS / 2) apply_load(at, sg.M, sg.N, i0, j0 + 64, lane, wcur);
+        if (rows_in) apply_store(p, at, apply_box(at, sg.M, sg.N, i0, j0), lane, wcur, bd);
+        if (qq + 2 < EPI_CHUNKS / 2) apply_load(at, apply_box(at, sg.M, sg.N, i0, j0 + 64), lane, wcur);
         __syncwarp();
         continue;
       }
@@ -586,8 +583,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       if (KIND == GEMM_COMBINE && sg.views != nullptr) {
         // the first two chunks' W values load while the accumulator is computed
         at = apply_target(p, sg.views, tc.mat);
-        apply_load(at, sg.M, sg.N, i - lane, tc.n0 + qbase * 32, lane, weven);
-        apply_load(at, sg.M, sg.N, i - lane, tc.n0 + qbase * 32 + 32, lane, wodd);
+        apply_load(at, apply_box(at, sg.M, sg.N, i - lane, tc.n0 + qbase * 32), lane, weven);
+        apply_load(at, apply_box(at, sg.M, sg.N, i - lane, tc.n0 + qbase * 32 + 32), lane, wodd);
       }
       const bool got = wait_bounded(&tfull_bar[acc], acc_phase, abort_flag, p.err, p.timeout_ns);
       if (!__all_sync(0xffffffffu, got)) break;

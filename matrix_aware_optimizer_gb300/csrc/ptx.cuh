@@ -119,13 +119,6 @@ __device__ __forceinline__ void tma_load_2d_hint(void* dst, const CUtensorMap* t
       : "memory");
 }
 
-// L2 prefetch of one 2-D box (no shared memory, no completion tracking).
-__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* tm, int x, int y) {
-  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(reinterpret_cast<uint64_t>(tm)),
-               "r"(x), "r"(y)
-               : "memory");
-}
-
 // Orders this thread's earlier generic-proxy view of global memory (e.g. data
 // another CTA published and this thread acquired) before its later
 // async-proxy accesses (bulk copies).

@@ -314,6 +314,11 @@ static_assert(FT_THREADS % FT_CX == 0 && FT_COLS <= FT_THREADS && FT_THREADS % F
               "stripe width and block shape");
 constexpr int FT_CTAS_PER_SM = 2;  // 64 registers per thread: two 512-thread CTAs per SM
 constexpr int FT_LAG_MUL = 1;      // D = FT_LAG_MUL * ceil(resident CTAs / tiles per stripe) + 1
+// The ring form keeps up to a tile and a half per CTA in flight and has half
+// as many CTAs: a lag of two windows (1.193 ms against 1.208 with one, 1.24
+// with three, on the 24 tall 8192 x 2048 matrices) leaves a stripe's last
+// momentum tile time to publish before its update tiles are claimed.
+constexpr int RG_LAG_MUL = 2;
 constexpr uint64_t FT_WAIT_LIMIT_NS = 2000000000ull;
 
 struct FusedTall {
@@ -920,7 +925,7 @@ cudaError_t launch_rownorm_tall_fused(const View* d_views, int count, int64_t ro
   const int64_t grid =
       std::min<int64_t>(total, static_cast<int64_t>(std::max(1, num_sms)) * (ring ? 1 : FT_CTAS_PER_SM));
   // the lag covers the CTAs' window on the queue, so updates rarely wait
-  a.D = static_cast<int>(std::min<int64_t>(a.S, FT_LAG_MUL * ((grid + a.R - 1) / a.R) + 1));
+  a.D = static_cast<int>(std::min<int64_t>(a.S, (ring ? RG_LAG_MUL : FT_LAG_MUL) * ((grid + a.R - 1) / a.R) + 1));
   a.beta = s.beta;
   a.decay = s.decay;
   a.eta = s.eta;
