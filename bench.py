@@ -521,7 +521,9 @@ def run_leg(name, args, dev, stream, world, local, peaks, wl=None):
         bsh = {sh: _block_shapes(sh[0], sh[1], ms.blocks) for sh in set(ms.shapes)}
         alg = sum(_ns_flops(*b) for sh in ms.shapes for b in bsh[sh]) * (ms.K - 1) * n
         blk = ns5_summary(fb, alg, n * (ms.K - 1), tf_sus, tf_burst) or {}
-        blk["ms_per_step_profiled"] = round(sum(fb[k]["ms"] for k in fb) / (n * (ms.K - 1)), 3)
+        nb = n * (ms.K - 1)
+        blk["ms_per_step_profiled"] = round(sum(fb[k]["ms"] for k in fb) / nb, 3)
+        blk["family_ms"] = {k: round(fb[k]["ms"] / nb, 3) for k in fb if fb[k]["records"]}
         out["block_step"] = blk
     else:
         out["rownorm"] = rownorm_summary(fam, hbm)

@@ -212,6 +212,36 @@ def test_edge_shapes_directions(gdtype):
         opt.close()
 
 
+@pytest.mark.parametrize("gdtype", [torch.float32, torch.bfloat16])
+def test_short_side_boundary_and_long_rows(gdtype):
+    """The fp32 rounds for short sides below 64 against the tensor-core
+    rounds from 64 up, at the boundary (63 and 64 in both orientations), and
+    on long matrices whose column tiles outnumber the 128 chunks a matrix is
+    split into (40 x 300000: 4688 tiles of 64 columns, ~37 per chunk; its
+    transpose; 1 x 1000000), one refresh step each against the oracle."""
+    shapes = [(63, 200), (200, 63), (64, 200), (200, 64), (40, 300000), (300000, 17), (1, 1000000)]
+    gen = torch.Generator().manual_seed(23)
+    Gh, Ws, Ms, Gs = [], [], [], []
+    for (m, n) in shapes:
+        G = (torch.randn(m, n, generator=gen) * torch.exp(torch.randn(m, 1, generator=gen) * 0.5)).to(gdtype)
+        Gh.append(G.double().numpy())
+        Gs.append(G.cuda())
+        Ws.append(torch.zeros(m, n, device="cuda"))
+        Ms.append(torch.zeros(m, n, device="cuda"))
+    opt = PeriodicRowMuon(Ws, Ms, Gs)
+    opt.workspace.fill_(0xFF)
+    assert opt.step(0, K=3, gamma=0.15, lr=0.1, wd=0.0, beta=0.9, eps=1e-8) == 1
+    opt.sync_status()
+    for i, (m, n) in enumerate(shapes):
+        assert N.prm_ns_route(m, n) == (2 if min(m, n) < 64 else N.prm_ns_route(m, n))
+        Dg = -host64(Ws[i]) / (0.1 * O.lr_shape_scale(m, n))
+        e = rel_frob(Dg, O.newton_schulz(Gh[i]))
+        assert e <= TOL_D_NS5, ((m, n), e)
+        if min(m, n) < 64:
+            assert e <= 1e-3, ((m, n), e)  # fp32 rounds: far inside the bf16 bound
+    opt.close()
+
+
 @pytest.mark.parametrize("ns_form", ["auto", "direct"])
 def test_more_shape_groups_than_one_launch_holds(ns_form):
     """Nine distinct shapes make nine NS5 groups (c = 2 r: all on the Gram
