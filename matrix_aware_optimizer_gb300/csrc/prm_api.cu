@@ -975,8 +975,16 @@ int prm_register_matrices(prm_ctx* c, const prm_matrix_desc* d, int count, int m
   if (muonbp_blocks > 0) build_ns_subplans(blocks, c->ws_limit, c->ns_form, c->ns_blocks);
   cudaError_t e = upload_sets(c->rn.wide);
   if (e == cudaSuccess) e = upload_sets(c->rn.tall);
-  for (auto& s : c->rn.tall)
-    if (e == cudaSuccess && s.ring) e = upload_ring_maps(s);
+  for (auto& s : c->rn.tall) {
+    if (e != cudaSuccess || !s.ring) continue;
+    // a view the tensor maps cannot describe keeps the register form
+    if (upload_ring_maps(s) != cudaSuccess) {
+      if (s.d_maps) cudaFree(s.d_maps);
+      s.d_maps = nullptr;
+      s.ring = false;
+      cudaGetLastError();
+    }
+  }
   for (auto* plans : {&c->ns_full, &c->ns_blocks})
     for (auto& p : *plans)
       for (auto& g : p.groups)

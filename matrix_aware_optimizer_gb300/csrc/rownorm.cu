@@ -638,7 +638,6 @@ __global__ void __launch_bounds__(RG_THREADS, 1) tall_ring_kernel(const FusedTal
       int s, rb;
       ft_decode(a, tile, p3, s, rb);
       const int view = s / a.spv;
-      const View* v = a.views + view;
       const int64_t c0 = static_cast<int64_t>(s % a.spv) * FT_COLS;
       const int ncols = static_cast<int>(a.cols - c0 < FT_COLS ? a.cols - c0 : FT_COLS);
       const int64_t row0 = static_cast<int64_t>(rb) * FT_TILE_ROWS;
