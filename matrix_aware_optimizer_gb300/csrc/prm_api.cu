@@ -19,11 +19,28 @@
 #include <tuple>
 #include <vector>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "internal.h"
 #include "prm.h"
 
 namespace prm {
 namespace {
+
+// NVTX range over the host-side enqueue of one kernel family (or one step),
+// named as the timer's families are, so that profilers can select launches
+// by range (e.g. ncu --nvtx --nvtx-include "prm_step/ns_combine/"). A no-op
+// unless a tool is attached.
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
+
+const char* const kFamilyNames[PRM_FAMILY_COUNT] = {"rownorm_wide", "rownorm_tall", "ns_prep",
+                                                    "ns_gram",      "ns_poly",      "ns_combine",
+                                                    "ns_sym",       "ns_small"};
 
 constexpr float NS_EPS = 1e-7f;  // added to ||M||_F before NS5 pre-normalisation
 constexpr float DEFAULT_COEFFS[3] = {3.4445f, -4.7750f, 2.0315f};
@@ -561,6 +578,7 @@ int run_ns_small(prm_ctx* c, NsGroup& g, char* b, bool update_momentum, float be
   const double r = static_cast<double>(g.r), cw = static_cast<double>(g.c);
   // executed flops per matrix: Gram pairs r (r + 1) c per round, P X 2 r^2 c, P 2 r^3
   const double flops = g.count * steps * (r * (r + 1) * cw + 2 * r * r * cw + 2 * r * r * r);
+  NvtxRange nr(kFamilyNames[PRM_FAMILY_NS_SMALL]);
   const size_t ev = c->prof.begin(stream);
   cudaError_t e;
   for (auto& s : g.sets) {
@@ -605,6 +623,7 @@ int run_ns(prm_ctx* c, NsPlan& plan, void* base, bool update_momentum, float bet
     for (auto& s : g.sets)
       prep_bytes += static_cast<double>(s.views.size()) * s.rows * s.cols *
                     (update_momentum ? (s.bf16 ? 12.0 : 14.0) : 6.0);
+    NvtxRange nr(kFamilyNames[PRM_FAMILY_NS_PREP]);
     const size_t ev = c->prof.begin(stream);
     // Views of one group may fill different numbers of partial slots (wide:
     // one per row; tall: one per 64x64 tile): unused slots must read as zero.
@@ -641,6 +660,7 @@ int run_ns(prm_ctx* c, NsPlan& plan, void* base, bool update_momentum, float bet
   auto run = [&](GemmKind kind, const std::vector<GemmSegSpec>& specs, int family, double flops,
                  const char* what) -> int {
     if (specs.empty()) return PRM_OK;
+    NvtxRange nr(kFamilyNames[family]);
     const size_t ev = c->prof.begin(stream);
     const cudaError_t err = launch_gemm(kind, specs.data(), static_cast<int>(specs.size()), epi, stream);
     if (err != cudaSuccess) return cuda_fail(c, err, what);
@@ -794,6 +814,7 @@ int run_rownorm(prm_ctx* c, void* base, StepScalars sc, cudaStream_t stream) {
   cudaError_t e;
   for (auto& s : c->rn.wide) {
     const double bytes = static_cast<double>(s.views.size()) * s.rows * s.cols * (s.bf16 ? 18.0 : 20.0);
+    NvtxRange nr(kFamilyNames[PRM_FAMILY_ROWNORM_WIDE]);
     const size_t ev = c->prof.begin(stream);
     e = launch_rownorm_wide(s.d_views, static_cast<int>(s.views.size()), s.rows, s.cols, s.vec_ok, s.bf16, sc,
                             stream);
@@ -802,6 +823,7 @@ int run_rownorm(prm_ctx* c, void* base, StepScalars sc, cudaStream_t stream) {
   }
   for (auto& s : c->rn.tall) {
     const double bytes = static_cast<double>(s.views.size()) * s.rows * s.cols * (s.bf16 ? 18.0 : 20.0);
+    NvtxRange nr(kFamilyNames[PRM_FAMILY_ROWNORM_TALL]);
     const size_t ev = c->prof.begin(stream);
     float* partials = reinterpret_cast<float*>(b + s.off_partials);
     float* inv = reinterpret_cast<float*>(b + s.off_inv);
@@ -1081,6 +1103,7 @@ int prm_step(prm_ctx* c, int64_t t, int K, float gamma, float lr, float wd, floa
   DeviceGuard guard(c->device);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const bool refresh = (t % K) == 0;
+  NvtxRange nr("prm_step");
   StepScalars sc;
   sc.beta = beta;
   sc.decay = 1.f - lr * wd;
