@@ -43,7 +43,6 @@ os.environ.setdefault("CUDA_DEVICE_MAX_CONNECTIONS", "32")
 
 METRIC = "ms per K=3 PR-Muon cycle (1.3B/15B DiT shapes); NS5 TFLOP/s; RowNorm GB/s"
 UNIT = "ms/cycle"
-BASELINE_VALUE = None  # the pages publish no single-GPU number for this metric
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 GEMM_FAMILIES = ("ns_gram", "ns_poly", "ns_combine", "ns_sym")
 WORKLOADS = ["dit_1p3b", "dit_15b", "dit_1p3b_muonbp", "dit_block_d2048", "dit_1p3b_4blk",
