@@ -45,12 +45,20 @@ def _stale(target: str, deps) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
+# Sources whose kernels never run in an optimizer step's launch list (the
+# non-matrix AdamW and the allocation-free tall RowNorm): a stored profile of
+# the step does not depend on them.
+_NOT_IN_STEP = ("adamw.cu", "rownorm_noalloc.cu")
+
+
 def source_digest() -> str:
-    """sha256 over the library's sources and headers (identifies the kernels
-    that a stored profile was taken on)."""
+    """sha256 over the sources and headers of the optimizer step (identifies
+    the kernels and launch plan that a stored profile was taken on)."""
     import hashlib
     h = hashlib.sha256()
     for path in _sources() + _headers():
+        if os.path.basename(path) in _NOT_IN_STEP:
+            continue
         h.update(os.path.basename(path).encode())
         with open(path, "rb") as f:
             h.update(f.read())

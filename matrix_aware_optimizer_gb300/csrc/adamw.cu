@@ -33,29 +33,52 @@ __device__ __forceinline__ void adam_elem(float& p, float& m, float& v, float g,
 }
 
 template <bool BF16>
+__device__ __forceinline__ float4 load_grad4(const void* g, int64_t k) {
+  if constexpr (BF16) {
+    const uint2 u = __ldcs(reinterpret_cast<const uint2*>(g) + k);
+    return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xFFFF0000u), __uint_as_float(u.y << 16),
+                       __uint_as_float(u.y & 0xFFFF0000u));
+  } else {
+    return __ldcs(reinterpret_cast<const float4*>(g) + k);
+  }
+}
+
+// Each thread takes ADAM_UNROLL groups of four elements a grid stride apart
+// per iteration, issuing all their loads before any arithmetic, so that more
+// bytes are in flight per thread.
+constexpr int ADAM_UNROLL = 4;
+
+template <bool BF16>
 __global__ void __launch_bounds__(256) adamw_vec_kernel(float* __restrict__ p, float* __restrict__ m,
                                                         float* __restrict__ v, const void* __restrict__ g,
                                                         int64_t n4, AdamScalars s) {
-  for (int64_t k = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; k < n4;
-       k += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    float4 pp = __ldcs(reinterpret_cast<const float4*>(p) + k);
-    float4 mm = __ldcs(reinterpret_cast<const float4*>(m) + k);
-    float4 vv = __ldcs(reinterpret_cast<const float4*>(v) + k);
-    float4 gg;
-    if constexpr (BF16) {
-      const uint2 u = __ldcs(reinterpret_cast<const uint2*>(g) + k);
-      gg = make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xFFFF0000u), __uint_as_float(u.y << 16),
-                       __uint_as_float(u.y & 0xFFFF0000u));
-    } else {
-      gg = __ldcs(reinterpret_cast<const float4*>(g) + k);
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t k0 = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; k0 < n4;
+       k0 += ADAM_UNROLL * stride) {
+    float4 pp[ADAM_UNROLL], mm[ADAM_UNROLL], vv[ADAM_UNROLL], gg[ADAM_UNROLL];
+#pragma unroll
+    for (int u = 0; u < ADAM_UNROLL; ++u) {
+      const int64_t k = k0 + u * stride;
+      if (k < n4) {
+        pp[u] = __ldcs(reinterpret_cast<const float4*>(p) + k);
+        mm[u] = __ldcs(reinterpret_cast<const float4*>(m) + k);
+        vv[u] = __ldcs(reinterpret_cast<const float4*>(v) + k);
+        gg[u] = load_grad4<BF16>(g, k);
+      }
     }
-    adam_elem(pp.x, mm.x, vv.x, gg.x, s);
-    adam_elem(pp.y, mm.y, vv.y, gg.y, s);
-    adam_elem(pp.z, mm.z, vv.z, gg.z, s);
-    adam_elem(pp.w, mm.w, vv.w, gg.w, s);
-    __stcs(reinterpret_cast<float4*>(p) + k, pp);
-    __stcs(reinterpret_cast<float4*>(m) + k, mm);
-    __stcs(reinterpret_cast<float4*>(v) + k, vv);
+#pragma unroll
+    for (int u = 0; u < ADAM_UNROLL; ++u) {
+      const int64_t k = k0 + u * stride;
+      if (k < n4) {
+        adam_elem(pp[u].x, mm[u].x, vv[u].x, gg[u].x, s);
+        adam_elem(pp[u].y, mm[u].y, vv[u].y, gg[u].y, s);
+        adam_elem(pp[u].z, mm[u].z, vv[u].z, gg[u].z, s);
+        adam_elem(pp[u].w, mm[u].w, vv[u].w, gg[u].w, s);
+        __stcs(reinterpret_cast<float4*>(p) + k, pp[u]);
+        __stcs(reinterpret_cast<float4*>(m) + k, mm[u]);
+        __stcs(reinterpret_cast<float4*>(v) + k, vv[u]);
+      }
+    }
   }
 }
 
