@@ -314,11 +314,11 @@ static_assert(FT_THREADS % FT_CX == 0 && FT_COLS <= FT_THREADS && FT_THREADS % F
               "stripe width and block shape");
 constexpr int FT_CTAS_PER_SM = 2;  // 64 registers per thread: two 512-thread CTAs per SM
 constexpr int FT_LAG_MUL = 1;      // D = FT_LAG_MUL * ceil(resident CTAs / tiles per stripe) + 1
-// The ring form keeps up to a tile and a half per CTA in flight and has half
-// as many CTAs: a lag of two windows (1.193 ms against 1.208 with one, 1.24
-// with three, on the 24 tall 8192 x 2048 matrices) leaves a stripe's last
-// momentum tile time to publish before its update tiles are claimed.
-constexpr int RG_LAG_MUL = 2;
+// The ring form runs two CTAs per SM with three stages each, and a lag of
+// one window of them (on the 24 tall 8192 x 2048 matrices: 1.172 ms against
+// 1.26 with a lag of two, and 1.21 with one CTA of six stages per SM).
+constexpr int RG_LAG_MUL = 1;
+constexpr int RG_CTAS_PER_SM = 2;
 constexpr uint64_t FT_WAIT_LIMIT_NS = 2000000000ull;
 
 struct FusedTall {
@@ -563,20 +563,21 @@ __global__ void __launch_bounds__(FT_THREADS, FT_CTAS_PER_SM) tall_fused_kernel(
 
 // ------------------------------------------ tall columns, fused, TMA ring
 // The same queue of phase-1 / phase-3 tiles and the same stripe protocol as
-// tall_fused_kernel, with the loads moved off the compute warps: one CTA per
-// SM, a producer warp that claims tiles and streams each tile into a ring of
-// shared-memory stages with TMA tensor loads (a 128-column x 32-row box of M
-// and one of G or W per stage, six stages: up to ~190 KB of loads in flight
-// per SM), and eight consumer warps that update M or W from the staged rows
-// and store the results. A phase-3 tile's loads of M are issued only after
+// tall_fused_kernel, with the loads moved off the compute warps: two CTAs
+// per SM, each with a producer warp that claims tiles and streams each tile
+// into a ring of shared-memory stages with TMA tensor loads (a 128-column x
+// 32-row box of M and one of G or W per stage, three stages per CTA: up to
+// ~190 KB of loads in flight per SM from two independent producers), and
+// eight consumer warps that update M or W from the staged rows and store the
+// results. A phase-3 tile's loads of M are issued only after
 // its stripe's inverse norms are published (acquire, then a proxy fence, so
 // that the tensor loads see the momentum other CTAs stored). The maps need
 // 16-byte row pitches: cols % 4 == 0, and cols % 8 == 0 with bf16 gradients.
 constexpr int RG_CONSUMER_WARPS = 8;
 constexpr int RG_CONSUMERS = 32 * RG_CONSUMER_WARPS;
 constexpr int RG_THREADS = 32 + RG_CONSUMERS;
-constexpr int RG_SR = 32;                              // rows per stage (one per producer lane)
-constexpr int RG_STAGES = 6;
+constexpr int RG_SR = 32;                              // rows per stage
+constexpr int RG_STAGES = 3;
 constexpr int RG_ROWS_PER_WARP = RG_SR / RG_CONSUMER_WARPS;  // 4
 constexpr uint32_t RG_ROW_BYTES = FT_COLS * 4;         // 512 (fp32 box rows)
 constexpr uint32_t RG_GROW_BYTES = FT_COLS * 2;        // 256 (bf16 box rows)
@@ -601,7 +602,7 @@ static_assert(RG_SMEM_BYTES <= 232448, "ring above the 227 KB per-block limit");
 __device__ __forceinline__ int shfl0(int v) { return __shfl_sync(0xffffffffu, v, 0); }
 
 template <bool BF16>
-__global__ void __launch_bounds__(RG_THREADS, 1) tall_ring_kernel(const FusedTall a) {
+__global__ void __launch_bounds__(RG_THREADS, RG_CTAS_PER_SM) tall_ring_kernel(const FusedTall a) {
   extern __shared__ uint8_t rg_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(rg_raw) + 127) & ~uintptr_t(127));
   uint8_t* stages = base;
@@ -922,7 +923,7 @@ cudaError_t launch_rownorm_tall_fused(const View* d_views, int count, int64_t ro
   const int64_t total = 2 * static_cast<int64_t>(a.S) * a.R;
   a.total = static_cast<int>(total);
   const int64_t grid =
-      std::min<int64_t>(total, static_cast<int64_t>(std::max(1, num_sms)) * (ring ? 1 : FT_CTAS_PER_SM));
+      std::min<int64_t>(total, static_cast<int64_t>(std::max(1, num_sms)) * (ring ? RG_CTAS_PER_SM : FT_CTAS_PER_SM));
   // the lag covers the CTAs' window on the queue, so updates rarely wait
   a.D = static_cast<int>(std::min<int64_t>(a.S, (ring ? RG_LAG_MUL : FT_LAG_MUL) * ((grid + a.R - 1) / a.R) + 1));
   a.beta = s.beta;

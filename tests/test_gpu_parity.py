@@ -341,12 +341,13 @@ def test_standalone_newton_schulz():
     (1.5, -0.5, 0.0),            # cubic: c = 0, the polynomial stage is skipped
     (1.875, -0.6, -0.275),       # c < 0: the square enters with a minus sign
 ])
-@pytest.mark.parametrize("shape", [(2, 320, 400), (2, 256, 600)])
+@pytest.mark.parametrize("shape", [(2, 320, 400), (2, 256, 600), (2, 40, 300)])
 def test_newton_schulz_coefficient_signs(coeffs, shape):
     """The library forms a I + b A + c A A as a completed square whose form
     depends on the sign of c; every branch must match the plain iteration,
-    on the direct route (320 x 400) and on the Gram route (256 x 600, which
-    falls back to the direct rounds for c = 0)."""
+    on the direct route (320 x 400), on the Gram route (256 x 600, which
+    falls back to the direct rounds for c = 0) and on the fp32 rounds of a
+    short side below 64 (40 x 300, the plain polynomial)."""
     gen = torch.Generator().manual_seed(5)
     X = torch.randn(*shape, generator=gen)
     D = newton_schulz(X.cuda(), ns_coeffs=coeffs).cpu().double().numpy()
@@ -441,9 +442,9 @@ def test_newton_schulz_round_counts(steps):
     """Other round counts than five: the Gram route splits them into legs of
     at most three (1: one direct-style round; 4: three + one; 7: three +
     three + one, the third leg back in the first X buffer); a 320 x 400
-    batch member runs the direct rounds."""
+    batch member runs the direct rounds, a 33 x 50 one the fp32 rounds."""
     gen = torch.Generator().manual_seed(100 + steps)
-    for shape in [(2, 192, 640), (1, 320, 400)]:
+    for shape in [(2, 192, 640), (1, 320, 400), (2, 33, 50)]:
         X = torch.randn(*shape, generator=gen)
         D = newton_schulz(X.cuda(), steps=steps).cpu().double().numpy()
         for i in range(shape[0]):
