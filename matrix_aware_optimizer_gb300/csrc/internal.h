@@ -60,8 +60,9 @@ struct TallFusedScratch {
 };
 bool tall_fused_fits(int count, int64_t rows, int64_t cols);  // queue and offsets within 32-bit limits
 TallFusedScratch tall_fused_scratch(int count, int64_t rows, int64_t cols);
-// ring: the TMA form (tall_ring_kernel, one CTA per SM with a producer warp
-// and a ring of shared-memory stages); needs tall_ring_ok.
+// ring: the TMA form (tall_ring_kernel, two CTAs per SM, each with a
+// producer warp feeding a ring of shared-memory stages, eight consumer warps
+// and a publisher warp for the stripe bookkeeping); needs tall_ring_ok.
 bool tall_ring_ok(int64_t cols, bool grad_bf16);
 cudaError_t rownorm_setup_attributes();
 // Ring form: tensor maps of each view's M, G and W (3 per view, device
