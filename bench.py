@@ -847,17 +847,20 @@ def run_e2e(args, wl, opt, ms, stream, dev, world, ws_limit):
 
 def load_traffic():
     """Per-launch DRAM bytes of each kernel family of the 1.3B set from the
-    committed ncu summary, if it was taken on the current kernel sources."""
+    committed ncu summary, for the families whose kernels (and the engine
+    and headers) are still the code the counters were taken on."""
     path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     try:
         with open(path) as f:
             d = json.load(f)
     except Exception:
         return {}
-    from matrix_aware_optimizer_gb300.build import source_digest
-    if d.get("source_digest") != source_digest():
-        return {}
-    return {k: v.get("dram_bytes_per_launch") for k, v in d.get("kernels", {}).items()}
+    from matrix_aware_optimizer_gb300.build import FAMILY_SOURCES, source_digest
+    out = {}
+    for k, v in d.get("kernels", {}).items():
+        if k in FAMILY_SOURCES and v.get("source_digest") == source_digest(k):
+            out[k] = v.get("dram_bytes_per_launch")
+    return out
 
 
 def main():

@@ -45,23 +45,44 @@ def _stale(target: str, deps) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-# Sources whose kernels never run in an optimizer step's launch list (the
-# non-matrix AdamW and the allocation-free tall RowNorm): a stored profile of
-# the step does not depend on them.
-_NOT_IN_STEP = ("adamw.cu", "rownorm_noalloc.cu")
+# The source of each kernel family's kernels; every family also depends on
+# the engine that plans and launches it (prm_api.cu) and on the headers.
+FAMILY_SOURCES = {
+    "ns_prep": ("refresh.cu",),
+    "ns_gram": ("ns5_gemm.cu",),
+    "ns_poly": ("ns5_gemm.cu",),
+    "ns_sym": ("ns5_gemm.cu",),
+    "ns_combine": ("ns5_gemm.cu",),
+    "ns_small": ("ns_small.cu",),
+    "rownorm_wide": ("rownorm.cu",),
+    "rownorm_tall": ("rownorm.cu",),
+}
+_ENGINE = "prm_api.cu"
 
 
-def source_digest() -> str:
-    """sha256 over the sources and headers of the optimizer step (identifies
-    the kernels and launch plan that a stored profile was taken on)."""
+def _code_only(text: bytes) -> bytes:
+    """The source without // and /* */ comments and blank-line differences,
+    so that editing a comment leaves a digest unchanged. (The sources hold
+    no comment markers inside string literals.)"""
+    import re
+    t = text.decode("utf-8")
+    t = re.sub(r"/\*.*?\*/", "", t, flags=re.S)
+    t = re.sub(r"//[^\n]*", "", t)
+    lines = [ln.rstrip() for ln in t.splitlines()]
+    return "\n".join(ln for ln in lines if ln).encode()
+
+
+def source_digest(family: str) -> str:
+    """sha256 over the code (comments stripped) of one kernel family's
+    source, the engine and the headers: identifies the kernels and launch
+    plan that a stored profile of that family was taken on."""
     import hashlib
+    names = set(FAMILY_SOURCES[family]) | {_ENGINE}
     h = hashlib.sha256()
-    for path in _sources() + _headers():
-        if os.path.basename(path) in _NOT_IN_STEP:
-            continue
+    for path in [p for p in _sources() if os.path.basename(p) in names] + _headers():
         h.update(os.path.basename(path).encode())
         with open(path, "rb") as f:
-            h.update(f.read())
+            h.update(_code_only(f.read()))
     return h.hexdigest()[:16]
 
 

@@ -83,3 +83,18 @@ def test_oracle_sample_is_bounded_and_labelled():
     v, sample, secs = bench.oracle_cycle_sample(synth.MATRIX_SETS["tiny"])
     assert v > 0 and secs < 5.0
     assert sample.startswith("timed:") and "64x64" in sample
+
+
+def test_traffic_digest_follows_code_not_comments():
+    """A stored DRAM figure stays valid across comment edits of its kernel's
+    source and is dropped when the code changes."""
+    from matrix_aware_optimizer_gb300 import build
+    a = b"int f(int x) {  // doubles x\n  return 2 * x;  /* twice */\n}\n"
+    b = b"// a new header line\nint f(int x) {  // twice x\n\n  return 2 * x;\n}\n"
+    c = b"int f(int x) {  // doubles x\n  return 3 * x;\n}\n"
+    assert build._code_only(a) == build._code_only(b)
+    assert build._code_only(a) != build._code_only(c)
+    digests = {f: build.source_digest(f) for f in build.FAMILY_SOURCES}
+    assert len(set(digests.values())) == len(set(build.FAMILY_SOURCES.values()))  # one per kernel source
+    traffic = bench.load_traffic()
+    assert set(traffic) <= set(build.FAMILY_SOURCES)
