@@ -291,7 +291,7 @@ __global__ void __launch_bounds__(TALL_TX* TALL_TY) tall_update_kernel(const Vie
 //   P3(S-D) .. P3(S-1)          (Pk(s): the tiles of stripe s)
 // so a stripe's momentum is read back by its update D stripes after it was
 // written, from L2 rather than HBM: D just covers the resident CTAs' window
-// on the queue (1.3B-shaped set: 11 stripes of 4 MB), and the momentum is
+// on the queue (1.3B-shaped set: 10 - 11 stripes of 4 MB), and the momentum is
 // stored with an evict-last L2 policy while G and W stream through
 // evict-first. The phase-1 tile that completes a stripe (the last one to
 // count itself on the stripe's counter) sums the stripe's partials in a
@@ -315,9 +315,14 @@ static_assert(FT_THREADS % FT_CX == 0 && FT_COLS <= FT_THREADS && FT_THREADS % F
 constexpr int FT_CTAS_PER_SM = 2;  // 64 registers per thread: two 512-thread CTAs per SM
 constexpr int FT_LAG_MUL = 1;      // D = FT_LAG_MUL * ceil(resident CTAs / tiles per stripe) + 1
 // The ring form runs two CTAs per SM with three stages each, and a lag of
-// one window of them (on the 24 tall 8192 x 2048 matrices: 1.172 ms against
-// 1.26 with a lag of two, and 1.21 with one CTA of six stages per SM).
+// exactly one window of them, D = ceil(resident CTAs / tiles per stripe): a
+// longer lag lets fewer update tiles wait for their stripe's norms but keeps
+// more momentum live in L2 than it holds (24 tall 8192 x 2048 matrices:
+// 1.117 against 1.120 ms with one stripe more, and each further stripe
+// slower again; 8 of 20480 x 5120: 2.486 against 2.525 ms with one more and
+// 2.580 with two more).
 constexpr int RG_LAG_MUL = 1;
+constexpr int RG_LAG_ADD = 0;  // the register form adds one stripe
 constexpr int RG_CTAS_PER_SM = 2;
 constexpr uint64_t FT_WAIT_LIMIT_NS = 2000000000ull;
 
@@ -1020,7 +1025,8 @@ cudaError_t launch_rownorm_tall_fused(const View* d_views, int count, int64_t ro
   const int64_t grid =
       std::min<int64_t>(total, static_cast<int64_t>(std::max(1, num_sms)) * (ring ? RG_CTAS_PER_SM : FT_CTAS_PER_SM));
   // the lag covers the CTAs' window on the queue, so updates rarely wait
-  a.D = static_cast<int>(std::min<int64_t>(a.S, (ring ? RG_LAG_MUL : FT_LAG_MUL) * ((grid + a.R - 1) / a.R) + 1));
+  a.D = static_cast<int>(std::min<int64_t>(
+      a.S, (ring ? RG_LAG_MUL : FT_LAG_MUL) * ((grid + a.R - 1) / a.R) + (ring ? RG_LAG_ADD : 1)));
   a.beta = s.beta;
   a.decay = s.decay;
   a.eta = s.eta;
