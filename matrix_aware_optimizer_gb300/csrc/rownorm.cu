@@ -573,13 +573,12 @@ __global__ void __launch_bounds__(FT_THREADS, FT_CTAS_PER_SM) tall_fused_kernel(
 // compute warps. Two CTAs per SM, each with
 //   warp 0     : producer -- claims tiles one at a time, waits for a phase-3
 //                tile's stripe norms, and streams each tile into a ring of
-//                shared-memory
-//                stages with TMA tensor loads (a 128-column x 32-row box of M
-//                and one of G or W per stage, three stages per CTA: up to
-//                ~200 KB of loads in flight per SM from two independent
-//                producers; claiming the next tile ahead was slower: a
-//                claimed phase-1 tile then waits behind its CTA's phase-3
-//                wait, and the stripe it belongs to with it);
+//                shared-memory stages with TMA tensor loads (a 128-column x
+//                32-row box of M and one of G or W per stage, three stages
+//                per CTA: up to ~200 KB of loads in flight per SM from two
+//                independent producers). Claiming the next tile ahead was
+//                slower: a claimed phase-1 tile then waits behind its CTA's
+//                phase-3 wait, and the stripe it belongs to with it;
 //   warps 1..8 : consumers -- update M or W from the staged rows and store
 //                the results; at the end of a phase-1 tile they leave their
 //                column partial sums in one of two shared-memory slots and

@@ -242,6 +242,19 @@ def test_short_side_boundary_and_long_rows(gdtype):
     opt.close()
 
 
+@pytest.mark.parametrize("gdtype", [synth.GRAD_FP32, synth.GRAD_BF16])
+def test_wide_rows_past_the_256_thread_forms(gdtype):
+    """Wide rows longer than the 256-thread forms hold (12288 floats) take
+    the 512-thread ones: 12292 (the first width past), 13000 and 20480 (ten
+    float4 per thread, partly or fully used), 24576 (fourteen), beside
+    12288 (the last 256-thread width) and 13002, a width that is not a
+    multiple of 4 (the scalar form), over a refresh and two RowNorm steps
+    against the oracle."""
+    shapes = [(24, 13000), (16, 20480), (8, 24576), (6, 12292), (5, 12288), (7, 13002)]
+    ms = make_set(shapes, gdtype, seed=29)
+    _run_teacher_forced(ms, steps=[0, 1, 2])
+
+
 @pytest.mark.parametrize("ns_form", ["auto", "direct"])
 def test_more_shape_groups_than_one_launch_holds(ns_form):
     """Nine distinct shapes make nine NS5 groups (c = 2 r: all on the Gram
