@@ -38,14 +38,16 @@ def _hp(ms, K=None):
     return dict(K=ms.K if K is None else K, gamma=ms.gamma, lr=ms.lr, wd=ms.wd, beta=ms.beta, eps=ms.eps)
 
 
-def _run_teacher_forced(ms, steps, check_idx=None, mode="prmuon", blocks=0, ns_form="auto", K=None):
+def _run_teacher_forced(ms, steps, check_idx=None, mode="prmuon", blocks=0, ns_form="auto", K=None, hp=None,
+                        coeffs=None):
     shapes = ms.shapes
     Ws, Ms = synth.make_state(ms, device="cuda")
     gdt = torch.bfloat16 if ms.grad_dtype == synth.GRAD_BF16 else torch.float32
     grads = [torch.empty(s, device="cuda", dtype=gdt) for s in shapes]
     opt = PeriodicRowMuon(Ws, Ms, grads, muonbp_blocks=blocks, ns_form=ns_form)
     opt.workspace.fill_(0xFF)  # NaN bit patterns: any read of unwritten scratch shows up
-    hp = _hp(ms, K)
+    hp = _hp(ms, K) if hp is None else hp
+    okw = {} if coeffs is None else {"coeffs": coeffs}
     idx = range(len(shapes)) if check_idx is None else check_idx
     report = []
     for t in steps:
@@ -53,7 +55,7 @@ def _run_teacher_forced(ms, steps, check_idx=None, mode="prmuon", blocks=0, ns_f
             synth.make_grad(shapes[i], ms.seed, t, i, ms.grad_std, ms.grad_dtype, ms.row_sigma, device="cuda", out=g)
         torch.cuda.synchronize()
         prev = {i: (host64(Ws[i]), host64(Ms[i]), host64(grads[i])) for i in idx}
-        branch = opt.step(t, mode=mode, **hp)
+        branch = opt.step(t, mode=mode, ns_coeffs=coeffs, **hp)
         opt.sync_status()
         assert branch == O.refresh_indicator(t, hp["K"])
         for i in idx:
@@ -61,13 +63,13 @@ def _run_teacher_forced(ms, steps, check_idx=None, mode="prmuon", blocks=0, ns_f
             m, n = shapes[i]
             s = O.lr_shape_scale(m, n)
             if mode == "prmuon":
-                W1, M1, D1, rho = O.prmuon_step(W0, M0, G0, t, **hp)
+                W1, M1, D1, rho = O.prmuon_step(W0, M0, G0, t, **hp, **okw)
             else:
-                W1, M1, D1, rho = O.muonbp_step(W0, M0, G0, t, P=blocks, **hp)
+                W1, M1, D1, rho = O.muonbp_step(W0, M0, G0, t, P=blocks, **hp, **okw)
             assert rho == branch
             Wg, Mg = host64(Ws[i]), host64(Ms[i])
-            eta = ms.lr if rho else ms.lr * ms.gamma
-            Dg = direction_from_update(W0, Wg, ms.lr, ms.wd, eta, s)
+            eta = hp["lr"] if rho else hp["lr"] * hp["gamma"]
+            Dg = direction_from_update(W0, Wg, hp["lr"], hp["wd"], eta, s)
             eM, eW, eD = rel_frob(Mg, M1), rel_frob(Wg, W1), rel_frob(Dg, D1)
             report.append((t, i, rho, eM, eW, eD))
             assert eM <= TOL_M, (t, i, eM)
@@ -253,6 +255,30 @@ def test_wide_rows_past_the_256_thread_forms(gdtype):
     shapes = [(24, 13000), (16, 20480), (8, 24576), (6, 12292), (5, 12288), (7, 13002)]
     ms = make_set(shapes, gdtype, seed=29)
     _run_teacher_forced(ms, steps=[0, 1, 2])
+
+
+HP_CASES = [
+    # K, gamma, lr, wd, beta, eps, Newton-Schulz (a, b, c), mode, blocks
+    (2, 0.3, 0.05, 0.05, 0.0, 1e-8, (1.875, -0.6, -0.275), "prmuon", 0),       # no momentum history; c < 0
+    (5, 0.1, 0.01, 0.0, 0.99, 1e-6, (1.5, -0.5, 0.0), "prmuon", 0),            # long period; c = 0
+    (2, 1.25, 0.016, 0.02, 0.9, 1e-8, (1.875, -0.6, -0.275), "muonbp", 4),
+    (4, 0.5, 0.02, 0.01, 0.5, 1e-8, (3.4445, -4.7750, 2.0315), "muonbp", 3),
+]
+
+
+@pytest.mark.parametrize("K,gamma,lr,wd,beta,eps,coeffs,mode,blocks", HP_CASES)
+def test_step_hyperparameters_and_ns_coefficients(K, gamma, lr, wd, beta, eps, coeffs, mode, blocks):
+    """prm_step with hyper-parameters other than the defaults and with
+    Newton-Schulz coefficients whose c is negative or zero (the completed
+    square's other sign; POLY skipped) as well as the default, teacher-forced
+    against the oracle over two refreshes and the steps between, on shapes
+    that take every NS5 path: a short side below 64 (fp32 rounds), the direct
+    rounds (square), the Gram route (c >= 2 r; direct rounds when c = 0), a
+    tall matrix and a ragged one."""
+    shapes = [(40, 300), (256, 256), (128, 512), (512, 128), (96, 80)]
+    ms = make_set(shapes, synth.GRAD_BF16, seed=31)
+    hp = dict(K=K, gamma=gamma, lr=lr, wd=wd, beta=beta, eps=eps)
+    _run_teacher_forced(ms, steps=range(K + 1), mode=mode, blocks=blocks, hp=hp, coeffs=coeffs)
 
 
 @pytest.mark.parametrize("ns_form", ["auto", "direct"])
