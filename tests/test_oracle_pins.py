@@ -122,18 +122,22 @@ def test_ns5_diagonal_worked_example():
     np.testing.assert_allclose(O.newton_schulz(X, gd["coeffs"]), np.array(gd["expected_D"]), atol=1e-6)
 
 
+@pytest.mark.parametrize("coeffs", [None, (1.5, -0.5, 0.0), (1.875, -0.6, -0.275)])
 @pytest.mark.parametrize("shape", [(3, 8), (8, 3), (6, 6), (1, 5), (5, 1), (12, 40)])
-def test_ns5_matches_svd_closed_form(shape):
+def test_ns5_matches_svd_closed_form(shape, coeffs):
     """NS commutes with the SVD: NS5(X) = U diag(p^5(sigma / ||X||_F)) V^T with
-    p(s) = a s + b s^3 + c s^5 (numpy's LAPACK SVD, not the oracle's matmuls).
-    Catches a dropped or sign-flipped polynomial term, X^T X in place of X X^T,
-    and a missing transpose for tall inputs."""
+    p(s) = a s + b s^3 + c s^5 (numpy's LAPACK SVD, not the oracle's matmuls),
+    for the default quintic and for triples with c = 0 and c < 0. Catches a
+    dropped or sign-flipped polynomial term, X^T X in place of X X^T, and a
+    missing transpose for tall inputs."""
     rng = np.random.default_rng(3)
     X = rng.standard_normal(shape)
     U, S, Vt = np.linalg.svd(X, full_matrices=False)
     sig = S / (np.linalg.norm(X) + O.NS_EPS)
-    expected = U @ np.diag([_ns_scalar(s, O.DEFAULT_NS_COEFFS, 5) for s in sig]) @ Vt
-    np.testing.assert_allclose(O.newton_schulz(X), expected, rtol=0, atol=1e-12)
+    cf = O.DEFAULT_NS_COEFFS if coeffs is None else coeffs
+    expected = U @ np.diag([_ns_scalar(s, cf, 5) for s in sig]) @ Vt
+    got = O.newton_schulz(X) if coeffs is None else O.newton_schulz(X, coeffs)
+    np.testing.assert_allclose(got, expected, rtol=0, atol=1e-12)
 
 
 def test_cubic_newton_schulz_reaches_polar_factor():
