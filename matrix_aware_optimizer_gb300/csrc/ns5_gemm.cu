@@ -198,7 +198,10 @@ __device__ __forceinline__ uint32_t stage_off(int row, int chunk) {
 // the bf16 X5 as the separate update pass would read it). Each 32 x 32 chunk
 // of X5 is staged in W's orientation (tall views transposed while staging),
 // so both orientations update W the same way: 8 W rows x 128 contiguous bytes
-// per instruction, each lane two float4 of one row. A warp loads the W values
+// per instruction, each lane two float4 of one row. W is read and written
+// with streaming (evict-first) hints, so that its 8 bytes per parameter do
+// not push the operand tiles other pairs still re-read out of L2 (about 1 %
+// off the update launches). A warp loads the W values
 // of its first two chunks while the accumulator is computed, and those of
 // chunk q + 2 right after using chunk q's, so each load has a whole chunk of
 // work to hide behind.
@@ -249,8 +252,8 @@ __device__ __forceinline__ void apply_load(const ApplyTarget& t, const ApplyBox&
     const int i = b.r0 + 8 * it + (lane >> 2);
     const float* row = t.dst + static_cast<int64_t>(i) * t.ld + j;
     if (i < b.R && t.vec && j + 8 <= b.C) {
-      const float4 a = *reinterpret_cast<const float4*>(row);
-      const float4 c = *reinterpret_cast<const float4*>(row + 4);
+      const float4 a = __ldcs(reinterpret_cast<const float4*>(row));  // read once: evict first
+      const float4 c = __ldcs(reinterpret_cast<const float4*>(row + 4));
       wv[8 * it + 0] = a.x;
       wv[8 * it + 1] = a.y;
       wv[8 * it + 2] = a.z;
@@ -287,8 +290,8 @@ __device__ __forceinline__ void apply_store(const GemmParams& p, const ApplyTarg
     }
     float* row = t.dst + static_cast<int64_t>(i) * t.ld + j;
     if (t.vec && j + 8 <= b.C) {
-      *reinterpret_cast<float4*>(row) = make_float4(o[0], o[1], o[2], o[3]);
-      *reinterpret_cast<float4*>(row + 4) = make_float4(o[4], o[5], o[6], o[7]);
+      __stcs(reinterpret_cast<float4*>(row), make_float4(o[0], o[1], o[2], o[3]));  // written once
+      __stcs(reinterpret_cast<float4*>(row + 4), make_float4(o[4], o[5], o[6], o[7]));
     } else {
 #pragma unroll
       for (int e = 0; e < 8; ++e)
