@@ -170,6 +170,7 @@ struct GemmEpilogue {
   float decay = 1.f, eta = 0.f;
   int* err = nullptr;     // device error word
   int num_sms = 0;
+  bool reverse = false;   // each segment's matrices last to first
 };
 
 constexpr int GEMM_MAX_SEGMENTS = 6;  // segments per launch (kernel parameter block within 4 KB)

@@ -23,7 +23,10 @@
 // GRAM writes P = b A + a I directly (bf16) and POLY is skipped.
 //
 // Each launch covers every matrix of a same-shape batch: the tile queue runs
-// over (matrix, tile) pairs, so small r x r products still fill the GPU.
+// over (matrix, tile) pairs, so small r x r products still fill the GPU. A
+// launch can visit each segment's matrices last to first (the engine
+// alternates, so that a launch starts where its predecessor's outputs are
+// still in L2); the results do not depend on the order.
 //
 // CTA pairs. The kernel runs in 2-CTA clusters, one CTA per SM; a pair owns a
 // 256 x 256 output tile and computes it with tcgen05.mma.cta_group::2
@@ -120,6 +123,8 @@ struct Segment {
   float gain, diag;     // GRAM / POLY: out = gain * (scale^2) * acc + diag * [i == j]
   float gain2;          // SEG_DUAL: gain of the second output
   const View* views;    // COMBINE: apply D to these views (by batch slot) instead of storing it
+  int batch;            // matrices of this segment
+  int reverse;          // visit the matrices last to first
 };
 
 struct GemmParams {
@@ -153,6 +158,7 @@ __device__ __forceinline__ TileCoord tile_coord(const Segment& p, int64_t tile) 
   TileCoord t;
   t.mat = static_cast<int>(tile / p.tiles_per_mat);
   const int local = static_cast<int>(tile - static_cast<int64_t>(t.mat) * p.tiles_per_mat);
+  if (p.reverse) t.mat = p.batch - 1 - t.mat;
   if (KIND == GEMM_COMBINE) {
     // m fastest: consecutive tiles share the same 256-column stripe of X.
     const int tm = local % p.tiles_m;
@@ -766,6 +772,8 @@ cudaError_t launch_gemm(GemmKind kind, const GemmSegSpec* specs, int count, cons
       sg.gain2 = g.gain2;
       sg.tile_begin = tiles;
       sg.out_z0 = g.out_z0;
+      sg.batch = g.batch;
+      sg.reverse = epi.reverse ? 1 : 0;
       if (kind == GEMM_COMBINE) {
         sg.M = static_cast<int>(g.r);
         sg.N = static_cast<int>(g.c);
