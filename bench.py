@@ -526,6 +526,20 @@ def run_leg(name, args, dev, stream, world, local, peaks, wl=None):
         out["block_step"] = blk
     else:
         out["rownorm"] = rownorm_summary(fam, hbm)
+        if ms.K > 1:
+            # vanilla Muon (K = 1: NS5 on every step) on the same state, K steps
+            # after one warm-up step, for the optimizer-time comparison
+            v0, v1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            opt.step(0, K=1, gamma=ms.gamma, lr=ms.lr, wd=ms.wd, beta=ms.beta, eps=ms.eps)
+            torch.cuda.synchronize()
+            v0.record(stream)
+            for k in range(ms.K):
+                opt.step(k, K=1, gamma=ms.gamma, lr=ms.lr, wd=ms.wd, beta=ms.beta, eps=ms.eps)
+            v1.record(stream)
+            torch.cuda.synchronize()
+            vm = max_over_ranks(v0.elapsed_time(v1), dev)
+            out["vanilla_muon"] = {"ms_per_3_steps": round(vm, 3),
+                                   "optimizer_time_reduction": round(1.0 - ms_cycle / vm, 4)}
     out["clocks"] = clk
     opt.sync_status()
     opt.close()
